@@ -1,0 +1,388 @@
+#!/usr/bin/env python3
+"""Benchmark of one DCP decode step (append -> partial attention on every
+virtual shard -> LSE merge) through the C ABI, on synthetic seeded inputs.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0). `value` is whole-job achieved HBM GB/s: the
+step's algorithmic bytes (KV read once, queries, partials written and read,
+output, appended rows) over the device-timed step, summed over ranks and
+divided by the slowest rank's time. With N > 1 each rank runs an independent
+replica of the workload (weak scaling; the shards of one step live in one
+GPU's memory, so nothing crosses GPUs). `--impl reference` times the float64
+CPU oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DCP decode attn: achieved HBM GB/s (% of GB300 peak); decode tokens/s per layer"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _workload_config(wl, st=None) -> dict:
+    cfg = {"workload": wl.name, "batch": wl.batch, "q_heads": wl.q_heads, "kv_heads": wl.kv_heads,
+           "head_dim_k": wl.dk, "head_dim_v": wl.dv, "block_size": wl.block_size, "shards": wl.shards,
+           "context": (f"{wl.ctx_fixed}+1" if wl.ctx_kind == "fixed"
+                       else f"lognormal(median {wl.median:g}, sigma {wl.sigma}) in [{wl.ctx_lo},{wl.ctx_hi}] +1"),
+           "fragmented_pools": wl.capacity_factor > 1.0,
+           "l2": "inputs larger than L2 (KV read per step >> 129 MB); no flush"}
+    if st is not None:
+        cfg["attended_tokens"] = st.attended_tokens()
+        cfg["kv_bytes_per_step"] = st.kv_bytes()
+    return cfg
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.15)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.06)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+        except Exception:
+            pass
+        finally:
+            if self.path and os.path.exists(self.path):
+                os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+def _traffic_for(kernel_file: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel is unchanged."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        ent = d[workload]
+        src = os.path.join(ROOT, "sequence_sharded_decode_gb300", "csrc", kernel_file)
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if ent.get("source_sha256_16") != h:
+            return None
+        return float(ent["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle leg (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+def oracle_prepare(wl, seqs):
+    """Generate (outside any timing) the bf16 inputs of the sampled sequences."""
+    import oracle as O
+    from sequence_sharded_decode_gb300 import configs, inputs
+
+    ctx = wl.ctx_lens()
+    starts = O.shard_starts(ctx, wl.shards)
+    data = []
+    for b in seqs:
+        L = int(ctx[b]) + 1
+        qs = inputs.STREAM_Q_MLA if wl.kind == configs.MLA else inputs.STREAM_Q
+        q = inputs.bf16_bits(inputs.query(wl.seed, [b], wl.q_heads, wl.dk, stream=qs))[0]
+        if wl.kind == configs.MLA:
+            kb = inputs.bf16_bits(inputs.sequence_kv(wl.seed, inputs.STREAM_LATENT, b, 0, L, 1, wl.dk))
+            vb = None
+        else:
+            kb = inputs.bf16_bits(inputs.sequence_kv(wl.seed, inputs.STREAM_K, b, 0, L, wl.kv_heads, wl.dk))
+            vb = inputs.bf16_bits(inputs.sequence_kv(wl.seed, inputs.STREAM_V, b, 0, L, wl.kv_heads, wl.dv))
+        data.append((b, L, q, kb, vb, starts[b]))
+    return data
+
+
+def oracle_pass(wl, data):
+    """One timed oracle pass (bf16 widening + per-shard partials + merge) over
+    the prepared sequences; returns (seconds, KV bytes covered)."""
+    import oracle as O
+
+    t0 = time.perf_counter()
+    nbytes = 0
+    for b, L, q, kb, vb, starts_b in data:
+        qf = O.bf16_bits_to_f64(q)
+        K = O.bf16_bits_to_f64(kb)
+        V = K[:, :, :wl.dv] if vb is None else O.bf16_bits_to_f64(vb)
+        O.sharded_attention(qf, K, V, wl.scale, starts_b, L)
+        nbytes += L * wl.kv_bytes_per_token
+    return time.perf_counter() - t0, nbytes
+
+
+def _cores() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+def oracle_sample(wl, seqs, budget_s: float):
+    """Oracle throughput over a bounded sample: repeat passes until budget_s."""
+    data = oracle_prepare(wl, seqs)
+    t_total, nbytes, runs = 0.0, 0, 0
+    while runs == 0 or t_total < budget_s:
+        t, n = oracle_pass(wl, data)
+        t_total += t
+        nbytes += n
+        runs += 1
+    desc = (f"sequence(s) {list(seqs)} of {wl.name} over their full contexts; {runs} oracle pass(es) of "
+            f"float64 per-shard partials + merge; input generation excluded")
+    return nbytes / t_total / 1e9, t_total, desc, _cores()
+
+
+def run_reference(args, wl):
+    """Reference arm: the float64 CPU oracle, K timed passes over one sampled
+    sequence of the workload after W untimed ones (rank 0 only)."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    seqs = [0]
+    data = oracle_prepare(wl, seqs)
+    times, nbytes = [], 0
+    for i in range(args.warmup + args.steps):
+        t, n = oracle_pass(wl, data)
+        if i >= args.warmup:
+            times.append(t)
+            nbytes = n
+    value = nbytes / float(np.mean(times)) / 1e9
+    desc = (f"sequence 0 of {wl.name} over its full context per step; float64 per-shard partials + merge; "
+            f"input generation excluded")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * float(np.mean(times)), 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": _workload_config(wl),
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": _cores(), "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# the CUDA path
+# ---------------------------------------------------------------------------
+def run_ours(args, wl):
+    import torch
+
+    from sequence_sharded_decode_gb300 import dcp
+    from sequence_sharded_decode_gb300.state import DecodeState
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dcp.load()
+    st = DecodeState(wl, device=f"cuda:{local}")
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    bytes_ = st.step_bytes()
+    step_bytes = sum(bytes_.values())
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            st.step(stream)
+    barrier()
+    K = args.steps
+    ev_p0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_p1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for i in range(K):
+                st.append(stream)
+                ev_p0[i].record(stream)
+                st.partial(stream)
+                ev_p1[i].record(stream)
+                st.merge(stream)
+            end.record(stream)
+        stream.synchronize()
+    barrier()
+    clocks = clk.summary()
+    ms = start.elapsed_time(end) / K
+    partial_ms = sum(a.elapsed_time(b) for a, b in zip(ev_p0, ev_p1)) / K
+    err = int(st.err.item())
+    if err:
+        raise RuntimeError(f"device error flag set: {err}")
+
+    # end to end through the public API: host (pinned) inputs in, result out
+    h_q = st.q.cpu().pin_memory()
+    h_k = st.k_new.cpu().pin_memory()
+    h_v = st.v_new.cpu().pin_memory() if st.v_new is not None else None
+    h_pos = st.positions.cpu().pin_memory()
+    h_len = st.seq_lens.cpu().pin_memory()
+    h_o = torch.empty(st.o.shape, dtype=torch.float32).pin_memory()
+    h_lse = torch.empty(st.lse.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_pos, h_len) if t is not None)
+    d2h = h_o.numel() * 4 + h_lse.numel() * 4
+
+    def e2e_step():
+        st.q.copy_(h_q, non_blocking=True)
+        st.k_new.copy_(h_k, non_blocking=True)
+        if h_v is not None:
+            st.v_new.copy_(h_v, non_blocking=True)
+        st.positions.copy_(h_pos, non_blocking=True)
+        st.seq_lens.copy_(h_len, non_blocking=True)
+        st.step(stream)
+        h_o.copy_(st.o, non_blocking=True)
+        h_lse.copy_(st.lse, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(K):
+            e2e_step()
+        e1.record(stream)
+    stream.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / K
+
+    # max over ranks
+    vals = torch.tensor([ms, partial_ms, e2e_ms], dtype=torch.float64, device=f"cuda:{local}")
+    if dist is not None:
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    ms, partial_ms, e2e_ms = (float(x) for x in vals.cpu())
+
+    if rank == 0:
+        peak, peak_kind = _peaks()
+        value = world * step_bytes / (ms * 1e-3) / 1e9
+        achieved = bytes_["partial"] / (partial_ms * 1e-3) / 1e9
+        kern = "dcp_mla.cu" if wl.kind == 1 else "dcp_gqa.cu"
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": _workload_config(wl, st) | {"parallelism": f"replicas x{world}"},
+            "hbm_frac_of_peak": round(value / world / peak, 4),
+            "tokens_per_s_per_layer": round(world * wl.batch / (ms * 1e-3), 1),
+            "roofline": {"bound": "hbm", "kernel": "dcp_decode_partial_all (plan + attention + combine)",
+                         "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "traffic": _traffic_for(kern, wl.name),
+                         "algorithmic_bytes_per_launch": bytes_["partial"]},
+            "step_bytes": bytes_,
+            "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 5 * K,
+            "clocks": clocks,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            gbs, secs, desc, cores = oracle_sample(wl, [0, min(1, wl.batch - 1)] if wl.batch > 1 else [0],
+                                                   args.cpu_seconds)
+            line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                    "sample": desc, "seconds": round(secs, 2)}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gqa_mid")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None, help="override the preset's batch (profiling cases)")
+    ap.add_argument("--shards", type=int, default=None, help="override the preset's shard count")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from sequence_sharded_decode_gb300 import configs
+    wl = configs.get(args.workload)
+    if args.batch is not None:
+        wl = wl.with_(batch=args.batch)
+    if args.shards is not None:
+        wl = wl.with_(shards=args.shards)
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,195 @@
+/*
+ * dcp.h -- C ABI of libdcp: decode-time context parallelism (DCP) on one GPU.
+ *
+ * The method (Qiita write-up "vLLMの-dcpが長文脈のKVキャッシュ重複を消して3倍速くする",
+ * section "トークンの区間でGPUに割り振る"; "Inference Systems Infrastructure
+ * Notes (7): DCP", sections 2 and 3): the KV cache of every sequence is split
+ * along the token axis into N contiguous ranges (shards). Each shard attends
+ * the one-token decode query against its own slice only and emits a partial
+ * output plus its log-sum-exp (LSE); the partials are then combined by
+ * online-softmax reweighting into the exact full-context attention. Here the
+ * N shards are virtual: N paged KV pools in the memory of one GPU, and the
+ * cross-GPU gather/reduce-scatter becomes an on-device merge that reads one
+ * caller-owned scratch buffer reused every step.
+ *
+ * Conventions for every entry point below:
+ *  - Ownership: the caller allocates and frees every buffer. The library
+ *    allocates no memory, keeps no per-call state and is re-entrant; the only
+ *    global state is a per-device cache of launch limits (SM count, opt-in
+ *    shared memory), filled on first use.
+ *  - Pointers documented "device" must point to memory of the current CUDA
+ *    device; "host" pointers to host memory. Arrays are dense, row-major,
+ *    in the stated shape.
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *    default stream). All work is enqueued on it; nothing synchronises.
+ *  - Errors: arguments are validated on the host before any launch and a
+ *    negative dcp_status is returned without touching the GPU. A failed launch
+ *    returns DCP_ERR_CUDA. Inside kernels, a block-table entry outside
+ *    [0, num_blocks), a logical block beyond max_blocks_per_seq or a position
+ *    before shard 0 OR a DCP_DEVERR_* bit into *dev_err_flag (when the pointer
+ *    is non-NULL) and skips that access; the caller reads the flag after the
+ *    stream is synchronised and clears it itself.
+ *  - Data types: KV, queries and appended tokens are bf16 (raw 16-bit
+ *    patterns); outputs and partials are fp32; LSE is the natural logarithm.
+ */
+#ifndef DCP_H_
+#define DCP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DCP_API __attribute__((visibility("default")))
+#else
+#define DCP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DCP_OK = 0,
+  DCP_ERR_INVALID_ARG = -1, /* NULL where a pointer is required, bad count  */
+  DCP_ERR_SHAPE = -2,       /* inconsistent sizes in the descriptor/shards   */
+  DCP_ERR_UNSUPPORTED = -3, /* valid but not implemented (e.g. head_dim 96) */
+  DCP_ERR_CUDA = -4,        /* a CUDA call or launch failed                  */
+  DCP_ERR_WORKSPACE = -5    /* workspace NULL, misaligned or too small       */
+} dcp_status;
+
+/* Bits OR'ed into *dev_err_flag by kernels. */
+#define DCP_DEVERR_BLOCK_RANGE 1 /* table entry < 0 or >= num_blocks            */
+#define DCP_DEVERR_TABLE_RANGE 2 /* logical block >= max_blocks_per_seq        */
+#define DCP_DEVERR_POSITION 4    /* position < 0 or before the first shard     */
+#define DCP_DEVERR_TIMEOUT 8     /* a bounded on-device wait gave up            */
+
+#define DCP_MAX_SHARDS 32
+
+typedef enum { DCP_KIND_GQA = 0, DCP_KIND_MLA = 1 } dcp_kind;
+
+/* Shape of one attention layer's decode step.
+ *  GQA: query head h reads KV head h / (num_q_heads / num_kv_heads);
+ *       head_dim_k == head_dim_v in {64, 128}; block_size a multiple of 16.
+ *  MLA (absorbed): num_kv_heads == 1; the cached row is the latent of width
+ *       head_dim_k (576); the key is the whole row and the value is its first
+ *       head_dim_v (512) entries; block_size == 64.
+ *  scale multiplies q.k before the softmax (e.g. 1/sqrt(head_dim_k)). */
+typedef struct {
+  int kind;          /* dcp_kind */
+  int num_q_heads;
+  int num_kv_heads;
+  int head_dim_k;
+  int head_dim_v;
+  int block_size;    /* tokens per paged block */
+  float scale;
+} dcp_attn_desc;
+
+/* One shard's paged KV pool and block table (all device memory).
+ *  GQA: k_pool [num_blocks, num_kv_heads, block_size, head_dim_k] bf16,
+ *       v_pool [num_blocks, num_kv_heads, block_size, head_dim_v] bf16.
+ *  MLA: k_pool [num_blocks, block_size, head_dim_k] bf16, v_pool NULL.
+ *  block_table: int32 [B, max_blocks_per_seq]; row b maps the shard-local
+ *  logical block index (local position / block_size) of sequence b to a
+ *  physical block of this pool. Pools must be 16-byte aligned. */
+typedef struct {
+  void* k_pool;
+  void* v_pool;
+  int64_t num_blocks;
+  const int32_t* block_table;
+  int32_t max_blocks_per_seq;
+} dcp_shard;
+
+/* Human-readable text for a dcp_status value (static storage). */
+DCP_API const char* dcp_status_string(int status);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+DCP_API int dcp_version(void);
+
+/* Routing plan on the host (step 1 of the method: contiguous token ranges).
+ * For each sequence b with ctx_lens[b] tokens before decoding, the chunk is
+ * C = max(1, ceil(ctx_lens[b] / N)); shard i starts at global position i*C;
+ * shard i < N-1 owns [i*C, (i+1)*C) and the last shard is open-ended, so
+ * appended decode tokens land there once the earlier shards are full.
+ *   ctx_lens      host int32 [B], each >= 0
+ *   shard_starts  host int32 [B, N] (out): i*C
+ *   blocks_needed host int32 [B, N] (out, may be NULL): paged blocks shard i
+ *                 needs to hold sequence b's tokens in [0, ctx_lens[b] +
+ *                 reserve_tokens): ceil(tokens_in_shard / block_size).
+ * Returns DCP_ERR_INVALID_ARG for N outside [1, DCP_MAX_SHARDS], B < 0,
+ * block_size < 1, reserve_tokens < 0, a negative length, NULL outputs, or a
+ * position that would not fit in int32. */
+DCP_API int dcp_shard_plan(const int32_t* ctx_lens, int B, int N, int block_size, int reserve_tokens,
+                   int32_t* shard_starts, int32_t* blocks_needed);
+
+/* Write T tokens' K/V into the owning shards' paged pools (the per-step KV
+ * append of decoding; with many tokens it also fills pools from a prefill).
+ * Token j belongs to sequence seq_ids[j] (or to sequence j when seq_ids is
+ * NULL, which requires T == B) at global position positions[j]. Its owner is
+ * the last shard i with shard_starts[b, i] <= position; the local position
+ * p = position - shard_starts[b, i] selects logical block p / block_size and
+ * slot p % block_size, and the block table gives the physical block.
+ *   shards        host array of N dcp_shard (device pools/tables)
+ *   shard_starts  device int32 [B, N] (from dcp_shard_plan)
+ *   seq_ids       device int32 [T] or NULL;   positions device int32 [T]
+ *   k_new         device bf16: GQA [T, num_kv_heads, head_dim_k]; MLA [T, head_dim_k]
+ *   v_new         device bf16: GQA [T, num_kv_heads, head_dim_v]; MLA NULL
+ * Bytes are copied as they are (bit-exact). T == 0 is a no-op. */
+DCP_API int dcp_kv_append(const dcp_attn_desc* desc, const dcp_shard* shards, int N,
+                  const int32_t* shard_starts, int B, const int32_t* seq_ids,
+                  const int32_t* positions, const void* k_new, const void* v_new, int T,
+                  int32_t* dev_err_flag, void* stream);
+
+/* Bytes of workspace dcp_decode_partial / dcp_decode_partial_all need for up
+ * to B sequences and N shards with this descriptor (0 on invalid input). The
+ * workspace holds the work list and the split-KV temporaries; it is reused
+ * by every call (no per-step allocation) and must be 256-byte aligned. */
+DCP_API size_t dcp_workspace_size(const dcp_attn_desc* desc, int B, int N);
+
+/* Step 2 of the method for one shard: partial decode attention of every
+ * sequence's one-token query against the tokens this shard holds.
+ * For sequence b and query head h, over global positions t in
+ * [shard_range[b,0], min(shard_range[b,1], seq_lens[b])):
+ *   s_t = scale * <q[b,h], k_t>,  m = max s_t,  l = sum exp(s_t - m),
+ *   o_part[b,h] = sum exp(s_t - m) v_t / l,  lse[b,h] = m + ln l.
+ * A sequence with no token in range gets o_part = 0 and lse = -inf.
+ *   q          device bf16 [B, num_q_heads, head_dim_k]
+ *   shard      host pointer to one dcp_shard
+ *   seq_lens   device int32 [B], global lengths including appended tokens
+ *   shard_range device int32 [B, 2], global [start, end) of this shard
+ *              (start is the shard's first position: local position 0)
+ *   o_part     device fp32 [B, num_q_heads, head_dim_v] (out)
+ *   lse        device fp32 [B, num_q_heads] (out)
+ *   workspace  device, >= dcp_workspace_size(desc, B, 1) bytes            */
+DCP_API int dcp_decode_partial(const dcp_attn_desc* desc, const void* q, const dcp_shard* shard,
+                       const int32_t* seq_lens, const int32_t* shard_range, int B,
+                       float* o_part, float* lse, void* workspace, size_t ws_bytes,
+                       int32_t* dev_err_flag, void* stream);
+
+/* Step 2 for all N shards in one pass of launches. Shard i of sequence b
+ * covers [shard_starts[b,i], shard_starts[b,i+1]) (the last shard up to
+ * seq_lens[b]), clipped to seq_lens[b].
+ *   o_parts device fp32 [N, B, num_q_heads, head_dim_v] (out)
+ *   lses    device fp32 [N, B, num_q_heads] (out)
+ *   workspace >= dcp_workspace_size(desc, B, N) bytes                      */
+DCP_API int dcp_decode_partial_all(const dcp_attn_desc* desc, const void* q, const dcp_shard* shards,
+                           int N, const int32_t* seq_lens, const int32_t* shard_starts, int B,
+                           float* o_parts, float* lses, void* workspace, size_t ws_bytes,
+                           int32_t* dev_err_flag, void* stream);
+
+/* Step 3 of the method: combine N partials by LSE reweighting
+ * ("Inference Systems Infrastructure Notes (7): DCP", section 2; the Qiita
+ * section "トークンの区間でGPUに割り振る", third step). For every row r:
+ *   M = max_i lses[i,r],  w_i = exp(lses[i,r] - M),
+ *   o[r] = sum_i w_i o_parts[i,r] / sum_i w_i,  lse_out[r] = M + ln sum_i w_i;
+ * rows whose partials are all empty (LSE -inf) give o = 0, lse_out = -inf.
+ *   o_parts device fp32 [N, B, Hq, Dv]; lses device fp32 [N, B, Hq]
+ *   o       device fp32 [B, Hq, Dv] (out); lse_out device fp32 [B, Hq] or NULL
+ * Dv must be a multiple of 4 and the pointers 16-byte aligned. */
+DCP_API int dcp_merge(const float* o_parts, const float* lses, int N, int B, int Hq, int Dv, float* o,
+              float* lse_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DCP_H_ */

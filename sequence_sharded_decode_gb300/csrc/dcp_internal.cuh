@@ -1,0 +1,121 @@
+// Internal declarations shared by the libdcp translation units.
+//
+// Work decomposition (all kernels): a *lane* is one independent softmax
+// problem over a token range -- (shard, sequence, KV head, head group) for GQA,
+// (shard, sequence) for MLA. Lanes are cut into tiles of TILE tokens. The
+// plan kernel lays every lane's tiles end to end and gives each persistent
+// CTA (or CTA pair) an equal, contiguous run of tiles, so work is balanced to
+// one tile whatever the length mix. A CTA's run crosses at most a few lane
+// boundaries; each piece of a lane it touches is an *item*. A lane covered by
+// one item is written straight to the shard's partial output; a lane split
+// over several items is written as per-item partials to the workspace and
+// merged by the combine kernel (same LSE merge as across shards).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dcp.h"
+
+namespace dcp {
+
+constexpr int kMaxShards = DCP_MAX_SHARDS;
+
+// Shard descriptors passed by value as a kernel parameter.
+struct ShardSet {
+  const void* k[kMaxShards];
+  const void* v[kMaxShards];
+  const int32_t* table[kMaxShards];
+  int64_t nblk[kMaxShards];
+  int32_t max_blocks[kMaxShards];
+};
+
+// How a lane's token range is found: unit u = shard * B + b.
+//   mode 0 (all shards): [starts[b*N+i], i<N-1 ? starts[b*N+i+1] : inf) clipped to seq_lens[b]
+//   mode 1 (one shard) : [range[2b], range[2b+1]) clipped to seq_lens[b]
+struct RangeSpec {
+  const int32_t* seq_lens;
+  const int32_t* starts;  // mode 0
+  const int32_t* range;   // mode 1
+  int32_t* err;           // device error flags (may be NULL)
+  int mode;
+  int B;
+  int N;
+};
+
+struct LaneRec {     // 32 bytes
+  int lo;            // first global position attended
+  int hi;            // one past the last
+  int start;         // global position of local position 0 (shard start)
+  int tiles;         // ceil((hi - lo) / TILE)
+  int item_begin;
+  int n_items;
+  int tmp_begin;     // first workspace partial row if n_items > 1
+  int pad;
+};
+
+struct ItemRec {     // 16 bytes
+  int lane;
+  int t0;            // tile range [t0, t1) within the lane
+  int t1;
+  int out_row;       // >= 0: workspace partial row; -1: write the lane's output directly
+};
+
+struct WsHeader {
+  int n_items;
+  int n_lanes;
+  int n_ctas;
+  int total_tiles;
+  int pad[60];       // 256 bytes
+};
+
+struct WsLayout {
+  size_t lanes_off, items_off, cta_off, tmp_o_off, tmp_lse_off, total;
+  int max_lanes, max_items, max_ctas, max_tmp, rows_per_lane;
+};
+
+// Workspace layout for n_lanes lanes, up to max_ctas work CTAs, rows_per_lane
+// query heads per lane and dv-wide outputs.
+WsLayout ws_layout(int n_lanes, int max_ctas, int rows_per_lane, int dv);
+
+// Per-device launch facts (cached).
+struct DeviceInfo {
+  int sm_count;
+  int max_smem_optin;
+};
+int device_info(DeviceInfo* out);
+
+// Lane geometry of a descriptor.
+struct LaneGeom {
+  int heads_per_lane;  // query heads of one lane
+  int groups;          // lanes per (unit, kv head) for GQA (g > 16 -> several)
+  int lanes_per_unit;  // kv_heads * groups (GQA) or 1 (MLA)
+  int tile;            // tokens per tile
+};
+LaneGeom lane_geom(const dcp_attn_desc& d);
+
+// Kernel launchers (return the launch's cudaError_t).
+cudaError_t launch_plan(const RangeSpec& rs, int lanes_per_unit, int tile, int n_ctas,
+                        void* ws, const WsLayout& L, cudaStream_t st);
+cudaError_t launch_gqa(const dcp_attn_desc& d, const void* q, const ShardSet& sh, const RangeSpec& rs,
+                       float* o_parts, float* lses, void* ws, const WsLayout& L, int n_ctas,
+                       int32_t* err, cudaStream_t st);
+int gqa_ctas(const dcp_attn_desc& d, const DeviceInfo& di);
+cudaError_t launch_mla(const dcp_attn_desc& d, const void* q, const ShardSet& sh, const RangeSpec& rs,
+                       float* o_parts, float* lses, void* ws, const WsLayout& L, int n_ctas,
+                       int32_t* err, cudaStream_t st);
+int mla_ctas(const dcp_attn_desc& d, const DeviceInfo& di);
+cudaError_t launch_combine(const dcp_attn_desc& d, int B, int n_lanes, const void* ws, const WsLayout& L,
+                           float* o_parts, float* lses, cudaStream_t st);
+cudaError_t launch_merge(const float* o_parts, const float* lses, int N, int rows, int dv, float* o,
+                         float* lse_out, cudaStream_t st);
+cudaError_t launch_append(const dcp_attn_desc& d, const ShardSet& sh, int N, const int32_t* starts,
+                          int B, const int32_t* seq_ids, const int32_t* positions, const void* k_new,
+                          const void* v_new, int T, int32_t* err, cudaStream_t st);
+
+// Device helpers ------------------------------------------------------------
+__device__ __forceinline__ void raise_flag(int32_t* err, int bit) {
+  if (err) atomicOr(err, bit);
+}
+
+}  // namespace dcp

@@ -1,0 +1,142 @@
+// LSE merge of partial attention results (step 3 of the method: the partial
+// outputs of the shards are combined by online-softmax reweighting into the
+// exact full-context attention -- Qiita write-up "vLLMの-dcpが長文脈のKV
+// キャッシュ重複を消して3倍速くする", section "トークンの区間でGPUに割り振る";
+// "Inference Systems Infrastructure Notes (7): DCP", sections 2-3).
+//
+// For every output row r (a (sequence, query head) pair) and partials i:
+//   M = max_i lse_i,  w_i = exp(lse_i - M),
+//   O = sum_i w_i O_i / sum_i w_i,  lse = M + ln sum_i w_i,
+// an all-empty row (every lse_i = -inf) gives O = 0, lse = -inf.
+//
+// The same arithmetic serves two places: dcp_merge combines the N shard
+// partials held in the caller's scratch buffer, and the combine kernel joins
+// the pieces of a lane that the balanced split cut across several CTAs. Both
+// stream fp32 rows with 16-byte loads: HBM-bound.
+#include <cmath>
+
+#include "dcp_internal.cuh"
+
+namespace dcp {
+namespace {
+
+constexpr int kMergeThreads = 256;
+
+// One warp per row: lane i < N reads lse_i; the weights are broadcast by
+// shuffles; the row's Dv/4 float4 columns are spread over the lanes.
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __restrict__ o_parts,
+                                                              const float* __restrict__ lses, int N,
+                                                              long long rows, int dv4, float* __restrict__ o,
+                                                              float* __restrict__ lse_out) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * (kMergeThreads / 32);
+  for (long long r = (long long)blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5); r < rows; r += warps) {
+    float M = -INFINITY;
+    for (int i = lane; i < N; i += 32) M = fmaxf(M, lses[(long long)i * rows + r]);
+    for (int s = 16; s > 0; s >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, s));
+    const float4* src = reinterpret_cast<const float4*>(o_parts);
+    float4* dst = reinterpret_cast<float4*>(o) + r * dv4;
+    if (M == -INFINITY) {
+      for (int c = lane; c < dv4; c += 32) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (lse_out && lane == 0) lse_out[r] = -INFINITY;
+      continue;
+    }
+    float wsum = 0.f;
+    for (int i = lane; i < N; i += 32) {
+      const float li = lses[(long long)i * rows + r];
+      wsum += li == -INFINITY ? 0.f : expf(li - M);
+    }
+    for (int s = 16; s > 0; s >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, s);
+    const float inv = 1.f / wsum;
+    for (int c = lane; c < dv4; c += 32) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i = 0; i < N; ++i) {
+        const float li = lses[(long long)i * rows + r];
+        if (li == -INFINITY) continue;
+        const float w = expf(li - M);
+        const float4 v = src[((long long)i * rows + r) * dv4 + c];
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        acc.z += w * v.z;
+        acc.w += w * v.w;
+      }
+      acc.x *= inv;
+      acc.y *= inv;
+      acc.z *= inv;
+      acc.w *= inv;
+      dst[c] = acc;
+    }
+    if (lse_out && lane == 0) lse_out[r] = M + logf(wsum);
+  }
+}
+
+// Joins the items of split lanes (workspace partial rows) into the lane's
+// output rows; writes O = 0, LSE = -inf for lanes with no tokens at all.
+__global__ void __launch_bounds__(kMergeThreads) combine_kernel(const char* __restrict__ ws, WsLayout L,
+                                                                int B, int Hq, int dv, int lanes_per_unit,
+                                                                int heads_per_lane, int groups, int g,
+                                                                float* __restrict__ o_parts,
+                                                                float* __restrict__ lses) {
+  const int lane_id = blockIdx.x;
+  const LaneRec ln = reinterpret_cast<const LaneRec*>(ws + L.lanes_off)[lane_id];
+  if (ln.n_items == 1) return;
+  const float* tmp_o = reinterpret_cast<const float*>(ws + L.tmp_o_off);
+  const float* tmp_lse = reinterpret_cast<const float*>(ws + L.tmp_lse_off);
+  const int u = lane_id / lanes_per_unit, j = lane_id - u * lanes_per_unit;
+  int head0, nheads;
+  if (groups > 0) {  // GQA lane = (unit, kv head, head group)
+    const int kvh = j / groups, hg = j - kvh * groups;
+    head0 = kvh * g + hg * heads_per_lane;
+    nheads = min(heads_per_lane, g - hg * heads_per_lane);
+  } else {
+    head0 = 0;
+    nheads = Hq;
+  }
+  float* out_o = o_parts + ((size_t)u * Hq + head0) * dv;
+  float* out_l = lses + (size_t)u * Hq + head0;
+  const int rpl = L.rows_per_lane;
+  for (int idx = threadIdx.x; idx < nheads * dv; idx += kMergeThreads) {
+    const int r = idx / dv, c = idx - r * dv;
+    float M = -INFINITY;
+    for (int i = 0; i < ln.n_items; ++i) M = fmaxf(M, tmp_lse[(size_t)(ln.tmp_begin + i) * rpl + r]);
+    float num = 0.f, den = 0.f;
+    if (M != -INFINITY) {
+      for (int i = 0; i < ln.n_items; ++i) {
+        const float li = tmp_lse[(size_t)(ln.tmp_begin + i) * rpl + r];
+        if (li == -INFINITY) continue;
+        const float w = expf(li - M);
+        num += w * tmp_o[((size_t)(ln.tmp_begin + i) * rpl + r) * dv + c];
+        den += w;
+      }
+    }
+    out_o[(size_t)r * dv + c] = den > 0.f ? num / den : 0.f;
+    if (c == 0) out_l[r] = den > 0.f ? M + logf(den) : -INFINITY;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const float* o_parts, const float* lses, int N, int rows, int dv, float* o,
+                         float* lse_out, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  DeviceInfo di;
+  if (device_info(&di) != 0) return cudaErrorUnknown;
+  const long long want = ((long long)rows + kMergeThreads / 32 - 1) / (kMergeThreads / 32);
+  const int grid = (int)(want < di.sm_count * 16LL ? want : di.sm_count * 16LL);
+  merge_kernel<<<grid, kMergeThreads, 0, st>>>(o_parts, lses, N, rows, dv / 4, o, lse_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const dcp_attn_desc& d, int B, int n_lanes, const void* ws, const WsLayout& L,
+                           float* o_parts, float* lses, cudaStream_t st) {
+  if (n_lanes <= 0) return cudaSuccess;
+  const LaneGeom lg = lane_geom(d);
+  const int groups = d.kind == DCP_KIND_GQA ? lg.groups : 0;
+  const int g = d.num_q_heads / d.num_kv_heads;
+  combine_kernel<<<n_lanes, kMergeThreads, 0, st>>>(static_cast<const char*>(ws), L, B, d.num_q_heads,
+                                                     d.head_dim_v, lg.lanes_per_unit, lg.heads_per_lane,
+                                                     groups, g, o_parts, lses);
+  return cudaGetLastError();
+}
+
+}  // namespace dcp

@@ -1,0 +1,191 @@
+// Work planning on the device: lanes, tiles and the balanced split over CTAs.
+//
+// One CTA of 1024 threads reads the per-sequence lengths and shard ranges
+// (device memory, so the host never synchronises), and writes into the
+// workspace:
+//   lanes[l]   token range, tile count, and the items covering the lane
+//   items[k]   (lane, tile range, output row) in lane order
+//   cta_begin  CTA c processes items [cta_begin[c], cta_begin[c+1])
+// CTA c's tiles are [c*T/S, (c+1)*T/S) of the T tiles laid end to end, so the
+// CTAs' loads differ by at most one tile.
+#include <climits>
+
+#include "dcp_internal.cuh"
+
+namespace dcp {
+namespace {
+
+constexpr int kPlanThreads = 1024;
+
+struct Scan2 {
+  long long a, b;
+};
+
+// Block-wide exclusive scan of two int64 values per thread; returns the
+// exclusive prefix for this thread and writes the block totals.
+__device__ Scan2 block_exclusive_scan2(Scan2 v, Scan2* totals) {
+  __shared__ long long sa[32], sb[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long ia = v.a, ib = v.b;
+  for (int o = 1; o < 32; o <<= 1) {
+    long long ta = __shfl_up_sync(0xffffffffu, ia, o);
+    long long tb = __shfl_up_sync(0xffffffffu, ib, o);
+    if (lane >= o) { ia += ta; ib += tb; }
+  }
+  if (lane == 31) { sa[warp] = ia; sb[warp] = ib; }
+  __syncthreads();
+  if (warp == 0) {
+    long long wa = sa[lane], wb = sb[lane];
+    for (int o = 1; o < 32; o <<= 1) {
+      long long ta = __shfl_up_sync(0xffffffffu, wa, o);
+      long long tb = __shfl_up_sync(0xffffffffu, wb, o);
+      if (lane >= o) { wa += ta; wb += tb; }
+    }
+    sa[lane] = wa;
+    sb[lane] = wb;
+  }
+  __syncthreads();
+  Scan2 r;
+  const long long pa = warp ? sa[warp - 1] : 0, pb = warp ? sb[warp - 1] : 0;
+  r.a = pa + ia - v.a;
+  r.b = pb + ib - v.b;
+  totals->a = sa[31];
+  totals->b = sb[31];
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ void unit_range(const RangeSpec& rs, int u, int* lo, int* hi, int* start) {
+  const int i = u / rs.B, b = u - i * rs.B;
+  int L = rs.seq_lens[b];
+  if (L < 0) L = 0;
+  int s, e;
+  if (rs.mode == 0) {
+    s = rs.starts[b * rs.N + i];
+    e = (i + 1 < rs.N) ? rs.starts[b * rs.N + i + 1] : INT_MAX;
+  } else {
+    s = rs.range[2 * b];
+    e = rs.range[2 * b + 1];
+  }
+  if (s < 0) {  // a shard cannot start before position 0: flag it, attend nothing
+    raise_flag(rs.err, DCP_DEVERR_POSITION);
+    s = 0;
+    e = 0;
+  }
+  int l = s;
+  if (l > L) l = L;
+  int h = e < L ? e : L;
+  if (h < l) h = l;
+  *lo = l;
+  *hi = h;
+  *start = s;
+}
+
+// CTA that owns flattened tile x: the largest c with floor(c*T/S) <= x.
+__device__ __forceinline__ int cta_of(long long x, long long T, long long S) {
+  return (int)(((x + 1) * S - 1) / T);
+}
+__device__ __forceinline__ long long cta_start(long long c, long long T, long long S) {
+  return c * T / S;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(RangeSpec rs, int lanes_per_unit, int tile,
+                                                            int n_ctas, char* ws, WsLayout L) {
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  LaneRec* lanes = reinterpret_cast<LaneRec*>(ws + L.lanes_off);
+  ItemRec* items = reinterpret_cast<ItemRec*>(ws + L.items_off);
+  int* cta_begin = reinterpret_cast<int*>(ws + L.cta_off);
+
+  const int n_lanes = rs.B * rs.N * lanes_per_unit;
+  const int per = (n_lanes + kPlanThreads - 1) / kPlanThreads;
+  const int l0 = threadIdx.x * per;
+  const int l1 = min(n_lanes, l0 + per);
+
+  // pass 1: ranges and tile counts
+  long long my_tiles = 0;
+  for (int l = l0; l < l1; ++l) {
+    int lo, hi, start;
+    unit_range(rs, l / lanes_per_unit, &lo, &hi, &start);
+    LaneRec r;
+    r.lo = lo;
+    r.hi = hi;
+    r.start = start;
+    r.tiles = (hi - lo + tile - 1) / tile;
+    r.item_begin = 0;
+    r.n_items = 0;
+    r.tmp_begin = 0;
+    r.pad = 0;
+    lanes[l] = r;
+    my_tiles += r.tiles;
+  }
+  Scan2 tot;
+  Scan2 pre = block_exclusive_scan2(Scan2{my_tiles, 0}, &tot);
+  const long long T = tot.a;
+  // With fewer tiles than CTAs only the first T CTAs get work, so that no
+  // CTA's run is empty and every item covers at least one tile.
+  const long long S = T < n_ctas ? (T > 0 ? T : 1) : n_ctas;
+
+  // pass 2: items per lane (number of CTA runs the lane overlaps)
+  long long p = pre.a, my_items = 0, my_split = 0;
+  for (int l = l0; l < l1; ++l) {
+    const int t = lanes[l].tiles;
+    int n = 0;
+    if (t > 0) n = cta_of(p + t - 1, T, S) - cta_of(p, T, S) + 1;
+    lanes[l].n_items = n;
+    lanes[l].pad = (int)p;  // tile prefix, used in pass 3
+    my_items += n;
+    if (n > 1) my_split += n;
+    p += t;
+  }
+  Scan2 tot2;
+  Scan2 pre2 = block_exclusive_scan2(Scan2{my_items, my_split}, &tot2);
+
+  // pass 3: items
+  long long ib = pre2.a, tb = pre2.b;
+  for (int l = l0; l < l1; ++l) {
+    LaneRec r = lanes[l];
+    const long long P = r.pad;
+    r.item_begin = (int)ib;
+    r.tmp_begin = (int)tb;
+    r.pad = 0;
+    lanes[l] = r;
+    if (r.n_items > 0) {
+      const int c0 = cta_of(P, T, S);
+      for (int j = 0; j < r.n_items; ++j) {
+        const int c = c0 + j;
+        const long long cs = cta_start(c, T, S), ce = cta_start(c + 1, T, S);
+        const long long a = cs > P ? cs : P;
+        const long long e = ce < P + r.tiles ? ce : P + r.tiles;
+        ItemRec it;
+        it.lane = l;
+        it.t0 = (int)(a - P);
+        it.t1 = (int)(e - P);
+        it.out_row = r.n_items > 1 ? (int)(tb + j) : -1;
+        items[ib + j] = it;
+        if (a == cs) cta_begin[c] = (int)(ib + j);  // first item of CTA c
+      }
+    }
+    ib += r.n_items;
+    if (r.n_items > 1) tb += r.n_items;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int n_items = (int)tot2.a;
+    // CTAs past the last run (T < n_ctas, or no tiles at all) get no items
+    for (int c = (T > 0 ? (int)S : 0); c <= n_ctas; ++c) cta_begin[c] = n_items;
+    hdr->n_items = n_items;
+    hdr->n_lanes = n_lanes;
+    hdr->n_ctas = n_ctas;
+    hdr->total_tiles = (int)T;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const RangeSpec& rs, int lanes_per_unit, int tile, int n_ctas, void* ws,
+                        const WsLayout& L, cudaStream_t st) {
+  plan_kernel<<<1, kPlanThreads, 0, st>>>(rs, lanes_per_unit, tile, n_ctas, static_cast<char*>(ws), L);
+  return cudaGetLastError();
+}
+
+}  // namespace dcp

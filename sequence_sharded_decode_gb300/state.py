@@ -1,0 +1,118 @@
+"""Device state of one decode step for a workload preset.
+
+Allocates the N shard pools, block tables, queries, the step's new tokens,
+the reused workspace and the output buffers with torch, fills the pools
+through dcp_kv_append, and runs one step through the C ABI:
+append -> partial attention on every shard -> LSE merge.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import configs, dcp, inputs
+
+
+class DecodeState:
+    def __init__(self, wl: configs.Workload, device: str = "cuda", fill: bool = True,
+                 canary: int | None = None, table_seed: int | None = None, fill_chunk: int = 1 << 18):
+        self.wl = wl
+        self.device = device
+        self.ctx = wl.ctx_lens().astype(np.int64)
+        B, N = wl.batch, wl.shards
+        self.desc = dcp.AttnDesc(wl.kind, wl.q_heads, wl.kv_heads, wl.dk, wl.dv, wl.block_size, wl.scale)
+        starts, blocks = dcp.dcp_shard_plan(self.ctx, N, wl.block_size, 1)
+        self.starts_host, self.blocks_host = starts, blocks
+        seed_t = wl.seed + 1 if table_seed is None else table_seed
+        self.tables_host = inputs.block_tables(seed_t, blocks, wl.capacity_factor)
+        self.shards = []
+        for cap, tab in self.tables_host:
+            if wl.kind == configs.MLA:
+                k = torch.empty((cap, wl.block_size, wl.dk), dtype=torch.bfloat16, device=device)
+                v = None
+            else:
+                k = torch.empty((cap, wl.kv_heads, wl.block_size, wl.dk), dtype=torch.bfloat16, device=device)
+                v = torch.empty((cap, wl.kv_heads, wl.block_size, wl.dv), dtype=torch.bfloat16, device=device)
+            if canary is not None:
+                k.view(torch.int16).fill_(canary)
+                if v is not None:
+                    v.view(torch.int16).fill_(canary)
+            self.shards.append(dcp.Shard(k, v, torch.from_numpy(tab).to(device)))
+        self.starts = torch.from_numpy(starts).to(device)
+        qstream = inputs.STREAM_Q_MLA if wl.kind == configs.MLA else inputs.STREAM_Q
+        self.q = inputs.query(wl.seed, np.arange(B), wl.q_heads, wl.dk, device, stream=qstream)
+        self.positions = torch.from_numpy(self.ctx.astype(np.int32)).to(device)
+        self.seq_lens = torch.from_numpy((self.ctx + 1).astype(np.int32)).to(device)
+        self.k_new, self.v_new = self.token_rows(np.arange(B), self.ctx)
+        ws = dcp.dcp_workspace_size(self.desc, B, N)
+        if ws <= 0:
+            raise RuntimeError("dcp_workspace_size failed")
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=device)
+        self.o_parts = torch.empty((N, B, wl.q_heads, wl.dv), dtype=torch.float32, device=device)
+        self.lses = torch.empty((N, B, wl.q_heads), dtype=torch.float32, device=device)
+        self.o = torch.empty((B, wl.q_heads, wl.dv), dtype=torch.float32, device=device)
+        self.lse = torch.empty((B, wl.q_heads), dtype=torch.float32, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        if fill:
+            self.fill_context(fill_chunk)
+
+    # -- token rows from the seeded generator -------------------------------
+    def token_rows(self, b, t):
+        wl = self.wl
+        if wl.kind == configs.MLA:
+            lat = inputs.kv_tokens(wl.seed, inputs.STREAM_LATENT, b, t, 1, wl.dk, self.device, chunk=1 << 18)
+            return lat.view(-1, wl.dk), None
+        k = inputs.kv_tokens(wl.seed, inputs.STREAM_K, b, t, wl.kv_heads, wl.dk, self.device, chunk=1 << 16)
+        v = inputs.kv_tokens(wl.seed, inputs.STREAM_V, b, t, wl.kv_heads, wl.dv, self.device, chunk=1 << 16)
+        return k, v
+
+    def fill_context(self, chunk: int = 1 << 18):
+        """Write every context token [0, ctx[b]) of every sequence into the pools."""
+        ctx = torch.from_numpy(self.ctx).to(self.device)
+        ends = torch.cumsum(ctx, 0)
+        begins = ends - ctx
+        total = int(ends[-1]) if ctx.numel() else 0
+        for s in range(0, total, chunk):
+            idx = torch.arange(s, min(total, s + chunk), dtype=torch.int64, device=self.device)
+            b = torch.searchsorted(ends, idx, right=True)
+            t = idx - begins[b]
+            k, v = self.token_rows(b, t)
+            dcp.dcp_kv_append(self.desc, self.shards, self.starts, t.to(torch.int32), k, v,
+                              seq_ids=b.to(torch.int32), err=self.err)
+
+    # -- the decode step through the C ABI ------------------------------------
+    def append(self, stream=None):
+        dcp.dcp_kv_append(self.desc, self.shards, self.starts, self.positions, self.k_new, self.v_new,
+                          err=self.err, stream=stream)
+
+    def partial(self, stream=None):
+        dcp.dcp_decode_partial_all(self.desc, self.q, self.shards, self.seq_lens, self.starts, self.o_parts,
+                                   self.lses, self.workspace, err=self.err, stream=stream)
+
+    def merge(self, stream=None):
+        dcp.dcp_merge(self.o_parts, self.lses, self.o, self.lse, stream=stream)
+
+    def step(self, stream=None):
+        self.append(stream)
+        self.partial(stream)
+        self.merge(stream)
+
+    # -- algorithmic bytes ---------------------------------------------------
+    def attended_tokens(self) -> int:
+        return int((self.ctx + 1).sum())
+
+    def kv_bytes(self) -> int:
+        """KV bytes the partial-attention pass must read (each attended token once)."""
+        return self.attended_tokens() * self.wl.kv_bytes_per_token
+
+    def step_bytes(self) -> dict:
+        """Algorithmic HBM bytes of one step, by kernel."""
+        wl = self.wl
+        B, N, Hq, dv, dk = wl.batch, wl.shards, wl.q_heads, wl.dv, wl.dk
+        part = N * B * Hq * (dv + 1) * 4
+        new_tok = B * (wl.kv_heads * (dk + dv) * 2 if wl.kind == configs.GQA else dk * 2)
+        return {
+            "append": 2 * new_tok,                      # read the new rows, write them
+            "partial": self.kv_bytes() + B * Hq * dk * 2 + part,
+            "merge": part + B * Hq * (dv + 1) * 4,
+        }

@@ -223,6 +223,24 @@ def run_reference(args, wl):
 
 
 # ---------------------------------------------------------------------------
+# cross-rank aggregation (host side; replicas share no data)
+# ---------------------------------------------------------------------------
+def max_over_ranks(vals, device="cpu"):
+    """Element-wise max of per-rank timings (all ranks get the result)."""
+    import torch
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def whole_job_gbs(world: int, bytes_per_step_per_rank: int, ms_slowest: float) -> float:
+    """Whole-job GB/s: the bytes every rank processed over the slowest rank's time."""
+    return world * bytes_per_step_per_rank / (ms_slowest * 1e-3) / 1e9
+
+
+# ---------------------------------------------------------------------------
 # the CUDA path
 # ---------------------------------------------------------------------------
 def run_ours(args, wl):
@@ -318,15 +336,11 @@ def run_ours(args, wl):
     barrier()
     e2e_ms = e0.elapsed_time(e1) / K
 
-    # max over ranks
-    vals = torch.tensor([ms, partial_ms, e2e_ms], dtype=torch.float64, device=f"cuda:{local}")
-    if dist is not None:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    ms, partial_ms, e2e_ms = (float(x) for x in vals.cpu())
+    ms, partial_ms, e2e_ms = max_over_ranks([ms, partial_ms, e2e_ms], device=f"cuda:{local}")
 
     if rank == 0:
         peak, peak_kind = _peaks()
-        value = world * step_bytes / (ms * 1e-3) / 1e9
+        value = whole_job_gbs(world, step_bytes, ms)
         achieved = bytes_["partial"] / (partial_ms * 1e-3) / 1e9
         kern = "dcp_mla.cu" if wl.kind == 1 else "dcp_gqa.cu"
         line = {
@@ -342,7 +356,7 @@ def run_ours(args, wl):
                          "traffic": _traffic_for(kern, wl.name),
                          "algorithmic_bytes_per_launch": bytes_["partial"]},
             "step_bytes": bytes_,
-            "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "e2e": {"value": round(whole_job_gbs(world, step_bytes, e2e_ms), 2), "unit": "GB/s",
                     "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": 5 * K,
             "clocks": clocks,

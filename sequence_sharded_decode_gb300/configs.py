@@ -38,6 +38,7 @@ class Workload:
     ctx_hi: int = 262144
     capacity_factor: float = 1.0   # > 1: fragmented pools with holes
     seed: int = 0
+    needles: int = 0               # planted q-aligned keys per sequence (structured parity cases)
 
     def ctx_lens(self) -> np.ndarray:
         """Context length of every sequence before the decode step."""
@@ -45,6 +46,11 @@ class Workload:
             return np.full(self.batch, self.ctx_fixed, dtype=np.int64)
         return inputs.lognormal_lengths(self.seed, self.batch, self.median, self.sigma,
                                         self.ctx_lo, self.ctx_hi)
+
+    def needle_plan(self) -> dict:
+        if self.needles <= 0:
+            return {}
+        return inputs.needle_plan(self.seed, self.ctx_lens() + 1, self.needles, self.q_heads)
 
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)

@@ -182,8 +182,43 @@ def block_tables(seed: int, counts: np.ndarray, capacity_factor: float = 1.0):
     return out
 
 
-def needle_positions(seed: int, seq_len: int, count: int) -> np.ndarray:
-    """`count` distinct token positions in [0, seq_len), drawn uniformly."""
+def needle_plan(seed: int, seq_lens, per_seq: int, q_heads: int) -> dict:
+    """Planted "needle" keys: for each sequence, `per_seq` (position, query
+    head) pairs drawn uniformly from [0, seq_len) x [0, q_heads)."""
     rng = np.random.default_rng(seed + 7919)
-    count = min(count, seq_len)
-    return np.sort(rng.choice(seq_len, size=count, replace=False)).astype(np.int64)
+    plan = {}
+    for b, L in enumerate(seq_lens):
+        L = int(L)
+        if L <= 0:
+            continue
+        n = min(per_seq, L)
+        pos = rng.choice(L, size=n, replace=False)
+        heads = rng.integers(0, q_heads, size=n)
+        plan[b] = sorted((int(t), int(h)) for t, h in zip(pos, heads))
+    return plan
+
+
+def plant_needles(rows: torch.Tensor, batch_ids, positions, q: torch.Tensor, plan: dict, q_heads: int,
+                  alpha: float = 4.0) -> torch.Tensor:
+    """Replace the key rows of planted positions by alpha * q[b, h] (bf16).
+
+    rows: [T, Hkv, Dk] (GQA keys) or [T, Dk] (MLA latent); q: [B, Hq, Dk] on
+    the rows' device. GQA puts the needle in KV head h // (Hq / Hkv). alpha is
+    a power of two, so the product is exact in bf16 on every device.
+    """
+    if not plan:
+        return rows
+    b = torch.as_tensor(batch_ids, dtype=torch.int64, device=rows.device).reshape(-1)
+    t = torch.as_tensor(positions, dtype=torch.int64, device=rows.device).reshape(-1)
+    for bb, needles in plan.items():
+        for tt, h in needles:
+            idx = torch.nonzero((b == bb) & (t == tt)).reshape(-1)
+            if idx.numel() == 0:
+                continue
+            val = (q[bb, h].to(torch.float32) * alpha).to(torch.bfloat16)
+            if rows.dim() == 3:
+                kvh = h // (q_heads // rows.shape[1])
+                rows[idx, kvh, :] = val
+            else:
+                rows[idx, :] = val
+    return rows

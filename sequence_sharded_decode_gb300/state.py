@@ -41,6 +41,7 @@ class DecodeState:
         self.starts = torch.from_numpy(starts).to(device)
         qstream = inputs.STREAM_Q_MLA if wl.kind == configs.MLA else inputs.STREAM_Q
         self.q = inputs.query(wl.seed, np.arange(B), wl.q_heads, wl.dk, device, stream=qstream)
+        self.needles = wl.needle_plan()
         self.positions = torch.from_numpy(self.ctx.astype(np.int32)).to(device)
         self.seq_lens = torch.from_numpy((self.ctx + 1).astype(np.int32)).to(device)
         self.k_new, self.v_new = self.token_rows(np.arange(B), self.ctx)
@@ -61,8 +62,10 @@ class DecodeState:
         wl = self.wl
         if wl.kind == configs.MLA:
             lat = inputs.kv_tokens(wl.seed, inputs.STREAM_LATENT, b, t, 1, wl.dk, self.device, chunk=1 << 18)
-            return lat.view(-1, wl.dk), None
+            lat = inputs.plant_needles(lat.view(-1, wl.dk), b, t, self.q, self.needles, wl.q_heads)
+            return lat, None
         k = inputs.kv_tokens(wl.seed, inputs.STREAM_K, b, t, wl.kv_heads, wl.dk, self.device, chunk=1 << 16)
+        k = inputs.plant_needles(k, b, t, self.q, self.needles, wl.q_heads)
         v = inputs.kv_tokens(wl.seed, inputs.STREAM_V, b, t, wl.kv_heads, wl.dv, self.device, chunk=1 << 16)
         return k, v
 

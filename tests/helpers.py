@@ -31,13 +31,25 @@ def oracle_query(wl: configs.Workload, b: int) -> np.ndarray:
 
 
 def oracle_kv(wl: configs.Workload, b: int, L: int):
-    """Logical K [L, Hkv, Dk] and V [L, Hkv, Dv] (float64) of sequence b."""
+    """Logical K [L, Hkv, Dk] and V [L, Hkv, Dv] (float64) of sequence b,
+    with the workload's planted needles (if any) applied on the CPU."""
+    plan = wl.needle_plan()
+    plan_b = {b: plan[b]} if b in plan else {}
+    pos = np.arange(L)
+    bids = np.full(L, b)
     if wl.kind == configs.MLA:
-        lat = f64(inputs.sequence_kv(wl.seed, inputs.STREAM_LATENT, b, 0, L, 1, wl.dk))
+        lat = inputs.sequence_kv(wl.seed, inputs.STREAM_LATENT, b, 0, L, 1, wl.dk)
+        if plan_b:
+            q = inputs.query(wl.seed, np.arange(b + 1), wl.q_heads, wl.dk, stream=inputs.STREAM_Q_MLA)
+            lat = inputs.plant_needles(lat.view(L, wl.dk), bids, pos, q, plan_b, wl.q_heads).view(L, 1, wl.dk)
+        lat = f64(lat)
         return lat, lat[:, :, :wl.dv]
-    k = f64(inputs.sequence_kv(wl.seed, inputs.STREAM_K, b, 0, L, wl.kv_heads, wl.dk))
+    k = inputs.sequence_kv(wl.seed, inputs.STREAM_K, b, 0, L, wl.kv_heads, wl.dk)
+    if plan_b:
+        q = inputs.query(wl.seed, np.arange(b + 1), wl.q_heads, wl.dk)
+        k = inputs.plant_needles(k, bids, pos, q, plan_b, wl.q_heads)
     v = f64(inputs.sequence_kv(wl.seed, inputs.STREAM_V, b, 0, L, wl.kv_heads, wl.dv))
-    return k, v
+    return f64(k), v
 
 
 def oracle_sequence(wl: configs.Workload, b: int, L: int, starts_b):

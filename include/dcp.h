@@ -54,7 +54,9 @@ typedef enum {
   DCP_ERR_SHAPE = -2,       /* inconsistent sizes in the descriptor/shards   */
   DCP_ERR_UNSUPPORTED = -3, /* valid but not implemented (e.g. head_dim 96) */
   DCP_ERR_CUDA = -4,        /* a CUDA call or launch failed                  */
-  DCP_ERR_WORKSPACE = -5    /* workspace NULL, misaligned or too small       */
+  DCP_ERR_WORKSPACE = -5,   /* workspace NULL, misaligned or too small       */
+  DCP_ERR_SCRATCH_LIMIT = -6 /* problem needs more than the fixed scratch of
+                                dcp_decode_partial_all_noalloc                */
 } dcp_status;
 
 /* Bits OR'ed into *dev_err_flag by kernels. */
@@ -175,6 +177,37 @@ DCP_API int dcp_decode_partial_all(const dcp_attn_desc* desc, const void* q, con
                            int N, const int32_t* seq_lens, const int32_t* shard_starts, int B,
                            float* o_parts, float* lses, void* workspace, size_t ws_bytes,
                            int32_t* dev_err_flag, void* stream);
+
+/* Same computation as dcp_decode_partial_all, for callers that cannot
+ * allocate device memory at the point of the call: for example a plugin
+ * running inside a serving engine that owns every byte of device memory
+ * through its own pool and hands extensions no scratch buffer, or a
+ * latency-critical decode loop that must not call cudaMalloc because it can
+ * synchronise the device. (The pages describe no such entry point; it exists
+ * only for these callers.)
+ *
+ * Instead of a caller-provided workspace it uses one fixed scratch array of
+ * DCP_NOALLOC_SCRATCH_BYTES in device global memory, defined by the library
+ * itself; every GPU that loads the library keeps that array until the process
+ * exits. The call allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make
+ *    that first call before any stream capture.
+ *  - Problems whose workspace (dcp_workspace_size(desc, B, N)) exceeds
+ *    DCP_NOALLOC_SCRATCH_BYTES are rejected with DCP_ERR_SCRATCH_LIMIT before
+ *    any launch.
+ *  - All calls on a device share the one array and leave their contents in
+ *    it; nothing in it has to start at zero (each call writes everything it
+ *    later reads). Calls whose work overlaps on the GPU -- concurrent streams,
+ *    or several host threads -- race on the array: serialise them.
+ * Arguments and outputs are those of dcp_decode_partial_all. */
+#define DCP_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+DCP_API int dcp_decode_partial_all_noalloc(const dcp_attn_desc* desc, const void* q,
+                                           const dcp_shard* shards, int N, const int32_t* seq_lens,
+                                           const int32_t* shard_starts, int B, float* o_parts,
+                                           float* lses, int32_t* dev_err_flag, void* stream);
 
 /* Step 3 of the method: combine N partials by LSE reweighting
  * ("Inference Systems Infrastructure Notes (7): DCP", section 2; the Qiita

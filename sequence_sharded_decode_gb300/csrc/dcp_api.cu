@@ -155,6 +155,27 @@ static int run_partial(const dcp_attn_desc* desc, const void* q, const ShardSet&
   return DCP_OK;
 }
 
+// Fixed scratch of dcp_decode_partial_all_noalloc: the library's own device
+// array, for callers that cannot allocate. Host code must not pass the
+// symbol itself to a kernel (in host code it names a host-side stand-in);
+// noalloc_scratch() looks up its device address once per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DCP_NOALLOC_SCRATCH_BYTES];
+
+static int noalloc_scratch(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DCP_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return DCP_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return DCP_OK;
+}
+
 }  // namespace dcp
 
 using namespace dcp;
@@ -169,6 +190,8 @@ const char* dcp_status_string(int status) {
     case DCP_ERR_UNSUPPORTED: return "unsupported configuration";
     case DCP_ERR_CUDA: return "CUDA error";
     case DCP_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case DCP_ERR_SCRATCH_LIMIT:
+      return "problem needs more workspace than the fixed scratch of dcp_decode_partial_all_noalloc";
     default: return "unknown status";
   }
 }
@@ -258,6 +281,30 @@ int dcp_decode_partial_all(const dcp_attn_desc* desc, const void* q, const dcp_s
   if (!aligned16(q) || !aligned16(o_parts)) return DCP_ERR_INVALID_ARG;
   RangeSpec rs{seq_lens, shard_starts, nullptr, dev_err_flag, 0, B, N};
   return run_partial(desc, q, sh, rs, o_parts, lses, workspace, ws_bytes, dev_err_flag, stream);
+}
+
+int dcp_decode_partial_all_noalloc(const dcp_attn_desc* desc, const void* q, const dcp_shard* shards, int N,
+                                   const int32_t* seq_lens, const int32_t* shard_starts, int B, float* o_parts,
+                                   float* lses, int32_t* dev_err_flag, void* stream) {
+  int rc = check_desc(desc);
+  if (rc != DCP_OK) return rc;
+  ShardSet sh;
+  rc = check_shards(*desc, shards, N, &sh);
+  if (rc != DCP_OK) return rc;
+  if (B < 0) return DCP_ERR_INVALID_ARG;
+  if (B == 0) return DCP_OK;
+  if (!q || !seq_lens || !shard_starts || !o_parts || !lses) return DCP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(o_parts)) return DCP_ERR_INVALID_ARG;
+  WsLayout L;
+  int n_ctas = 0;
+  rc = layout_for(*desc, B, N, &L, &n_ctas);
+  if (rc != DCP_OK) return rc;
+  if (L.total > DCP_NOALLOC_SCRATCH_BYTES) return DCP_ERR_SCRATCH_LIMIT;
+  void* ws = nullptr;
+  rc = noalloc_scratch(&ws);
+  if (rc != DCP_OK) return rc;
+  RangeSpec rs{seq_lens, shard_starts, nullptr, dev_err_flag, 0, B, N};
+  return run_partial(desc, q, sh, rs, o_parts, lses, ws, DCP_NOALLOC_SCRATCH_BYTES, dev_err_flag, stream);
 }
 
 int dcp_merge(const float* o_parts, const float* lses, int N, int B, int Hq, int Dv, float* o, float* lse_out,

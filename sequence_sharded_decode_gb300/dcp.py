@@ -23,6 +23,8 @@ DCP_ERR_SHAPE = -2
 DCP_ERR_UNSUPPORTED = -3
 DCP_ERR_CUDA = -4
 DCP_ERR_WORKSPACE = -5
+DCP_ERR_SCRATCH_LIMIT = -6
+DCP_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 DCP_DEVERR_BLOCK_RANGE = 1
 DCP_DEVERR_TABLE_RANGE = 2
@@ -34,7 +36,7 @@ DCP_KIND_GQA = 0
 DCP_KIND_MLA = 1
 
 EXPORTED = ("dcp_status_string", "dcp_version", "dcp_shard_plan", "dcp_kv_append", "dcp_workspace_size",
-            "dcp_decode_partial", "dcp_decode_partial_all", "dcp_merge")
+            "dcp_decode_partial", "dcp_decode_partial_all", "dcp_decode_partial_all_noalloc", "dcp_merge")
 
 
 class DcpError(RuntimeError):
@@ -113,6 +115,8 @@ def load() -> ctypes.CDLL:
     lib.dcp_decode_partial.argtypes = [pdesc, vp, pshard, vp, vp, i32, vp, vp, vp, sz, vp, vp]
     lib.dcp_decode_partial_all.restype = i32
     lib.dcp_decode_partial_all.argtypes = [pdesc, vp, pshard, i32, vp, vp, i32, vp, vp, vp, sz, vp, vp]
+    lib.dcp_decode_partial_all_noalloc.restype = i32
+    lib.dcp_decode_partial_all_noalloc.argtypes = [pdesc, vp, pshard, i32, vp, vp, i32, vp, vp, vp, vp]
     lib.dcp_merge.restype = i32
     lib.dcp_merge.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
     _lib = lib
@@ -237,6 +241,25 @@ def dcp_decode_partial_all(desc: AttnDesc, q: torch.Tensor, shards, seq_lens: to
                                        o_parts.data_ptr(), lses.data_ptr(), workspace.data_ptr(),
                                        workspace.numel(), _ptr(err), _stream(stream))
     _raise(rc, "dcp_decode_partial_all")
+
+
+def dcp_decode_partial_all_noalloc(desc: AttnDesc, q: torch.Tensor, shards, seq_lens: torch.Tensor,
+                                   shard_starts: torch.Tensor, o_parts: torch.Tensor, lses: torch.Tensor,
+                                   err: torch.Tensor | None = None, stream=None):
+    """dcp_decode_partial_all without a caller workspace: the library's fixed
+    device scratch (DCP_NOALLOC_SCRATCH_BYTES) is used instead."""
+    _check(q, torch.bfloat16, "q")
+    _check(seq_lens, torch.int32, "seq_lens")
+    _check(shard_starts, torch.int32, "shard_starts")
+    _check(o_parts, torch.float32, "o_parts")
+    _check(lses, torch.float32, "lses")
+    if err is not None:
+        _check(err, torch.int32, "err")
+    arr = _shards(shards)
+    rc = load().dcp_decode_partial_all_noalloc(ctypes.byref(desc.c()), q.data_ptr(), arr, len(shards),
+                                               seq_lens.data_ptr(), shard_starts.data_ptr(), int(q.shape[0]),
+                                               o_parts.data_ptr(), lses.data_ptr(), _ptr(err), _stream(stream))
+    _raise(rc, "dcp_decode_partial_all_noalloc")
 
 
 def dcp_merge(o_parts: torch.Tensor, lses: torch.Tensor, o: torch.Tensor, lse_out: torch.Tensor | None = None,

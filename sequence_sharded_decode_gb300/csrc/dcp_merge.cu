@@ -72,45 +72,70 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __res
 
 // Joins the items of split lanes (workspace partial rows) into the lane's
 // output rows; writes O = 0, LSE = -inf for lanes with no tokens at all.
+// One warp per (lane, query-head row), float4 columns spread over the lanes;
+// warps of lanes written directly by the attention kernel return at once.
 __global__ void __launch_bounds__(kMergeThreads) combine_kernel(const char* __restrict__ ws, WsLayout L,
-                                                                int B, int Hq, int dv, int lanes_per_unit,
+                                                                int Hq, int dv, int lanes_per_unit,
                                                                 int heads_per_lane, int groups, int g,
                                                                 float* __restrict__ o_parts,
                                                                 float* __restrict__ lses) {
-  const int lane_id = blockIdx.x;
-  const LaneRec ln = reinterpret_cast<const LaneRec*>(ws + L.lanes_off)[lane_id];
-  if (ln.n_items == 1) return;
+  const int lane = threadIdx.x & 31;
+  const int rpl = L.rows_per_lane;
+  const long long total = (long long)L.max_lanes * rpl;
+  const long long warps = (long long)gridDim.x * (kMergeThreads / 32);
+  const LaneRec* lrec = reinterpret_cast<const LaneRec*>(ws + L.lanes_off);
   const float* tmp_o = reinterpret_cast<const float*>(ws + L.tmp_o_off);
   const float* tmp_lse = reinterpret_cast<const float*>(ws + L.tmp_lse_off);
-  const int u = lane_id / lanes_per_unit, j = lane_id - u * lanes_per_unit;
-  int head0, nheads;
-  if (groups > 0) {  // GQA lane = (unit, kv head, head group)
-    const int kvh = j / groups, hg = j - kvh * groups;
-    head0 = kvh * g + hg * heads_per_lane;
-    nheads = min(heads_per_lane, g - hg * heads_per_lane);
-  } else {
-    head0 = 0;
-    nheads = Hq;
-  }
-  float* out_o = o_parts + ((size_t)u * Hq + head0) * dv;
-  float* out_l = lses + (size_t)u * Hq + head0;
-  const int rpl = L.rows_per_lane;
-  for (int idx = threadIdx.x; idx < nheads * dv; idx += kMergeThreads) {
-    const int r = idx / dv, c = idx - r * dv;
-    float M = -INFINITY;
-    for (int i = 0; i < ln.n_items; ++i) M = fmaxf(M, tmp_lse[(size_t)(ln.tmp_begin + i) * rpl + r]);
-    float num = 0.f, den = 0.f;
-    if (M != -INFINITY) {
-      for (int i = 0; i < ln.n_items; ++i) {
-        const float li = tmp_lse[(size_t)(ln.tmp_begin + i) * rpl + r];
-        if (li == -INFINITY) continue;
-        const float w = expf(li - M);
-        num += w * tmp_o[((size_t)(ln.tmp_begin + i) * rpl + r) * dv + c];
-        den += w;
-      }
+  const int dv4 = dv / 4;
+  for (long long w = (long long)blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5); w < total; w += warps) {
+    const int lane_id = (int)(w / rpl), r = (int)(w - (long long)lane_id * rpl);
+    const LaneRec ln = lrec[lane_id];
+    if (ln.n_items == 1) continue;
+    const int u = lane_id / lanes_per_unit, j = lane_id - u * lanes_per_unit;
+    int head0, nheads;
+    if (groups > 0) {  // GQA lane = (unit, kv head, head group)
+      const int kvh = j / groups, hg = j - kvh * groups;
+      head0 = kvh * g + hg * heads_per_lane;
+      nheads = min(heads_per_lane, g - hg * heads_per_lane);
+    } else {
+      head0 = 0;
+      nheads = Hq;
     }
-    out_o[(size_t)r * dv + c] = den > 0.f ? num / den : 0.f;
-    if (c == 0) out_l[r] = den > 0.f ? M + logf(den) : -INFINITY;
+    if (r >= nheads) continue;
+    float4* dst = reinterpret_cast<float4*>(o_parts + ((size_t)u * Hq + head0 + r) * dv);
+    float* dst_lse = lses + (size_t)u * Hq + head0 + r;
+    const int n = ln.n_items;
+    float M = -INFINITY;
+    for (int i = lane; i < n; i += 32) M = fmaxf(M, tmp_lse[(size_t)(ln.tmp_begin + i) * rpl + r]);
+    for (int s = 16; s > 0; s >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, s));
+    if (M == -INFINITY) {  // no tokens (or no items) for this lane
+      for (int c = lane; c < dv4; c += 32) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (lane == 0) *dst_lse = -INFINITY;
+      continue;
+    }
+    float wsum = 0.f;
+    for (int i = lane; i < n; i += 32) {
+      const float li = tmp_lse[(size_t)(ln.tmp_begin + i) * rpl + r];
+      wsum += li == -INFINITY ? 0.f : expf(li - M);
+    }
+    for (int s = 16; s > 0; s >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, s);
+    const float inv = 1.f / wsum;
+    for (int c = lane; c < dv4; c += 32) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i = 0; i < n; ++i) {
+        const size_t row = (size_t)(ln.tmp_begin + i) * rpl + r;
+        const float li = tmp_lse[row];
+        if (li == -INFINITY) continue;
+        const float wt = expf(li - M);
+        const float4 v = reinterpret_cast<const float4*>(tmp_o + row * dv)[c];
+        acc.x += wt * v.x;
+        acc.y += wt * v.y;
+        acc.z += wt * v.z;
+        acc.w += wt * v.w;
+      }
+      dst[c] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    }
+    if (lane == 0) *dst_lse = M + logf(wsum);
   }
 }
 
@@ -133,9 +158,13 @@ cudaError_t launch_combine(const dcp_attn_desc& d, int B, int n_lanes, const voi
   const LaneGeom lg = lane_geom(d);
   const int groups = d.kind == DCP_KIND_GQA ? lg.groups : 0;
   const int g = d.num_q_heads / d.num_kv_heads;
-  combine_kernel<<<n_lanes, kMergeThreads, 0, st>>>(static_cast<const char*>(ws), L, B, d.num_q_heads,
-                                                     d.head_dim_v, lg.lanes_per_unit, lg.heads_per_lane,
-                                                     groups, g, o_parts, lses);
+  DeviceInfo di;
+  if (device_info(&di) != 0) return cudaErrorUnknown;
+  const long long warps = (long long)n_lanes * L.rows_per_lane;
+  const long long want = (warps + kMergeThreads / 32 - 1) / (kMergeThreads / 32);
+  const int grid = (int)(want < di.sm_count * 16LL ? want : di.sm_count * 16LL);
+  combine_kernel<<<grid, kMergeThreads, 0, st>>>(static_cast<const char*>(ws), L, d.num_q_heads, d.head_dim_v,
+                                                 lg.lanes_per_unit, lg.heads_per_lane, groups, g, o_parts, lses);
   return cudaGetLastError();
 }
 

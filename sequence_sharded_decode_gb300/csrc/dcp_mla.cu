@@ -1,13 +1,704 @@
-// MLA-absorbed partial decode attention (placeholder until the tcgen05 kernel lands).
+// Partial decode attention, MLA-absorbed form, on the 5th-generation tensor
+// cores (tcgen05 + TMEM + TMA) of sm_103a.
+//
+// What it computes (step 2 of the method: each shard attends the one-token
+// queries against its own KV slice and emits a partial output plus LSE --
+// Qiita write-up "vLLMの-dcpが長文脈のKVキャッシュ重複を消して3倍速くする",
+// section "トークンの区間でGPUに割り振る"): per sequence, 128 absorbed query
+// heads (576 wide) attend one latent KV head; the key is the cached 576-wide
+// latent row and the value its first 512 entries (MLA keeps effectively one KV
+// head -- same write-up, section "なぜテンソル並列だとKVキャッシュが二重に載るのか").
+//
+// Why a CTA pair: the fp32 output accumulator of 128 heads x 512 dims is
+// 256 KB, all of one SM's tensor memory. Each work item runs on a 2-CTA
+// cluster that splits the latent columns:
+//   CTA r owns score columns [288 r, 288 r + 288) and output dims [256 r, 256 r + 256);
+//   it loads latent columns [256 r, 256 r + 320) of each page (5 x 64-column
+//   TMA boxes; 32 columns overlap, read twice from L2, once from HBM)
+// and per 64-token tile (= one paged block):
+//   1. S_r = Q_r . K_r^T  (M=128 heads, N=64 tokens, K=288) into TMEM; Q_r
+//      sits in TMEM as the A operand, the K box in shared memory is B
+//   2. each CTA sends its whole partial row block S_r to the other one through
+//      distributed shared memory (st.async, completion counted in bytes on the
+//      receiver's mbarrier: no per-thread release fences)
+//   3. both compute S = S_0 + S_1 (bitwise the same in both: a + b == b + a)
+//      and run the same online softmax over the 64 tokens, so they agree on
+//      the running max and the row sums without exchanging them
+//   4. P is written to shared memory as two bf16 terms, hi = bf16(p) and
+//      lo = bf16(p - hi): P.V then carries ~16 mantissa bits of p
+//   5. O_r += P_hi . V_r + P_lo . V_r  (M=128, N=256, K=64) into TMEM.
+// Every KV byte is read from HBM once; the only recomputation is the softmax
+// (exp on 64 tokens instead of 32 per CTA). O is rescaled lazily, only when
+// the running max grows by more than 2^8.
+//
+// Roles per CTA (192 threads): warps 0-3 softmax + epilogue (thread h owns
+// query head h = TMEM lane h), warp 4 lane 0 TMA producer, warp 5 lane 0 MMA
+// issuer (warp 5 also allocates TMEM). Every barrier's phases are observed by
+// its waiter in order and never more than one phase late, so parity waits are
+// unambiguous; the end of a tile's P.V is read from the release of its P
+// buffer. Every wait is bounded: on expiry the kernel raises
+// DCP_DEVERR_TIMEOUT, stops all roles, drains what it issued and frees TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <cmath>
+#include <mutex>
+
 #include "dcp_internal.cuh"
 
 namespace dcp {
+namespace {
 
-int mla_ctas(const dcp_attn_desc&, const DeviceInfo& di) { return di.sm_count; }
+constexpr int kHeads = 128;
+constexpr int kDv = 512;
+constexpr int kTile = 64;                        // tokens per tile: one paged block
+constexpr int kChunks = 5;                       // 64-column boxes loaded per page per CTA
+constexpr int kKSteps = 18;                      // 16-column k-steps of the score MMA per CTA
+constexpr int kStages = 3;                       // K/V tile pipeline depth
+constexpr int kThreads = 192;
+constexpr int kKvChunkBytes = kTile * 128;       // 64 rows x 64 bf16
+constexpr int kStageBytes = kChunks * kKvChunkBytes;
+constexpr int kPBytes = kHeads * 128;            // 128 heads x 64 tokens bf16 (one term)
+constexpr int kXBytes = kHeads * kTile * 4;      // the peer's partial scores, fp32
 
-cudaError_t launch_mla(const dcp_attn_desc&, const void*, const ShardSet&, const RangeSpec&, float*, float*, void*,
-                       const WsLayout&, int, int32_t*, cudaStream_t) {
-  return cudaErrorNotSupported;
+constexpr int kOffKv = 0;
+constexpr int kOffP = kOffKv + kStages * kStageBytes;   // P[pb][term] at kOffP + (2 pb + term) kPBytes
+constexpr int kOffX = kOffP + 4 * kPBytes;
+constexpr int kOffBar = kOffX + kXBytes;
+constexpr int kNumBars = 24;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag
+constexpr int kSmemUsed = kOffMisc + 16;
+constexpr int kSmemBytes = kSmemUsed + 1024;      // slack to align the base to 1024
+
+// barrier slots
+constexpr int BQ_FULL = 0, BQ_EMPTY = 1, BS_FULL = 2, BS_EMPTY = 3, BX_FULL = 4, BX_FREE = 5, BX_READ = 6,
+              BDRAIN = 7, BKV_FULL = 8, BKV_EMPTY = 8 + kStages, BP_FULL = 8 + 2 * kStages,
+              BP_EMPTY = 10 + 2 * kStages;
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 0;       // 256 columns: O_r, fp32
+constexpr uint32_t kColS = 256;     // 64 columns: S_r, fp32
+constexpr uint32_t kColQ = 320;     // 144 columns: Q_r, bf16 pairs
+constexpr uint32_t kSpinLimit = 1u << 24;
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;       // log2 units
+
+struct MlaParams {
+  CUtensorMap tm_kv[kMaxShards];
+  ShardSet sh;
+  const __nv_bfloat16* q;
+  const char* ws;
+  WsLayout L;
+  float* o_parts;
+  float* lses;
+  int32_t* err;
+  int B;
+  float sl2;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t saddr(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t peer_addr(uint32_t a, uint32_t peer) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(a), "r"(peer));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void bar_init(uint32_t b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(b), "r"(count));
+}
+__device__ __forceinline__ void bar_arrive(uint32_t b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(b) : "memory");
+}
+__device__ __forceinline__ void bar_arrive_tx(uint32_t b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(b), "r"(bytes) : "memory");
+}
+// arrive on the barrier at the same offset in the peer CTA (orders this
+// thread's prior shared::cluster stores before the arrival)
+__device__ __forceinline__ void bar_arrive_peer(uint32_t b, uint32_t peer) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(peer_addr(b, peer)) : "memory");
+}
+__device__ __forceinline__ bool bar_try(uint32_t b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok) : "r"(b), "r"(parity) : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool bar_try_cluster(uint32_t b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok) : "r"(b), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Bounded wait. Returns false if the kernel is aborting (this wait expired, or
+// another role's did): the caller then stops.
+__device__ __noinline__ bool wait_bar(uint32_t b, uint32_t parity, volatile int* abort_flag, int32_t* err,
+                                      bool cluster_scope) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (cluster_scope ? bar_try_cluster(b, parity) : bar_try(b, parity)) return true;
+    if ((i & 63u) == 63u && *abort_flag) return false;
+  }
+  *abort_flag = 1;
+  raise_flag(err, DCP_DEVERR_TIMEOUT);
+  return false;
+}
+// Warp-uniform bounded wait for the softmax warps: the warp proceeds only if
+// every lane's wait succeeded, so the .sync.aligned TMEM accesses that follow
+// always run with the whole warp (and an abort leaves the warp together).
+__device__ __forceinline__ bool wait_warp(uint32_t b, uint32_t parity, volatile int* abort_flag, int32_t* err,
+                                          bool cluster_scope) {
+  const bool ok = wait_bar(b, parity, abort_flag, err, cluster_scope);
+  return __all_sync(0xffffffffu, ok);
+}
+// Bounded wait that ignores the abort flag (teardown drains).
+__device__ __forceinline__ void drain_bar(uint32_t b, uint32_t parity) {
+  for (uint32_t i = 0; i < (1u << 22); ++i)
+    if (bar_try(b, parity)) return;
+}
+
+__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar) : "memory");
+}
+
+// Shared-memory matrix descriptor: 128-byte swizzle, 8-row groups 1024 B apart.
+// lbo is the byte stride between 64-element atoms along M/N for MN-major
+// operands (unused for K-major ones).
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo) {
+  uint64_t d = (uint64_t)((addr >> 4) & 0x3FFF);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= 1ull << 46;   // descriptor version for tcgen05
+  d |= 2ull << 61;   // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor, kind::f16: bf16 A/B, fp32 accumulate.
+__host__ __device__ constexpr uint32_t idesc(int M, int N, int b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn_major << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, int accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+      ::"r"(d), "l"(a), "l"(b), "r"(id), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n"
+               :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]) : "memory");
+}
+
+__device__ __forceinline__ void st_local_v4(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+
+// S = Q . K^T with A (the queries) read from tensor memory
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id, int accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+      ::"r"(d), "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate));
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+// 16 bytes into the peer's shared memory; completion is counted on the
+// peer's mbarrier (transaction bytes), so no release fence is needed.
+__device__ __forceinline__ void st_async_peer(uint32_t remote, uint32_t remote_bar, uint32_t a, uint32_t b,
+                                              uint32_t c, uint32_t d) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];\n"
+               ::"r"(remote), "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar) : "memory");
+}
+__device__ __forceinline__ uint4 ld_local_v4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a)
+               : "memory");
+  return v;
+}
+// hi = bf16(x), lo = bf16(x - hi), for a pair of values
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// Shared geometry of one work item, derived identically by every role.
+struct ItemGeom {
+  int u, shard, b, t0, t1, out_row, lo, hi, start;
+};
+__device__ __forceinline__ ItemGeom item_geom(const MlaParams& p, int k) {
+  const ItemRec it = reinterpret_cast<const ItemRec*>(p.ws + p.L.items_off)[k];
+  const LaneRec ln = reinterpret_cast<const LaneRec*>(p.ws + p.L.lanes_off)[it.lane];
+  ItemGeom g;
+  g.u = it.lane;
+  g.shard = it.lane / p.B;
+  g.b = it.lane - g.shard * p.B;
+  g.t0 = it.t0;
+  g.t1 = it.t1;
+  g.out_row = it.out_row;
+  g.lo = ln.lo;
+  g.hi = ln.hi;
+  g.start = ln.start;
+  return g;
+}
+// Physical block of tile t of the item, or -1 if the table entry is unusable.
+__device__ __forceinline__ int tile_block(const MlaParams& p, const ItemGeom& g, int t) {
+  const int lb = (g.lo - g.start) / kTile + t;
+  if (lb >= p.sh.max_blocks[g.shard]) return -1;
+  const int phys = p.sh.table[g.shard][(size_t)g.b * p.sh.max_blocks[g.shard] + lb];
+  return (phys < 0 || phys >= p.sh.nblk[g.shard]) ? -1 : phys;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    mla_partial_kernel(const __grid_constant__ MlaParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = saddr(smem_raw);
+  unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  const uint32_t sbase = saddr(smem);
+  const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
+  const int cluster = blockIdx.x >> 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto bar = [&](int i) { return sbase + kOffBar + 8u * i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+
+  if (threadIdx.x == 0) {
+    bar_init(bar(BQ_FULL), kHeads);
+    bar_init(bar(BQ_EMPTY), 1);
+    bar_init(bar(BS_FULL), 1);
+    bar_init(bar(BS_EMPTY), kHeads);
+    bar_init(bar(BX_FULL), 1);       // armed with the byte count of the peer's scores
+    bar_init(bar(BX_FREE), 1);       // the peer's thread 0: "your scores were read"
+    bar_init(bar(BX_READ), kHeads);  // local softmax threads read the peer's scores
+    bar_init(bar(BDRAIN), 1);
+    for (int s = 0; s < kStages; ++s) {
+      bar_init(bar(BKV_FULL + s), 1);
+      bar_init(bar(BKV_EMPTY + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      bar_init(bar(BP_FULL + s), kHeads);
+      bar_init(bar(BP_EMPTY + s), 1);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    bar_arrive_tx(bar(BX_FULL), kXBytes);  // phase 0 expects the peer's first tile
+  }
+  if (warp == 5) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(saddr(tmem_slot)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the peer's barriers exist (and X_FULL is armed) before any remote traffic
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int* cta_begin = reinterpret_cast<const int*>(p.ws + p.L.cta_off);
+  const int k_begin = cta_begin[cluster], k_end = cta_begin[cluster + 1];
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t fills = 0;  // K/V tiles issued (global across items)
+      const int col_base = 256 * (int)rank;
+      bool stop = false;
+      for (int k = k_begin; k < k_end && !stop; ++k) {
+        const ItemGeom g = item_geom(p, k);
+        int phys_next = g.t0 < g.t1 ? tile_block(p, g, g.t0) : -1;
+        for (int t = g.t0; t < g.t1; ++t) {
+          const int phys = phys_next;
+          if (t + 1 < g.t1) phys_next = tile_block(p, g, t + 1);  // one tile ahead: off the issue path
+          const uint32_t s = fills % kStages, use = fills / kStages;
+          if (use > 0 && !wait_bar(bar(BKV_EMPTY + s), (use - 1) & 1u, abort_flag, p.err, false)) {
+            stop = true;
+            break;
+          }
+          if (phys < 0 && rank == 0) raise_flag(p.err, DCP_DEVERR_BLOCK_RANGE);
+          const int row = phys < 0 ? -kTile : phys * kTile;  // out of range: the copy reads zeros
+          bar_arrive_tx(bar(BKV_FULL + s), kChunks * kKvChunkBytes);
+          for (int c = 0; c < kChunks; ++c)
+            tma_load(sbase + kOffKv + s * kStageBytes + c * kKvChunkBytes, &p.tm_kv[g.shard], col_base + 64 * c,
+                     row, bar(BKV_FULL + s));
+          ++fills;
+        }
+      }
+      if (*abort_flag) {  // copies in flight must land before the CTA may exit
+        const uint32_t f0 = fills > (uint32_t)kStages ? fills - kStages : 0;
+        for (uint32_t f = f0; f < fills; ++f) drain_bar(bar(BKV_FULL + f % kStages), (f / kStages) & 1u);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = idesc(128, 64, 0);
+      const uint32_t id_pv = idesc(128, 256, 1);
+      const int koff = 2 * (int)rank;  // CTA 1's first score column is 32 into its first box
+      uint32_t gt = 0;
+      int n_items = 0;
+      auto pv = [&](uint32_t gi, bool first) -> bool {
+        const uint32_t pb = gi & 1u, s = gi % kStages;
+        if (!wait_bar(bar(BP_FULL + pb), (gi >> 1) & 1u, abort_flag, p.err, false)) return false;
+        tc_fence_after();
+        const uint32_t va = sbase + kOffKv + s * kStageBytes;
+        for (int term = 0; term < 2; ++term) {
+          const uint32_t pa = sbase + kOffP + (2 * pb + term) * kPBytes;
+          for (int kt = 0; kt < kTile / 16; ++kt)
+            mma(tmem + kColO, sdesc(pa + 32 * kt, 0), sdesc(va + 2048 * kt, kKvChunkBytes), id_pv,
+                (first && term == 0 && kt == 0) ? 0 : 1);
+        }
+        mma_commit(bar(BKV_EMPTY + s));
+        mma_commit(bar(BP_EMPTY + pb));  // also tells softmax that this P.V finished
+        return true;
+      };
+      bool ok = true;
+      for (int k = k_begin; k < k_end && ok; ++k) {
+        const ItemGeom g = item_geom(p, k);
+        const int nt = g.t1 - g.t0;
+        if (!wait_bar(bar(BQ_FULL), n_items & 1, abort_flag, p.err, false)) break;
+        tc_fence_after();
+        for (int j = 0; j < nt && ok; ++j) {
+          const uint32_t gi = gt + j, s = gi % kStages;
+          if (!wait_bar(bar(BKV_FULL + s), (gi / kStages) & 1u, abort_flag, p.err, false)) { ok = false; break; }
+          if (gi >= 1 && !wait_bar(bar(BS_EMPTY), (gi - 1) & 1u, abort_flag, p.err, false)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t ka = sbase + kOffKv + s * kStageBytes;
+          for (int kk = 0; kk < kKSteps; ++kk) {
+            const int gk = kk + koff;  // 16-column step within this CTA's five boxes
+            mma_ts(tmem + kColS, tmem + kColQ + 8 * kk, sdesc(ka + (gk >> 2) * kKvChunkBytes + 32 * (gk & 3), 0),
+                   id_s, kk > 0);
+          }
+          mma_commit(bar(BS_FULL));
+          if (j == nt - 1) mma_commit(bar(BQ_EMPTY));
+          if (j >= 1 && !pv(gi - 1, j == 1)) { ok = false; break; }
+        }
+        if (!ok) break;
+        if (!pv(gt + nt - 1, nt == 1)) break;
+        gt += nt;
+        ++n_items;
+      }
+      mma_commit(bar(BDRAIN));  // all issued MMAs complete before TMEM may be freed
+      drain_bar(bar(BDRAIN), 0);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int h = threadIdx.x;  // query head = TMEM lane
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t x_row = sbase + kOffX + h * (kTile * 4);
+    const uint32_t x_row_peer = peer_addr(x_row, peer);
+    const uint32_t x_full_peer = peer_addr(bar(BX_FULL), peer);
+    const int qd0 = 288 * (int)rank;
+    uint32_t gt = 0;
+    int n_items = 0;
+    bool ok = true;
+    for (int k = k_begin; k < k_end && ok; ++k) {
+      const ItemGeom g = item_geom(p, k);
+      const int nt = g.t1 - g.t0;
+      // queries of this item into TMEM (after the previous item's score MMAs)
+      if (n_items > 0 && !wait_warp(bar(BQ_EMPTY), (n_items - 1) & 1, abort_flag, p.err, false)) break;
+      tc_fence_after();
+      {
+        const uint4* qr = reinterpret_cast<const uint4*>(p.q + ((size_t)g.b * kHeads + h) * 576 + qd0);
+        uint32_t qv[16];
+        __syncwarp();
+#pragma unroll 1
+        for (int c = 0; c < 9; ++c) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint4 v = qr[4 * c + i];
+            qv[4 * i] = v.x;
+            qv[4 * i + 1] = v.y;
+            qv[4 * i + 2] = v.z;
+            qv[4 * i + 3] = v.w;
+          }
+          tmem_st16(tmem + lane_off + kColQ + 16 * c, qv);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      bar_arrive(bar(BQ_FULL));
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < nt; ++j) {
+        const uint32_t gi = gt + j, pb = gi & 1u, s = gi % kStages;
+        const int t = g.t0 + j;
+        const int phys = tile_block(p, g, t);  // its latency hides behind the score wait
+        // 1. this CTA's partial scores
+        if (!wait_warp(bar(BS_FULL), gi & 1u, abort_flag, p.err, false)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t sv[64];
+        __syncwarp();
+        tmem_ld32(tmem + lane_off + kColS, sv);
+        tmem_ld32(tmem + lane_off + kColS + 32, sv + 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        bar_arrive(bar(BS_EMPTY));
+        // 2. send them to the peer once it has read the previous tile's
+        if (gi >= 1 && !wait_warp(bar(BX_FREE), (gi - 1) & 1u, abort_flag, p.err, true)) { ok = false; break; }
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          st_async_peer(x_row_peer + 16 * i, x_full_peer, sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]);
+        // 3. the peer's partial scores -> full scores (same bits in both CTAs)
+        if (!wait_warp(bar(BX_FULL), gi & 1u, abort_flag, p.err, true)) { ok = false; break; }
+        float sc[64];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint4 v = ld_local_v4(x_row + 16 * i);
+          sc[4 * i] = __uint_as_float(sv[4 * i]) + __uint_as_float(v.x);
+          sc[4 * i + 1] = __uint_as_float(sv[4 * i + 1]) + __uint_as_float(v.y);
+          sc[4 * i + 2] = __uint_as_float(sv[4 * i + 2]) + __uint_as_float(v.z);
+          sc[4 * i + 3] = __uint_as_float(sv[4 * i + 3]) + __uint_as_float(v.w);
+        }
+        bar_arrive(bar(BX_READ));
+        if (h == 0) {
+          // every row read: arm the next phase, then let the peer send again
+          if (!wait_bar(bar(BX_READ), gi & 1u, abort_flag, p.err, false)) {
+            ok = false;
+          } else {
+            bar_arrive_tx(bar(BX_FULL), kXBytes);
+            bar_arrive_peer(bar(BX_FREE), peer);
+          }
+        }
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        // 4. online softmax over the 64 tokens (log2 units)
+        const int n_valid = phys < 0 ? 0 : min(kTile, g.hi - (g.lo + kTile * t));
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          sc[i] = i < n_valid ? sc[i] * p.sl2 : -INFINITY;
+          mx = fmaxf(mx, sc[i]);
+        }
+        float m_new = m_run, alpha = 1.f;
+        bool rescale = false;
+        if (m_run == -INFINITY) {
+          m_new = mx;
+        } else if (mx > m_run + kRescaleThreshold) {
+          m_new = mx;
+          alpha = exp2f(m_run - m_new);
+          rescale = true;
+        }
+        const float ref = m_new == -INFINITY ? 0.f : m_new;
+        // 5. P buffer pb is free once the P.V two tiles back has finished
+        if (gi >= 2 && !wait_warp(bar(BP_EMPTY + pb), ((gi >> 1) - 1) & 1u, abort_flag, p.err, false)) {
+          ok = false;
+          break;
+        }
+        float lsum = 0.f;
+        {
+          const uint32_t hrow = sbase + kOffP + (2 * pb) * kPBytes + h * 128;
+          const uint32_t lrow = hrow + kPBytes;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float a = exp2f(sc[8 * c + 2 * e] - ref), b = exp2f(sc[8 * c + 2 * e + 1] - ref);
+              lsum += a + b;
+              split2(a, b, hi[e], lo[e]);
+            }
+            const uint32_t off = ((uint32_t)c ^ (uint32_t)(h & 7)) << 4;
+            st_local_v4(hrow + off, hi[0], hi[1], hi[2], hi[3]);
+            st_local_v4(lrow + off, lo[0], lo[1], lo[2], lo[3]);
+          }
+        }
+        l_run = l_run * alpha + lsum;
+        m_run = m_new;
+        // 6. V rows past the end of a partial tile may hold anything: zero them
+        if (n_valid < kTile) {
+          const int rows = kTile - n_valid;
+          for (int e = h; e < rows * 4 * 8; e += kHeads) {
+            const int r = n_valid + e / 32, c = (e >> 3) & 3, piece = e & 7;
+            st_local_v4(sbase + kOffKv + s * kStageBytes + c * kKvChunkBytes + r * 128 + piece * 16, 0u, 0u, 0u, 0u);
+          }
+        }
+        // 7. lazy rescale of O after the previous P.V (warp-wide: TMEM access is per warp)
+        if (__any_sync(0xffffffffu, rescale)) {
+          const uint32_t gp = gi - 1;
+          if (!wait_warp(bar(BP_EMPTY + (gp & 1u)), (gp >> 1) & 1u, abort_flag, p.err, false)) { ok = false; break; }
+          tc_fence_after();
+          uint32_t ov[32];
+          __syncwarp();
+#pragma unroll 1
+          for (int c = 0; c < 8; ++c) {
+            tmem_ld32(tmem + lane_off + kColO + 32 * c, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st32(tmem + lane_off + kColO + 32 * c, ov);
+          }
+          tmem_wait_st();
+        }
+        // 8. publish P to the MMA issuer
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        tc_fence_before();
+        bar_arrive(bar(BP_FULL + pb));
+      }
+      if (!ok) break;
+      // epilogue: wait for the last P.V, then write O_r / l and the LSE
+      const uint32_t glast = gt + nt - 1;
+      if (!wait_warp(bar(BP_EMPTY + (glast & 1u)), (glast >> 1) & 1u, abort_flag, p.err, false)) break;
+      tc_fence_after();
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      float* out;
+      float* out_lse;
+      if (g.out_row >= 0) {
+        out = reinterpret_cast<float*>(const_cast<char*>(p.ws) + p.L.tmp_o_off) +
+              ((size_t)g.out_row * kHeads + h) * kDv;
+        out_lse = reinterpret_cast<float*>(const_cast<char*>(p.ws) + p.L.tmp_lse_off) + (size_t)g.out_row * kHeads + h;
+      } else {
+        out = p.o_parts + ((size_t)g.u * kHeads + h) * kDv;
+        out_lse = p.lses + (size_t)g.u * kHeads + h;
+      }
+      out += 256 * rank;
+      uint32_t ov[32];
+      __syncwarp();
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        tmem_ld32(tmem + lane_off + kColO + 32 * c, ov);
+        tmem_wait_ld();
+        float4* o4 = reinterpret_cast<float4*>(out + 32 * c);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          o4[i] = make_float4(__uint_as_float(ov[4 * i]) * inv, __uint_as_float(ov[4 * i + 1]) * inv,
+                              __uint_as_float(ov[4 * i + 2]) * inv, __uint_as_float(ov[4 * i + 3]) * inv);
+      }
+      if (rank == 0) *out_lse = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+      tc_fence_before();
+      gt += nt;
+      ++n_items;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols));
+  }
+  cluster_sync();
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 2-D bf16 map over rows of 576 latent/query columns; boxes of 64 columns
+// (128 bytes, 128-byte swizzle) by box_rows rows; out-of-range rows read 0.
+bool latent_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {576, rows};
+  cuuint64_t strides[1] = {576 * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Co-resident clusters on the current device (0 on failure), cached.
+int mla_clusters() {
+  static std::mutex mu;
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] > 0) return cache[dev];
+  if (cudaFuncSetAttribute(mla_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+      cudaSuccess)
+    return 0;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, mla_partial_kernel, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = sms / 2;
+  }
+  cache[dev] = n;
+  return n;
+}
+
+}  // namespace
+
+int mla_ctas(const dcp_attn_desc&, const DeviceInfo&) { return mla_clusters(); }
+
+cudaError_t launch_mla(const dcp_attn_desc& d, const void* q, const ShardSet& sh, const RangeSpec& rs,
+                       float* o_parts, float* lses, void* ws, const WsLayout& L, int n_ctas, int32_t* err,
+                       cudaStream_t st) {
+  if (n_ctas <= 0 || mla_clusters() <= 0) return cudaErrorNotSupported;
+  MlaParams p;
+  memset(&p, 0, sizeof(p));
+  for (int i = 0; i < rs.N; ++i)
+    if (!latent_map(&p.tm_kv[i], sh.k[i], (uint64_t)sh.nblk[i] * kTile, kTile)) return cudaErrorNotSupported;
+  p.sh = sh;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.ws = static_cast<const char*>(ws);
+  p.L = L;
+  p.o_parts = o_parts;
+  p.lses = lses;
+  p.err = err;
+  p.B = rs.B;
+  p.sl2 = d.scale * kLog2e;
+  mla_partial_kernel<<<2 * n_ctas, kThreads, kSmemBytes, st>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace dcp

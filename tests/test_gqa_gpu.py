@@ -28,6 +28,7 @@ CASES = [
     ("gqa_mid", dict(batch=2, q_heads=12, kv_heads=4, ctx_fixed=700, shards=2, block_size=32)),  # g=3, Bs 32
     ("gqa_tiny", dict(batch=2, ctx_fixed=1500, shards=4, block_size=64, scale=1.0)),  # peaky softmax
     ("gqa_mid", dict(batch=1, ctx_fixed=0, shards=4)),       # one token only
+    ("gqa_mid", dict(batch=3, ctx_fixed=4000, shards=4, needles=3)),   # planted q-aligned keys
 ]
 
 

@@ -9,35 +9,28 @@
 // latent row and the value its first 512 entries (MLA keeps effectively one KV
 // head -- same write-up, section "なぜテンソル並列だとKVキャッシュが二重に載るのか").
 //
-// Why a CTA pair: the fp32 output accumulator of 128 heads x 512 dims is
-// 256 KB, all of one SM's tensor memory. Each work item runs on a 2-CTA
-// cluster that splits the latent columns:
-//   CTA r owns score columns [288 r, 288 r + 288) and output dims [256 r, 256 r + 256);
-//   it loads latent columns [256 r, 256 r + 320) of each page (5 x 64-column
-//   TMA boxes; 32 columns overlap, read twice from L2, once from HBM)
-// and per 64-token tile (= one paged block):
-//   1. S_r = Q_r . K_r^T  (M=128 heads, N=64 tokens, K=288) into TMEM; Q_r
-//      sits in TMEM as the A operand, the K box in shared memory is B
-//   2. each CTA sends its whole partial row block S_r to the other one through
-//      distributed shared memory (st.async, completion counted in bytes on the
-//      receiver's mbarrier: no per-thread release fences)
-//   3. both compute S = S_0 + S_1 (bitwise the same in both: a + b == b + a)
-//      and run the same online softmax over the 64 tokens, so they agree on
-//      the running max and the row sums without exchanging them
-//   4. P is written to shared memory as two bf16 terms, hi = bf16(p) and
-//      lo = bf16(p - hi): P.V then carries ~16 mantissa bits of p
-//   5. O_r += P_hi . V_r + P_lo . V_r  (M=128, N=256, K=64) into TMEM.
-// Every KV byte is read from HBM once; the only recomputation is the softmax
-// (exp on 64 tokens instead of 32 per CTA). O is rescaled lazily, only when
-// the running max grows by more than 2^8.
-//
-// Roles per CTA (192 threads): warps 0-3 softmax + epilogue (thread h owns
-// query head h = TMEM lane h), warp 4 lane 0 TMA producer, warp 5 lane 0 MMA
-// issuer (warp 5 also allocates TMEM). Every barrier's phases are observed by
-// its waiter in order and never more than one phase late, so parity waits are
-// unambiguous; the end of a tile's P.V is read from the release of its P
-// buffer. Every wait is bounded: on expiry the kernel raises
-// DCP_DEVERR_TIMEOUT, stops all roles, drains what it issued and frees TMEM.
+// Layout of the work: the fp32 output accumulator of 128 heads x 512 dims is
+// 256 KB, all of one SM's tensor memory, so each work item runs on a 2-CTA
+// cluster and CTA r accumulates output dims [256 r, 256 r + 256). The two
+// CTAs share no data: each computes the full scores S = Q K^T of the tile
+// itself (the score MMA is repeated, 53 % of the flops) because moving the
+// 32 KB of fp32 partial scores per tile between two SMs costs more: the
+// SM-to-SM network measured ~9 B/clk per direction on this part, against
+// ~23 B/clk of HBM bandwidth per SM. Both CTAs stream the same pages, so the
+// second read of each page hits L2. Per 64-token tile (= one paged block):
+//   1. S = Q . K^T (M=128 heads, N=64 tokens, K=576) into TMEM; query dims
+//      0-383 are the MMA's A operand in TMEM, dims 384-575 in shared memory
+//   2. online softmax per head row (thread h owns TMEM lane h), in log2 units,
+//      lazy rescale of O (only when the running max grows by more than 2^8)
+//   3. P is written to shared memory as two bf16 terms, hi = bf16(p) and
+//      lo = bf16(p - hi), so P.V carries ~16 mantissa bits of p
+//   4. O_r += P_hi . V_r + P_lo . V_r (M=128, N=256, K=64) into TMEM.
+// TMA brings each page as nine 64-column, 128-byte-swizzled boxes into a
+// 2-stage ring; one thread issues all MMAs; 4 warps run the softmax and the
+// epilogue. Every barrier's phases are observed in order and never more than
+// one phase late, so parity waits are unambiguous; every wait is bounded: on
+// expiry the kernel raises DCP_DEVERR_TIMEOUT, stops all roles, drains what
+// it issued and frees TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -51,35 +44,37 @@ namespace dcp {
 namespace {
 
 constexpr int kHeads = 128;
+constexpr int kDk = 576;
 constexpr int kDv = 512;
 constexpr int kTile = 64;                        // tokens per tile: one paged block
-constexpr int kChunks = 5;                       // 64-column boxes loaded per page per CTA
-constexpr int kKSteps = 18;                      // 16-column k-steps of the score MMA per CTA
-constexpr int kStages = 3;                       // K/V tile pipeline depth
+constexpr int kChunks = 9;                       // 64-column boxes per page (576 columns)
+constexpr int kKStepsTmem = 24;                  // query dims 0-383: A operand in TMEM
+constexpr int kKSteps = 36;                      // 16-column k-steps of the score MMA
+constexpr int kQSmemChunks = 3;                  // query dims 384-575 in shared memory
+constexpr int kStages = 2;                       // K/V tile pipeline depth
 constexpr int kThreads = 192;
 constexpr int kKvChunkBytes = kTile * 128;       // 64 rows x 64 bf16
 constexpr int kStageBytes = kChunks * kKvChunkBytes;
+constexpr int kQChunkBytes = kHeads * 128;       // 128 rows x 64 bf16
 constexpr int kPBytes = kHeads * 128;            // 128 heads x 64 tokens bf16 (one term)
-constexpr int kXBytes = kHeads * kTile * 4;      // the peer's partial scores, fp32
 
 constexpr int kOffKv = 0;
-constexpr int kOffP = kOffKv + kStages * kStageBytes;   // P[pb][term] at kOffP + (2 pb + term) kPBytes
-constexpr int kOffX = kOffP + 4 * kPBytes;
-constexpr int kOffBar = kOffX + kXBytes;
-constexpr int kNumBars = 24;
+constexpr int kOffQ = kOffKv + kStages * kStageBytes;
+constexpr int kOffP = kOffQ + kQSmemChunks * kQChunkBytes;  // hi at kOffP, lo at kOffP + kPBytes
+constexpr int kOffBar = kOffP + 2 * kPBytes;
+constexpr int kNumBars = 16;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag
 constexpr int kSmemUsed = kOffMisc + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;      // slack to align the base to 1024
 
 // barrier slots
-constexpr int BQ_FULL = 0, BQ_EMPTY = 1, BS_FULL = 2, BS_EMPTY = 3, BX_FULL = 4, BX_FREE = 5, BX_READ = 6,
-              BDRAIN = 7, BKV_FULL = 8, BKV_EMPTY = 8 + kStages, BP_FULL = 8 + 2 * kStages,
-              BP_EMPTY = 10 + 2 * kStages;
+constexpr int BQ_FULL = 0, BQ_EMPTY = 1, BS_FULL = 2, BS_EMPTY = 3, BP_FULL = 4, BP_EMPTY = 5, BDRAIN = 6,
+              BKV_FULL = 7, BKV_EMPTY = 7 + kStages;
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;       // 256 columns: O_r, fp32
-constexpr uint32_t kColS = 256;     // 64 columns: S_r, fp32
-constexpr uint32_t kColQ = 320;     // 144 columns: Q_r, bf16 pairs
+constexpr uint32_t kColS = 256;     // 64 columns: S, fp32
+constexpr uint32_t kColQ = 320;     // 192 columns: query dims 0-383, bf16 pairs
 constexpr uint32_t kSpinLimit = 1u << 24;
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -87,6 +82,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;       // log2 units
 
 struct MlaParams {
+  CUtensorMap tm_q;
   CUtensorMap tm_kv[kMaxShards];
   ShardSet sh;
   const __nv_bfloat16* q;
@@ -109,14 +105,6 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ uint32_t peer_addr(uint32_t a, uint32_t peer) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(a), "r"(peer));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-}
 __device__ __forceinline__ void bar_init(uint32_t b, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(b), "r"(count));
 }
@@ -125,11 +113,6 @@ __device__ __forceinline__ void bar_arrive(uint32_t b) {
 }
 __device__ __forceinline__ void bar_arrive_tx(uint32_t b, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(b), "r"(bytes) : "memory");
-}
-// arrive on the barrier at the same offset in the peer CTA (orders this
-// thread's prior shared::cluster stores before the arrival)
-__device__ __forceinline__ void bar_arrive_peer(uint32_t b, uint32_t peer) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(peer_addr(b, peer)) : "memory");
 }
 __device__ __forceinline__ bool bar_try(uint32_t b, uint32_t parity) {
   uint32_t ok;
@@ -236,19 +219,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
-// 16 bytes into the peer's shared memory; completion is counted on the
-// peer's mbarrier (transaction bytes), so no release fence is needed.
-__device__ __forceinline__ void st_async_peer(uint32_t remote, uint32_t remote_bar, uint32_t a, uint32_t b,
-                                              uint32_t c, uint32_t d) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];\n"
-               ::"r"(remote), "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar) : "memory");
-}
-__device__ __forceinline__ uint4 ld_local_v4(uint32_t a) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a)
-               : "memory");
-  return v;
-}
 // hi = bf16(x), lo = bf16(x - hi), for a pair of values
 __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
@@ -257,6 +227,7 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
   hi = *reinterpret_cast<const uint32_t*>(&h);
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
+
 
 // Shared geometry of one work item, derived identically by every role.
 struct ItemGeom {
@@ -291,7 +262,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t raw = saddr(smem_raw);
   unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   const uint32_t sbase = saddr(smem);
-  const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
+  const uint32_t rank = cluster_rank();
   const int cluster = blockIdx.x >> 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto bar = [&](int i) { return sbase + kOffBar + 8u * i; };
@@ -299,25 +270,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
 
   if (threadIdx.x == 0) {
-    bar_init(bar(BQ_FULL), kHeads);
+    bar_init(bar(BQ_FULL), 1 + kHeads);  // producer's copy of Q[:, 384:576] + softmax threads' Q[:, 0:384]
     bar_init(bar(BQ_EMPTY), 1);
     bar_init(bar(BS_FULL), 1);
     bar_init(bar(BS_EMPTY), kHeads);
-    bar_init(bar(BX_FULL), 1);       // armed with the byte count of the peer's scores
-    bar_init(bar(BX_FREE), 1);       // the peer's thread 0: "your scores were read"
-    bar_init(bar(BX_READ), kHeads);  // local softmax threads read the peer's scores
+    bar_init(bar(BP_FULL), kHeads);
+    bar_init(bar(BP_EMPTY), 1);
     bar_init(bar(BDRAIN), 1);
     for (int s = 0; s < kStages; ++s) {
       bar_init(bar(BKV_FULL + s), 1);
       bar_init(bar(BKV_EMPTY + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      bar_init(bar(BP_FULL + s), kHeads);
-      bar_init(bar(BP_EMPTY + s), 1);
-    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    bar_arrive_tx(bar(BX_FULL), kXBytes);  // phase 0 expects the peer's first tile
   }
   if (warp == 5) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(saddr(tmem_slot)),
@@ -326,7 +291,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // the peer's barriers exist (and X_FULL is armed) before any remote traffic
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -337,11 +301,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t fills = 0;  // K/V tiles issued (global across items)
-      const int col_base = 256 * (int)rank;
+      int n_items = 0;
       bool stop = false;
       for (int k = k_begin; k < k_end && !stop; ++k) {
         const ItemGeom g = item_geom(p, k);
-        int phys_next = g.t0 < g.t1 ? tile_block(p, g, g.t0) : -1;
+        int phys_next = tile_block(p, g, g.t0);
+        if (n_items > 0 && !wait_bar(bar(BQ_EMPTY), (n_items - 1) & 1, abort_flag, p.err, false)) break;
+        bar_arrive_tx(bar(BQ_FULL), kQSmemChunks * kQChunkBytes);
+        for (int c = 0; c < kQSmemChunks; ++c)
+          tma_load(sbase + kOffQ + c * kQChunkBytes, &p.tm_q, 384 + 64 * c, g.b * kHeads, bar(BQ_FULL));
         for (int t = g.t0; t < g.t1; ++t) {
           const int phys = phys_next;
           if (t + 1 < g.t1) phys_next = tile_block(p, g, t + 1);  // one tile ahead: off the issue path
@@ -354,12 +322,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int row = phys < 0 ? -kTile : phys * kTile;  // out of range: the copy reads zeros
           bar_arrive_tx(bar(BKV_FULL + s), kChunks * kKvChunkBytes);
           for (int c = 0; c < kChunks; ++c)
-            tma_load(sbase + kOffKv + s * kStageBytes + c * kKvChunkBytes, &p.tm_kv[g.shard], col_base + 64 * c,
-                     row, bar(BKV_FULL + s));
+            tma_load(sbase + kOffKv + s * kStageBytes + c * kKvChunkBytes, &p.tm_kv[g.shard], 64 * c, row,
+                     bar(BKV_FULL + s));
           ++fills;
         }
+        ++n_items;
       }
       if (*abort_flag) {  // copies in flight must land before the CTA may exit
+        if (n_items > 0) drain_bar(bar(BQ_FULL), (n_items - 1) & 1u);
         const uint32_t f0 = fills > (uint32_t)kStages ? fills - kStages : 0;
         for (uint32_t f = f0; f < fills; ++f) drain_bar(bar(BKV_FULL + f % kStages), (f / kStages) & 1u);
       }
@@ -369,22 +339,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t id_s = idesc(128, 64, 0);
       const uint32_t id_pv = idesc(128, 256, 1);
-      const int koff = 2 * (int)rank;  // CTA 1's first score column is 32 into its first box
       uint32_t gt = 0;
       int n_items = 0;
       auto pv = [&](uint32_t gi, bool first) -> bool {
-        const uint32_t pb = gi & 1u, s = gi % kStages;
-        if (!wait_bar(bar(BP_FULL + pb), (gi >> 1) & 1u, abort_flag, p.err, false)) return false;
+        const uint32_t s = gi % kStages;
+        if (!wait_bar(bar(BP_FULL), gi & 1u, abort_flag, p.err, false)) return false;
         tc_fence_after();
-        const uint32_t va = sbase + kOffKv + s * kStageBytes;
+        const uint32_t va = sbase + kOffKv + s * kStageBytes + 4 * rank * kKvChunkBytes;  // V dims of this CTA
         for (int term = 0; term < 2; ++term) {
-          const uint32_t pa = sbase + kOffP + (2 * pb + term) * kPBytes;
+          const uint32_t pa = sbase + kOffP + term * kPBytes;
           for (int kt = 0; kt < kTile / 16; ++kt)
             mma(tmem + kColO, sdesc(pa + 32 * kt, 0), sdesc(va + 2048 * kt, kKvChunkBytes), id_pv,
                 (first && term == 0 && kt == 0) ? 0 : 1);
         }
         mma_commit(bar(BKV_EMPTY + s));
-        mma_commit(bar(BP_EMPTY + pb));  // also tells softmax that this P.V finished
+        mma_commit(bar(BP_EMPTY));  // also tells softmax that this P.V finished
         return true;
       };
       bool ok = true;
@@ -400,9 +369,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t ka = sbase + kOffKv + s * kStageBytes;
           for (int kk = 0; kk < kKSteps; ++kk) {
-            const int gk = kk + koff;  // 16-column step within this CTA's five boxes
-            mma_ts(tmem + kColS, tmem + kColQ + 8 * kk, sdesc(ka + (gk >> 2) * kKvChunkBytes + 32 * (gk & 3), 0),
-                   id_s, kk > 0);
+            const uint64_t bdesc = sdesc(ka + (kk >> 2) * kKvChunkBytes + 32 * (kk & 3), 0);
+            if (kk < kKStepsTmem) {
+              mma_ts(tmem + kColS, tmem + kColQ + 8 * kk, bdesc, id_s, kk > 0);
+            } else {
+              const int qk = kk - kKStepsTmem;
+              mma(tmem + kColS, sdesc(sbase + kOffQ + (qk >> 2) * kQChunkBytes + 32 * (qk & 3), 0), bdesc, id_s, 1);
+            }
           }
           mma_commit(bar(BS_FULL));
           if (j == nt - 1) mma_commit(bar(BQ_EMPTY));
@@ -420,25 +393,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ softmax / epilogue
     const int h = threadIdx.x;  // query head = TMEM lane
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t x_row = sbase + kOffX + h * (kTile * 4);
-    const uint32_t x_row_peer = peer_addr(x_row, peer);
-    const uint32_t x_full_peer = peer_addr(bar(BX_FULL), peer);
-    const int qd0 = 288 * (int)rank;
+    const int vlo = 4 * (int)rank;  // first V box of this CTA
     uint32_t gt = 0;
     int n_items = 0;
     bool ok = true;
     for (int k = k_begin; k < k_end && ok; ++k) {
       const ItemGeom g = item_geom(p, k);
       const int nt = g.t1 - g.t0;
-      // queries of this item into TMEM (after the previous item's score MMAs)
+      // query dims 0-383 of this item into TMEM (after the previous item's score MMAs)
       if (n_items > 0 && !wait_warp(bar(BQ_EMPTY), (n_items - 1) & 1, abort_flag, p.err, false)) break;
       tc_fence_after();
       {
-        const uint4* qr = reinterpret_cast<const uint4*>(p.q + ((size_t)g.b * kHeads + h) * 576 + qd0);
+        const uint4* qr = reinterpret_cast<const uint4*>(p.q + ((size_t)g.b * kHeads + h) * kDk);
         uint32_t qv[16];
         __syncwarp();
 #pragma unroll 1
-        for (int c = 0; c < 9; ++c) {
+        for (int c = 0; c < 12; ++c) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const uint4 v = qr[4 * c + i];
@@ -455,10 +425,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bar_arrive(bar(BQ_FULL));
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < nt; ++j) {
-        const uint32_t gi = gt + j, pb = gi & 1u, s = gi % kStages;
+        const uint32_t gi = gt + j, s = gi % kStages;
         const int t = g.t0 + j;
         const int phys = tile_block(p, g, t);  // its latency hides behind the score wait
-        // 1. this CTA's partial scores
+        // 1. scores of the tile
         if (!wait_warp(bar(BS_FULL), gi & 1u, abort_flag, p.err, false)) { ok = false; break; }
         tc_fence_after();
         uint32_t sv[64];
@@ -468,39 +438,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         tc_fence_before();
         bar_arrive(bar(BS_EMPTY));
-        // 2. send them to the peer once it has read the previous tile's
-        if (gi >= 1 && !wait_warp(bar(BX_FREE), (gi - 1) & 1u, abort_flag, p.err, true)) { ok = false; break; }
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          st_async_peer(x_row_peer + 16 * i, x_full_peer, sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]);
-        // 3. the peer's partial scores -> full scores (same bits in both CTAs)
-        if (!wait_warp(bar(BX_FULL), gi & 1u, abort_flag, p.err, true)) { ok = false; break; }
-        float sc[64];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint4 v = ld_local_v4(x_row + 16 * i);
-          sc[4 * i] = __uint_as_float(sv[4 * i]) + __uint_as_float(v.x);
-          sc[4 * i + 1] = __uint_as_float(sv[4 * i + 1]) + __uint_as_float(v.y);
-          sc[4 * i + 2] = __uint_as_float(sv[4 * i + 2]) + __uint_as_float(v.z);
-          sc[4 * i + 3] = __uint_as_float(sv[4 * i + 3]) + __uint_as_float(v.w);
-        }
-        bar_arrive(bar(BX_READ));
-        if (h == 0) {
-          // every row read: arm the next phase, then let the peer send again
-          if (!wait_bar(bar(BX_READ), gi & 1u, abort_flag, p.err, false)) {
-            ok = false;
-          } else {
-            bar_arrive_tx(bar(BX_FULL), kXBytes);
-            bar_arrive_peer(bar(BX_FREE), peer);
-          }
-        }
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        // 4. online softmax over the 64 tokens (log2 units)
+        // 2. online softmax over the 64 tokens (log2 units)
         const int n_valid = phys < 0 ? 0 : min(kTile, g.hi - (g.lo + kTile * t));
+        float sc[64];
         float mx = -INFINITY;
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
-          sc[i] = i < n_valid ? sc[i] * p.sl2 : -INFINITY;
+          sc[i] = i < n_valid ? __uint_as_float(sv[i]) * p.sl2 : -INFINITY;
           mx = fmaxf(mx, sc[i]);
         }
         float m_new = m_run, alpha = 1.f;
@@ -513,14 +457,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           rescale = true;
         }
         const float ref = m_new == -INFINITY ? 0.f : m_new;
-        // 5. P buffer pb is free once the P.V two tiles back has finished
-        if (gi >= 2 && !wait_warp(bar(BP_EMPTY + pb), ((gi >> 1) - 1) & 1u, abort_flag, p.err, false)) {
-          ok = false;
-          break;
-        }
+        // 3. the P buffer and O are free once the previous tile's P.V has finished
+        if (gi >= 1 && !wait_warp(bar(BP_EMPTY), (gi - 1) & 1u, abort_flag, p.err, false)) { ok = false; break; }
         float lsum = 0.f;
         {
-          const uint32_t hrow = sbase + kOffP + (2 * pb) * kPBytes + h * 128;
+          const uint32_t hrow = sbase + kOffP + h * 128;
           const uint32_t lrow = hrow + kPBytes;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
@@ -538,18 +479,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         l_run = l_run * alpha + lsum;
         m_run = m_new;
-        // 6. V rows past the end of a partial tile may hold anything: zero them
+        // 4. V rows past the end of a partial tile may hold anything: zero them
         if (n_valid < kTile) {
           const int rows = kTile - n_valid;
           for (int e = h; e < rows * 4 * 8; e += kHeads) {
-            const int r = n_valid + e / 32, c = (e >> 3) & 3, piece = e & 7;
+            const int r = n_valid + e / 32, c = vlo + ((e >> 3) & 3), piece = e & 7;
             st_local_v4(sbase + kOffKv + s * kStageBytes + c * kKvChunkBytes + r * 128 + piece * 16, 0u, 0u, 0u, 0u);
           }
         }
-        // 7. lazy rescale of O after the previous P.V (warp-wide: TMEM access is per warp)
+        // 5. lazy rescale of O (warp-wide: TMEM access is per warp; the others multiply by 1)
         if (__any_sync(0xffffffffu, rescale)) {
-          const uint32_t gp = gi - 1;
-          if (!wait_warp(bar(BP_EMPTY + (gp & 1u)), (gp >> 1) & 1u, abort_flag, p.err, false)) { ok = false; break; }
           tc_fence_after();
           uint32_t ov[32];
           __syncwarp();
@@ -563,15 +502,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           tmem_wait_st();
         }
-        // 8. publish P to the MMA issuer
+        // 6. publish P to the MMA issuer
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
         tc_fence_before();
-        bar_arrive(bar(BP_FULL + pb));
+        bar_arrive(bar(BP_FULL));
       }
       if (!ok) break;
       // epilogue: wait for the last P.V, then write O_r / l and the LSE
       const uint32_t glast = gt + nt - 1;
-      if (!wait_warp(bar(BP_EMPTY + (glast & 1u)), (glast >> 1) & 1u, abort_flag, p.err, false)) break;
+      if (!wait_warp(bar(BP_EMPTY), glast & 1u, abort_flag, p.err, false)) break;
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       float* out;
@@ -610,7 +549,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols));
   }
-  cluster_sync();
 }
 
 // ---------------------------------------------------------------------------
@@ -686,6 +624,7 @@ cudaError_t launch_mla(const dcp_attn_desc& d, const void* q, const ShardSet& sh
   if (n_ctas <= 0 || mla_clusters() <= 0) return cudaErrorNotSupported;
   MlaParams p;
   memset(&p, 0, sizeof(p));
+  if (!latent_map(&p.tm_q, q, (uint64_t)rs.B * kHeads, kHeads)) return cudaErrorNotSupported;
   for (int i = 0; i < rs.N; ++i)
     if (!latent_map(&p.tm_kv[i], sh.k[i], (uint64_t)sh.nblk[i] * kTile, kTile)) return cudaErrorNotSupported;
   p.sh = sh;

@@ -24,7 +24,12 @@
 //      lazy rescale of O (only when the running max grows by more than 2^8)
 //   3. P is written to shared memory as two bf16 terms, hi = bf16(p) and
 //      lo = bf16(p - hi), so P.V carries ~16 mantissa bits of p
-//   4. O_r += P_hi . V_r + P_lo . V_r (M=128, N=256, K=64) into TMEM.
+//   4. O_r += P_hi . V_r (M=128, N=256, K=64) into TMEM, plus P_lo . V_r for
+//      tiles that carry more than 1/32 of some row's running weight (the
+//      first tiles of an item, or a tile with a dominant token); for the
+//      others, dropping the residual changes O by at most 2^-9 x (that
+//      tile's share of the row weight, < 1/32) x max|v|, and the MMA is
+//      skipped.
 // TMA brings each page as nine 64-column, 128-byte-swizzled boxes into a
 // 2-stage ring; one thread issues all MMAs; 4 warps run the softmax and the
 // epilogue. Every barrier's phases are observed in order and never more than
@@ -52,6 +57,7 @@ constexpr int kKStepsTmem = 24;                  // query dims 0-383: A operand 
 constexpr int kKSteps = 36;                      // 16-column k-steps of the score MMA
 constexpr int kQSmemChunks = 3;                  // query dims 384-575 in shared memory
 constexpr int kStages = 2;                       // K/V tile pipeline depth
+constexpr int kPrefetch = 4;                     // pages pulled into L2 ahead of the ring
 constexpr int kThreads = 192;
 constexpr int kKvChunkBytes = kTile * 128;       // 64 rows x 64 bf16
 constexpr int kStageBytes = kChunks * kKvChunkBytes;
@@ -64,7 +70,7 @@ constexpr int kOffP = kOffQ + kQSmemChunks * kQChunkBytes;  // hi at kOffP, lo a
 constexpr int kOffBar = kOffP + 2 * kPBytes;
 constexpr int kNumBars = 16;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag
-constexpr int kSmemUsed = kOffMisc + 16;
+constexpr int kSmemUsed = kOffMisc + 32;
 constexpr int kSmemBytes = kSmemUsed + 1024;      // slack to align the base to 1024
 
 // barrier slots
@@ -80,6 +86,7 @@ constexpr uint32_t kSpinLimit = 1u << 24;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;       // log2 units
+constexpr float kLoFraction = 1.0f / 32.0f;      // tile share of the row sum above which P_lo . V is issued
 
 struct MlaParams {
   CUtensorMap tm_q;
@@ -156,6 +163,11 @@ __device__ __forceinline__ void drain_bar(uint32_t b, uint32_t parity) {
     if (bar_try(b, parity)) return;
 }
 
+// pull a box into L2 only (no shared memory, no barrier)
+__device__ __forceinline__ void tma_prefetch(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y) : "memory");
+}
 __device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n"
@@ -268,6 +280,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return sbase + kOffBar + 8u * i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 8);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* lo_flags = reinterpret_cast<volatile int*>(smem + kOffMisc + 16);  // one per softmax warp
 
   if (threadIdx.x == 0) {
     bar_init(bar(BQ_FULL), 1 + kHeads);  // producer's copy of Q[:, 384:576] + softmax threads' Q[:, 0:384]
@@ -299,92 +312,150 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t fills = 0;  // K/V tiles issued (global across items)
-      int n_items = 0;
-      bool stop = false;
-      for (int k = k_begin; k < k_end && !stop; ++k) {
-        const ItemGeom g = item_geom(p, k);
-        int phys_next = tile_block(p, g, g.t0);
-        if (n_items > 0 && !wait_bar(bar(BQ_EMPTY), (n_items - 1) & 1, abort_flag, p.err, false)) break;
-        bar_arrive_tx(bar(BQ_FULL), kQSmemChunks * kQChunkBytes);
-        for (int c = 0; c < kQSmemChunks; ++c)
-          tma_load(sbase + kOffQ + c * kQChunkBytes, &p.tm_q, 384 + 64 * c, g.b * kHeads, bar(BQ_FULL));
-        for (int t = g.t0; t < g.t1; ++t) {
-          const int phys = phys_next;
-          if (t + 1 < g.t1) phys_next = tile_block(p, g, t + 1);  // one tile ahead: off the issue path
+    // The whole warp reads block-table entries 32 tiles at a time (lane i
+    // holds tile base + i); lane 0 issues the copies. Pages kPrefetch tiles
+    // ahead of the ring are pulled into L2, so the ring's copies hit L2.
+    uint32_t fills = 0;  // K/V tiles issued (global across items)
+    int n_items = 0;
+    bool stop = false;
+    for (int k = k_begin; k < k_end && !stop; ++k) {
+      const ItemGeom g = item_geom(p, k);
+      const int nt = g.t1 - g.t0;
+      int cur = lane < nt ? tile_block(p, g, g.t0 + lane) : -1;
+      int nxt = 32 + lane < nt ? tile_block(p, g, g.t0 + 32 + lane) : -1;
+      bool ok = true;
+      if (lane == 0) {
+        if (n_items > 0 && !wait_bar(bar(BQ_EMPTY), (n_items - 1) & 1, abort_flag, p.err, false)) {
+          ok = false;
+        } else {
+          bar_arrive_tx(bar(BQ_FULL), kQSmemChunks * kQChunkBytes);
+          for (int c = 0; c < kQSmemChunks; ++c)
+            tma_load(sbase + kOffQ + c * kQChunkBytes, &p.tm_q, 384 + 64 * c, g.b * kHeads, bar(BQ_FULL));
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) { stop = true; break; }
+      for (int j = 0; j < nt; ++j) {
+        if ((j & 31) == 0 && j > 0) {
+          cur = nxt;
+          nxt = j + 32 + lane < nt ? tile_block(p, g, g.t0 + j + 32 + lane) : -1;
+        }
+        const int phys = __shfl_sync(0xffffffffu, cur, j & 31);
+        const int jp = j + kPrefetch;
+        const int phys_pf = __shfl_sync(0xffffffffu, ((jp >> 5) == (j >> 5)) ? cur : nxt, jp & 31);
+        if (lane == 0) {
           const uint32_t s = fills % kStages, use = fills / kStages;
           if (use > 0 && !wait_bar(bar(BKV_EMPTY + s), (use - 1) & 1u, abort_flag, p.err, false)) {
-            stop = true;
-            break;
+            ok = false;
+          } else {
+            if (phys < 0 && rank == 0) raise_flag(p.err, DCP_DEVERR_BLOCK_RANGE);
+            const int row = phys < 0 ? -kTile : phys * kTile;  // out of range: the copy reads zeros
+            bar_arrive_tx(bar(BKV_FULL + s), kChunks * kKvChunkBytes);
+            for (int c = 0; c < kChunks; ++c)
+              tma_load(sbase + kOffKv + s * kStageBytes + c * kKvChunkBytes, &p.tm_kv[g.shard], 64 * c, row,
+                       bar(BKV_FULL + s));
+            (void)phys_pf;
           }
-          if (phys < 0 && rank == 0) raise_flag(p.err, DCP_DEVERR_BLOCK_RANGE);
-          const int row = phys < 0 ? -kTile : phys * kTile;  // out of range: the copy reads zeros
-          bar_arrive_tx(bar(BKV_FULL + s), kChunks * kKvChunkBytes);
-          for (int c = 0; c < kChunks; ++c)
-            tma_load(sbase + kOffKv + s * kStageBytes + c * kKvChunkBytes, &p.tm_kv[g.shard], 64 * c, row,
-                     bar(BKV_FULL + s));
-          ++fills;
         }
-        ++n_items;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) { stop = true; break; }
+        ++fills;
       }
-      if (*abort_flag) {  // copies in flight must land before the CTA may exit
-        if (n_items > 0) drain_bar(bar(BQ_FULL), (n_items - 1) & 1u);
-        const uint32_t f0 = fills > (uint32_t)kStages ? fills - kStages : 0;
-        for (uint32_t f = f0; f < fills; ++f) drain_bar(bar(BKV_FULL + f % kStages), (f / kStages) & 1u);
-      }
+      ++n_items;
+    }
+    if (lane == 0 && *abort_flag) {  // copies in flight must land before the CTA may exit
+      if (n_items > 0) drain_bar(bar(BQ_FULL), (n_items - 1) & 1u);
+      const uint32_t f0 = fills > (uint32_t)kStages ? fills - kStages : 0;
+      for (uint32_t f = f0; f < fills; ++f) drain_bar(bar(BKV_FULL + f % kStages), (f / kStages) & 1u);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t id_s = idesc(128, 64, 0);
       const uint32_t id_pv = idesc(128, 256, 1);
-      uint32_t gt = 0;
-      int n_items = 0;
-      auto pv = [&](uint32_t gi, bool first) -> bool {
-        const uint32_t s = gi % kStages;
-        if (!wait_bar(bar(BP_FULL), gi & 1u, abort_flag, p.err, false)) return false;
-        tc_fence_after();
-        const uint32_t va = sbase + kOffKv + s * kStageBytes + 4 * rank * kKvChunkBytes;  // V dims of this CTA
-        for (int term = 0; term < 2; ++term) {
-          const uint32_t pa = sbase + kOffP + term * kPBytes;
-          for (int kt = 0; kt < kTile / 16; ++kt)
-            mma(tmem + kColO, sdesc(pa + 32 * kt, 0), sdesc(va + 2048 * kt, kKvChunkBytes), id_pv,
-                (first && term == 0 && kt == 0) ? 0 : 1);
-        }
-        mma_commit(bar(BKV_EMPTY + s));
-        mma_commit(bar(BP_EMPTY));  // also tells softmax that this P.V finished
-        return true;
+      const uint64_t kdesc0 = sdesc(sbase + kOffKv, 0);
+      const uint64_t qdesc0 = sdesc(sbase + kOffQ, 0);
+      const uint64_t pdesc0 = sdesc(sbase + kOffP, 0);
+      const uint64_t vdesc0 = sdesc(sbase + kOffKv + 4 * rank * kKvChunkBytes, kKvChunkBytes);
+      // Event-driven issue: the score MMA of the next tile and the P.V of the
+      // oldest tile whose P is ready go out as soon as their inputs are, so
+      // a late page copy never holds back the P.V that frees a stage.
+      auto n_tiles = [&](int k) {
+        const ItemRec it = reinterpret_cast<const ItemRec*>(p.ws + p.L.items_off)[k];
+        return it.t1 - it.t0;
       };
-      bool ok = true;
-      for (int k = k_begin; k < k_end && ok; ++k) {
-        const ItemGeom g = item_geom(p, k);
-        const int nt = g.t1 - g.t0;
-        if (!wait_bar(bar(BQ_FULL), n_items & 1, abort_flag, p.err, false)) break;
-        tc_fence_after();
-        for (int j = 0; j < nt && ok; ++j) {
-          const uint32_t gi = gt + j, s = gi % kStages;
-          if (!wait_bar(bar(BKV_FULL + s), (gi / kStages) & 1u, abort_flag, p.err, false)) { ok = false; break; }
-          if (gi >= 1 && !wait_bar(bar(BS_EMPTY), (gi - 1) & 1u, abort_flag, p.err, false)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t ka = sbase + kOffKv + s * kStageBytes;
-          for (int kk = 0; kk < kKSteps; ++kk) {
-            const uint64_t bdesc = sdesc(ka + (kk >> 2) * kKvChunkBytes + 32 * (kk & 3), 0);
-            if (kk < kKStepsTmem) {
-              mma_ts(tmem + kColS, tmem + kColQ + 8 * kk, bdesc, id_s, kk > 0);
-            } else {
-              const int qk = kk - kKStepsTmem;
-              mma(tmem + kColS, sdesc(sbase + kOffQ + (qk >> 2) * kQChunkBytes + 32 * (qk & 3), 0), bdesc, id_s, 1);
-            }
+      int ks = k_begin, js = 0, nts = ks < k_end ? n_tiles(ks) : 0;  // next score tile
+      int kp = k_begin, jp = 0, ntp = nts;                            // next P.V tile
+      uint32_t g_s = 0, g_p = 0, q_loads = 0;
+      bool q_ready = false;
+      uint32_t idle = 0;
+      while (kp < k_end) {
+        bool progressed = false;
+        if (ks < k_end) {
+          if (!q_ready && bar_try(bar(BQ_FULL), q_loads & 1u)) {
+            q_ready = true;
+            tc_fence_after();
           }
-          mma_commit(bar(BS_FULL));
-          if (j == nt - 1) mma_commit(bar(BQ_EMPTY));
-          if (j >= 1 && !pv(gi - 1, j == 1)) { ok = false; break; }
+          const uint32_t s = g_s % kStages;
+          if (q_ready && bar_try(bar(BKV_FULL + s), (g_s / kStages) & 1u) &&
+              (g_s == 0 || bar_try(bar(BS_EMPTY), (g_s - 1) & 1u))) {
+            tc_fence_after();
+            // descriptors advance by (byte offset >> 4) in their address field
+            const uint64_t kd = kdesc0 + (uint64_t)((s * kStageBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < kKSteps; ++kk) {
+              const uint64_t bdesc = kd + (uint64_t)((((kk >> 2) * kKvChunkBytes) + 32 * (kk & 3)) >> 4);
+              if (kk < kKStepsTmem) {
+                mma_ts(tmem + kColS, tmem + kColQ + 8 * kk, bdesc, id_s, kk > 0);
+              } else {
+                const int qk = kk - kKStepsTmem;
+                mma(tmem + kColS, qdesc0 + (uint64_t)((((qk >> 2) * kQChunkBytes) + 32 * (qk & 3)) >> 4), bdesc,
+                    id_s, 1);
+              }
+            }
+            mma_commit(bar(BS_FULL));
+            if (++js == nts) {  // last score tile of the item: its queries may be replaced
+              mma_commit(bar(BQ_EMPTY));
+              ++ks;
+              js = 0;
+              nts = ks < k_end ? n_tiles(ks) : 0;
+              ++q_loads;
+              q_ready = false;
+            }
+            ++g_s;
+            progressed = true;
+          }
         }
-        if (!ok) break;
-        if (!pv(gt + nt - 1, nt == 1)) break;
-        gt += nt;
-        ++n_items;
+        if (g_p < g_s && bar_try(bar(BP_FULL), g_p & 1u)) {
+          tc_fence_after();
+          const uint32_t s = g_p % kStages;
+          const uint64_t vd = vdesc0 + (uint64_t)((s * kStageBytes) >> 4);  // V dims of this CTA
+          const int terms = (lo_flags[0] | lo_flags[1] | lo_flags[2] | lo_flags[3]) ? 2 : 1;
+#pragma unroll
+          for (int term = 0; term < 2; ++term) {
+            if (term >= terms) break;
+#pragma unroll
+            for (int kt = 0; kt < kTile / 16; ++kt)
+              mma(tmem + kColO, pdesc0 + (uint64_t)((term * kPBytes + 32 * kt) >> 4),
+                  vd + (uint64_t)((2048 * kt) >> 4), id_pv, (jp == 0 && term == 0 && kt == 0) ? 0 : 1);
+          }
+          mma_commit(bar(BKV_EMPTY + s));
+          mma_commit(bar(BP_EMPTY));  // also tells softmax that this P.V finished
+          if (++jp == ntp) {
+            ++kp;
+            jp = 0;
+            ntp = kp < k_end ? n_tiles(kp) : 0;
+          }
+          ++g_p;
+          progressed = true;
+        }
+        if (progressed) {
+          idle = 0;
+        } else if (++idle >= kSpinLimit) {
+          *abort_flag = 1;
+          raise_flag(p.err, DCP_DEVERR_TIMEOUT);
+          break;
+        } else if ((idle & 63u) == 0 && *abort_flag) {
+          break;
+        }
       }
       mma_commit(bar(BDRAIN));  // all issued MMAs complete before TMEM may be freed
       drain_bar(bar(BDRAIN), 0);
@@ -479,6 +550,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         l_run = l_run * alpha + lsum;
         m_run = m_new;
+        // The residual term matters only where this tile carries a noticeable
+        // share of the row's weight (the first tiles of an item, or a tile
+        // with a dominant token); elsewhere its P.V is skipped.
+        {
+          const bool any_lo = __any_sync(0xffffffffu, lsum > kLoFraction * l_run);
+          if (lane == 0) lo_flags[warp] = any_lo ? 1 : 0;
+        }
         // 4. V rows past the end of a partial tile may hold anything: zero them
         if (n_valid < kTile) {
           const int rows = kTile - n_valid;

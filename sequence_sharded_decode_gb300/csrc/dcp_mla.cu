@@ -31,8 +31,12 @@
 //      tile's share of the row weight, < 1/32) x max|v|, and the MMA is
 //      skipped.
 // TMA brings each page as nine 64-column, 128-byte-swizzled boxes into a
-// 2-stage ring; one thread issues all MMAs; 4 warps run the softmax and the
-// epilogue. Every barrier's phases are observed in order and never more than
+// 2-stage ring. One warp schedules the MMAs: it polls its barriers with the
+// non-blocking test_wait (a suspended try_wait reacts hundreds of cycles
+// late) and runs with uniform control flow so that one elect.sync-chosen lane
+// issues each MMA without per-instruction operand shuffling. 4 warps run the
+// softmax (exp2 on the SFU, tree max, the residual formed only when needed)
+// and the epilogue. Every barrier's phases are observed in order and never more than
 // one phase late, so parity waits are unambiguous; every wait is bounded: on
 // expiry the kernel raises DCP_DEVERR_TIMEOUT, stops all roles, drains what
 // it issued and frees TMEM.
@@ -137,6 +141,21 @@ __device__ __forceinline__ bool bar_try_cluster(uint32_t b, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe: unlike try_wait, test_wait never suspends the thread,
+// so a loop polling several barriers reacts to whichever completes first.
+__device__ __forceinline__ bool bar_test(uint32_t b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok) : "r"(b), "r"(parity) : "memory");
+  return ok != 0;
+}
+// Poll by a whole warp: true only if every lane saw the phase complete, so
+// the warp's control flow stays uniform.
+__device__ __forceinline__ bool bar_test_warp(uint32_t b, uint32_t parity) {
+  return __all_sync(0xffffffffu, bar_test(b, parity));
+}
+
 // Bounded wait. Returns false if the kernel is aborting (this wait expired, or
 // another role's did): the caller then stops.
 __device__ __noinline__ bool wait_bar(uint32_t b, uint32_t parity, volatile int* abort_flag, int32_t* err,
@@ -163,11 +182,6 @@ __device__ __forceinline__ void drain_bar(uint32_t b, uint32_t parity) {
     if (bar_try(b, parity)) return;
 }
 
-// pull a box into L2 only (no shared memory, no barrier)
-__device__ __forceinline__ void tma_prefetch(const CUtensorMap* map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n"
-               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y) : "memory");
-}
 __device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n"
@@ -192,11 +206,13 @@ __host__ __device__ constexpr uint32_t idesc(int M, int N, int b_mn_major) {
 }
 __device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, int accumulate) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+      "{\n .reg .pred p, e;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
       ::"r"(d), "l"(a), "l"(b), "r"(id), "r"(accumulate));
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
+  asm volatile("{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+               " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar)
                : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
@@ -221,7 +237,8 @@ __device__ __forceinline__ void st_local_v4(uint32_t a, uint32_t x, uint32_t y, 
 // S = Q . K^T with A (the queries) read from tensor memory
 __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id, int accumulate) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+      "{\n .reg .pred p, e;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
       ::"r"(d), "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate));
 }
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
@@ -231,13 +248,22 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
-// hi = bf16(x), lo = bf16(x - hi), for a pair of values
-__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+// 2^x on the SFU, denormal results flushed to zero
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+// bf16 pair (x0 in the low half), round to nearest even
+__device__ __forceinline__ uint32_t pack_bf16(float x0, float x1) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+// bf16 pair of the rounding residuals x - bf16(x)
+__device__ __forceinline__ uint32_t residual_bf16(float x0, float x1) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
   const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
+  return pack_bf16(x0 - hf.x, x1 - hf.y);
 }
 
 
@@ -368,7 +394,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {  // the whole warp runs the loop (uniform control flow); one elected lane issues
       const uint32_t id_s = idesc(128, 64, 0);
       const uint32_t id_pv = idesc(128, 256, 1);
       const uint64_t kdesc0 = sdesc(sbase + kOffKv, 0);
@@ -390,13 +416,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       while (kp < k_end) {
         bool progressed = false;
         if (ks < k_end) {
-          if (!q_ready && bar_try(bar(BQ_FULL), q_loads & 1u)) {
+          if (!q_ready && bar_test_warp(bar(BQ_FULL), q_loads & 1u)) {
             q_ready = true;
             tc_fence_after();
           }
           const uint32_t s = g_s % kStages;
-          if (q_ready && bar_try(bar(BKV_FULL + s), (g_s / kStages) & 1u) &&
-              (g_s == 0 || bar_try(bar(BS_EMPTY), (g_s - 1) & 1u))) {
+          if (q_ready && bar_test_warp(bar(BKV_FULL + s), (g_s / kStages) & 1u) &&
+              (g_s == 0 || bar_test_warp(bar(BS_EMPTY), (g_s - 1) & 1u))) {
             tc_fence_after();
             // descriptors advance by (byte offset >> 4) in their address field
             const uint64_t kd = kdesc0 + (uint64_t)((s * kStageBytes) >> 4);
@@ -424,7 +450,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             progressed = true;
           }
         }
-        if (g_p < g_s && bar_try(bar(BP_FULL), g_p & 1u)) {
+        if (g_p < g_s && bar_test_warp(bar(BP_FULL), g_p & 1u)) {
           tc_fence_after();
           const uint32_t s = g_p % kStages;
           const uint64_t vd = vdesc0 + (uint64_t)((s * kStageBytes) >> 4);  // V dims of this CTA
@@ -453,7 +479,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           *abort_flag = 1;
           raise_flag(p.err, DCP_DEVERR_TIMEOUT);
           break;
-        } else if ((idle & 63u) == 0 && *abort_flag) {
+        } else if ((idle & 63u) == 0 && __any_sync(0xffffffffu, *abort_flag != 0)) {
           break;
         }
       }
@@ -512,11 +538,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // 2. online softmax over the 64 tokens (log2 units)
         const int n_valid = phys < 0 ? 0 : min(kTile, g.hi - (g.lo + kTile * t));
         float sc[64];
-        float mx = -INFINITY;
+        float mx;
+        if (n_valid == kTile) {  // common case: no masking; the max as a tree for ILP
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          sc[i] = i < n_valid ? __uint_as_float(sv[i]) * p.sl2 : -INFINITY;
-          mx = fmaxf(mx, sc[i]);
+          for (int i = 0; i < 64; ++i) sc[i] = __uint_as_float(sv[i]) * p.sl2;
+          float m8[8];
+#pragma unroll
+          for (int j8 = 0; j8 < 8; ++j8)
+            m8[j8] = fmaxf(fmaxf(fmaxf(sc[8 * j8], sc[8 * j8 + 1]), fmaxf(sc[8 * j8 + 2], sc[8 * j8 + 3])),
+                           fmaxf(fmaxf(sc[8 * j8 + 4], sc[8 * j8 + 5]), fmaxf(sc[8 * j8 + 6], sc[8 * j8 + 7])));
+          mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        } else {
+          mx = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            sc[i] = i < n_valid ? __uint_as_float(sv[i]) * p.sl2 : -INFINITY;
+            mx = fmaxf(mx, sc[i]);
+          }
         }
         float m_new = m_run, alpha = 1.f;
         bool rescale = false;
@@ -528,33 +566,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           rescale = true;
         }
         const float ref = m_new == -INFINITY ? 0.f : m_new;
-        // 3. the P buffer and O are free once the previous tile's P.V has finished
-        if (gi >= 1 && !wait_warp(bar(BP_EMPTY), (gi - 1) & 1u, abort_flag, p.err, false)) { ok = false; break; }
-        float lsum = 0.f;
+        float lsum;
         {
-          const uint32_t hrow = sbase + kOffP + h * 128;
-          const uint32_t lrow = hrow + kPBytes;
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float a = exp2f(sc[8 * c + 2 * e] - ref), b = exp2f(sc[8 * c + 2 * e + 1] - ref);
-              lsum += a + b;
-              split2(a, b, hi[e], lo[e]);
-            }
-            const uint32_t off = ((uint32_t)c ^ (uint32_t)(h & 7)) << 4;
-            st_local_v4(hrow + off, hi[0], hi[1], hi[2], hi[3]);
-            st_local_v4(lrow + off, lo[0], lo[1], lo[2], lo[3]);
+          for (int i = 0; i < 64; ++i) {
+            sc[i] = ex2_ftz(sc[i] - ref);  // masked entries: 2^-inf = 0
+            ls[i & 3] += sc[i];
           }
+          lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
         }
         l_run = l_run * alpha + lsum;
         m_run = m_new;
         // The residual term matters only where this tile carries a noticeable
         // share of the row's weight (the first tiles of an item, or a tile
-        // with a dominant token); elsewhere its P.V is skipped.
+        // with a dominant token); elsewhere it is neither formed nor applied.
+        const bool any_lo = __any_sync(0xffffffffu, lsum > kLoFraction * l_run);
+        // 3. the P buffer and O are free once the previous tile's P.V has finished
+        if (gi >= 1 && !wait_warp(bar(BP_EMPTY), (gi - 1) & 1u, abort_flag, p.err, false)) { ok = false; break; }
         {
-          const bool any_lo = __any_sync(0xffffffffu, lsum > kLoFraction * l_run);
+          const uint32_t hrow = sbase + kOffP + h * 128;
+          const uint32_t lrow = hrow + kPBytes;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t hi[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) hi[e] = pack_bf16(sc[8 * c + 2 * e], sc[8 * c + 2 * e + 1]);
+            st_local_v4(hrow + (((uint32_t)c ^ (uint32_t)(h & 7)) << 4), hi[0], hi[1], hi[2], hi[3]);
+          }
+          if (any_lo) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              uint32_t lo[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) lo[e] = residual_bf16(sc[8 * c + 2 * e], sc[8 * c + 2 * e + 1]);
+              st_local_v4(lrow + (((uint32_t)c ^ (uint32_t)(h & 7)) << 4), lo[0], lo[1], lo[2], lo[3]);
+            }
+          }
           if (lane == 0) lo_flags[warp] = any_lo ? 1 : 0;
         }
         // 4. V rows past the end of a partial tile may hold anything: zero them

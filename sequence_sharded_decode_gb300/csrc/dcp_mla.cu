@@ -35,11 +35,10 @@
 // non-blocking test_wait (a suspended try_wait reacts hundreds of cycles
 // late) and runs with uniform control flow so that one elect.sync-chosen lane
 // issues each MMA without per-instruction operand shuffling. 4 warps run the
-// softmax (exp2 on the SFU, tree max, the residual formed only when needed)
-// and the epilogue. Every barrier's phases are observed in order and never more than
-// one phase late, so parity waits are unambiguous; every wait is bounded: on
-// expiry the kernel raises DCP_DEVERR_TIMEOUT, stops all roles, drains what
-// it issued and frees TMEM.
+// softmax (exp2 on the SFU, tree max) and the epilogue. Every barrier's
+// phases are observed in order and never more than one phase late, so parity
+// waits are unambiguous; every wait is bounded: on expiry the kernel raises
+// DCP_DEVERR_TIMEOUT, stops all roles, drains what it issued and frees TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -580,7 +579,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         m_run = m_new;
         // The residual term matters only where this tile carries a noticeable
         // share of the row's weight (the first tiles of an item, or a tile
-        // with a dominant token); elsewhere it is neither formed nor applied.
+        // with a dominant token); elsewhere its P.V is skipped. The residual
+        // itself is stored for every row on every tile: the P.V covers all
+        // 128 rows, so when any warp asks for it, every row must be current.
         const bool any_lo = __any_sync(0xffffffffu, lsum > kLoFraction * l_run);
         // 3. the P buffer and O are free once the previous tile's P.V has finished
         if (gi >= 1 && !wait_warp(bar(BP_EMPTY), (gi - 1) & 1u, abort_flag, p.err, false)) { ok = false; break; }
@@ -594,7 +595,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 4; ++e) hi[e] = pack_bf16(sc[8 * c + 2 * e], sc[8 * c + 2 * e + 1]);
             st_local_v4(hrow + (((uint32_t)c ^ (uint32_t)(h & 7)) << 4), hi[0], hi[1], hi[2], hi[3]);
           }
-          if (any_lo) {
+          {
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
               uint32_t lo[4];

@@ -29,6 +29,9 @@ CASES = [
     ("gqa_tiny", dict(batch=2, ctx_fixed=1500, shards=4, block_size=64, scale=1.0)),  # peaky softmax
     ("gqa_mid", dict(batch=1, ctx_fixed=0, shards=4)),       # one token only
     ("gqa_mid", dict(batch=3, ctx_fixed=4000, shards=4, needles=3)),   # planted q-aligned keys
+    ("gqa_mid", dict(batch=2, q_heads=256, kv_heads=2, ctx_fixed=700, shards=3)),  # largest Hq: g=128, 8 head groups
+    ("gqa_tiny", dict(batch=2, ctx_fixed=900, shards=3, scale=0.0)),   # uniform weights: O = mean of V
+    ("gqa_mid", dict(batch=2, ctx_fixed=800, shards=2, scale=-0.0884)),  # negative scale
 ]
 
 

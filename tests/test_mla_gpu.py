@@ -25,6 +25,8 @@ CASES = [
     ("mla_decode", dict(batch=2, ctx_kind="fixed", ctx_fixed=5000, shards=3, scale=1.0)),  # peaky: lazy rescale
     ("mla_high_concurrency", dict(batch=6, shards=8, **RAGGED)),                  # fragmented pools
     ("mla_decode", dict(batch=3, ctx_kind="fixed", ctx_fixed=3000, shards=4, needles=3)),  # planted keys
+    ("mla_decode", dict(batch=2, ctx_kind="fixed", ctx_fixed=900, shards=3, scale=0.0)),   # uniform weights
+    ("mla_decode", dict(batch=2, ctx_kind="fixed", ctx_fixed=900, shards=2, scale=-0.0417)),  # negative scale
 ]
 
 
@@ -101,3 +103,13 @@ def test_mla_decode_full_size_sampled():
     st.step()
     ctx = wl.ctx_lens()
     _check(st, wl, seqs=[int(np.argmin(ctx)), int(np.argmax(ctx)), 17])
+
+
+def test_mla_high_concurrency_full_size_sampled():
+    """The 512-sequence workload with fragmented pools, at full size: the
+    shortest and the longest sequence and one in between, every shard."""
+    wl = configs.get("mla_high_concurrency")
+    st = DecodeState(wl)
+    st.step()
+    ctx = wl.ctx_lens()
+    _check(st, wl, seqs=[int(np.argmin(ctx)), int(np.argmax(ctx)), 255])

@@ -60,7 +60,6 @@ constexpr int kKStepsTmem = 24;                  // query dims 0-383: A operand 
 constexpr int kKSteps = 36;                      // 16-column k-steps of the score MMA
 constexpr int kQSmemChunks = 3;                  // query dims 384-575 in shared memory
 constexpr int kStages = 2;                       // K/V tile pipeline depth
-constexpr int kPrefetch = 4;                     // pages pulled into L2 ahead of the ring
 constexpr int kThreads = 192;
 constexpr int kKvChunkBytes = kTile * 128;       // 64 rows x 64 bf16
 constexpr int kStageBytes = kChunks * kKvChunkBytes;
@@ -338,8 +337,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 4) {
     // ------------------------------------------------------------ producer
     // The whole warp reads block-table entries 32 tiles at a time (lane i
-    // holds tile base + i); lane 0 issues the copies. Pages kPrefetch tiles
-    // ahead of the ring are pulled into L2, so the ring's copies hit L2.
+    // holds tile base + i); lane 0 issues the copies.
     uint32_t fills = 0;  // K/V tiles issued (global across items)
     int n_items = 0;
     bool stop = false;
@@ -365,8 +363,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           nxt = j + 32 + lane < nt ? tile_block(p, g, g.t0 + j + 32 + lane) : -1;
         }
         const int phys = __shfl_sync(0xffffffffu, cur, j & 31);
-        const int jp = j + kPrefetch;
-        const int phys_pf = __shfl_sync(0xffffffffu, ((jp >> 5) == (j >> 5)) ? cur : nxt, jp & 31);
         if (lane == 0) {
           const uint32_t s = fills % kStages, use = fills / kStages;
           if (use > 0 && !wait_bar(bar(BKV_EMPTY + s), (use - 1) & 1u, abort_flag, p.err, false)) {
@@ -378,7 +374,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int c = 0; c < kChunks; ++c)
               tma_load(sbase + kOffKv + s * kStageBytes + c * kKvChunkBytes, &p.tm_kv[g.shard], 64 * c, row,
                        bar(BKV_FULL + s));
-            (void)phys_pf;
           }
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) { stop = true; break; }

@@ -275,3 +275,51 @@ def sharded_attention(q, K, V, scale: float, starts_b, seq_len: int):
         lses.append(l_i)
     O, lse = merge(np.stack(parts), np.stack(lses))
     return O, lse, np.stack(parts), np.stack(lses)
+
+
+# ---------------------------------------------------------------------------
+# Multi-token decode queries (speculative / multi-token-prediction steps)
+# ---------------------------------------------------------------------------
+# The pages name speculative decoding and MTP as what DCP is to be combined
+# with next (Qiita write-up, section "実務でどう見るか"; "Inference Systems
+# Infrastructure Notes (7): DCP", section 5) but give no formula. Reading
+# taken: a step that verifies q_len new tokens of sequence b appends all of
+# them (seq_len counts them), and query token i sits at global position
+# seq_len - q_len + i and attends every token at or before its own position
+# (causal among the new tokens), exactly as q_len consecutive one-token decode
+# steps would. Under sharding each query is routed like a one-token query
+# whose sequence ends at its own position; the merge is unchanged.
+def mtp_limits(seq_len: int, q_len: int) -> list[int]:
+    """Exclusive causal limit of each query token: seq_len - q_len + i + 1,
+    floored at 0 (a query before position 0 attends nothing)."""
+    if q_len < 1:
+        raise ValueError("q_len must be >= 1")
+    return [max(0, int(seq_len) - q_len + i + 1) for i in range(q_len)]
+
+
+def mtp_attention(q, K, V, scale: float, seq_len: int):
+    """Unsharded attention of q_len query tokens q [q_len, Hq, Dk] over the
+    logical K/V of one sequence, each query causal at its own position.
+    Returns O [q_len, Hq, Dv] and LSE [q_len, Hq]."""
+    q = np.asarray(q, dtype=np.float64)
+    outs, lses = [], []
+    for i, hi in enumerate(mtp_limits(seq_len, q.shape[0])):
+        o_i, l_i = attention(q[i], K, V, scale, 0, hi)
+        outs.append(o_i)
+        lses.append(l_i)
+    return np.stack(outs), np.stack(lses)
+
+
+def sharded_mtp_attention(q, K, V, scale: float, starts_b, seq_len: int):
+    """The method for q_len query tokens of one sequence: per query token,
+    partial attention on every shard's range clipped to the query's causal
+    limit, then the LSE merge. Returns (O [q_len, Hq, Dv], LSE [q_len, Hq],
+    O_parts [N, q_len, Hq, Dv], LSE_parts [N, q_len, Hq])."""
+    q = np.asarray(q, dtype=np.float64)
+    res = [sharded_attention(q[i], K, V, scale, starts_b, hi)
+           for i, hi in enumerate(mtp_limits(seq_len, q.shape[0]))]
+    O = np.stack([r[0] for r in res])
+    lse = np.stack([r[1] for r in res])
+    parts = np.stack([r[2] for r in res], axis=1)
+    part_lses = np.stack([r[3] for r in res], axis=1)
+    return O, lse, parts, part_lses

@@ -2,12 +2,14 @@
 """Benchmark of one DCP decode step (append -> partial attention on every
 virtual shard -> LSE merge) through the C ABI, on synthetic seeded inputs.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--q-len Q] [--impl ours|reference]
 
 Prints one JSON line (rank 0). `value` is whole-job achieved HBM GB/s: the
 step's algorithmic bytes (KV read once, queries, partials written and read,
 output, appended rows) over the device-timed step, summed over ranks and
-divided by the slowest rank's time. With N > 1 each rank runs an independent
+divided by the slowest rank's time. `--q-len Q` (Q > 1) runs a multi-token
+step instead: Q new tokens per sequence, query token j at position ctx + j,
+causal among the new tokens; each KV token still counts once. With N > 1 each rank runs an independent
 replica of the workload (weak scaling; the shards of one step live in one
 GPU's memory, so nothing crosses GPUs). `--impl reference` times the float64
 CPU oracle on a bounded sample of the same workload instead.
@@ -43,11 +45,11 @@ def _peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def _workload_config(wl, st=None) -> dict:
-    cfg = {"workload": wl.name, "batch": wl.batch, "q_heads": wl.q_heads, "kv_heads": wl.kv_heads,
+def _workload_config(wl, st=None, q_len: int = 1) -> dict:
+    cfg = {"workload": wl.name if q_len == 1 else f"{wl.name}, {q_len} query tokens per sequence", "batch": wl.batch, "q_heads": wl.q_heads, "kv_heads": wl.kv_heads,
            "head_dim_k": wl.dk, "head_dim_v": wl.dv, "block_size": wl.block_size, "shards": wl.shards,
-           "context": (f"{wl.ctx_fixed}+1" if wl.ctx_kind == "fixed"
-                       else f"lognormal(median {wl.median:g}, sigma {wl.sigma}) in [{wl.ctx_lo},{wl.ctx_hi}] +1"),
+           "context": (f"{wl.ctx_fixed}+{q_len}" if wl.ctx_kind == "fixed"
+                       else f"lognormal(median {wl.median:g}, sigma {wl.sigma}) in [{wl.ctx_lo},{wl.ctx_hi}] +{q_len}"),
            "fragmented_pools": wl.capacity_factor > 1.0,
            "l2": "inputs larger than L2 (KV read per step >> 129 MB); no flush"}
     if st is not None:
@@ -139,7 +141,7 @@ def _traffic_for(kernel_file: str, workload: str):
 # ---------------------------------------------------------------------------
 # the CPU oracle leg (reference arm and cpu_baseline)
 # ---------------------------------------------------------------------------
-def oracle_prepare(wl, seqs):
+def oracle_prepare(wl, seqs, q_len: int = 1):
     """Generate (outside any timing) the bf16 inputs of the sampled sequences."""
     import oracle as O
     from sequence_sharded_decode_gb300 import configs, inputs
@@ -148,9 +150,12 @@ def oracle_prepare(wl, seqs):
     starts = O.shard_starts(ctx, wl.shards)
     data = []
     for b in seqs:
-        L = int(ctx[b]) + 1
+        L = int(ctx[b]) + q_len
         qs = inputs.STREAM_Q_MLA if wl.kind == configs.MLA else inputs.STREAM_Q
-        q = inputs.bf16_bits(inputs.query(wl.seed, [b], wl.q_heads, wl.dk, stream=qs))[0]
+        if q_len == 1:
+            q = inputs.bf16_bits(inputs.query(wl.seed, [b], wl.q_heads, wl.dk, stream=qs))[0]
+        else:
+            q = inputs.bf16_bits(inputs.query_tokens(wl.seed, [b], q_len, wl.q_heads, wl.dk, stream=qs))[0]
         if wl.kind == configs.MLA:
             kb = inputs.bf16_bits(inputs.sequence_kv(wl.seed, inputs.STREAM_LATENT, b, 0, L, 1, wl.dk))
             vb = None
@@ -172,7 +177,10 @@ def oracle_pass(wl, data):
         qf = O.bf16_bits_to_f64(q)
         K = O.bf16_bits_to_f64(kb)
         V = K[:, :, :wl.dv] if vb is None else O.bf16_bits_to_f64(vb)
-        O.sharded_attention(qf, K, V, wl.scale, starts_b, L)
+        if qf.ndim == 2:
+            O.sharded_attention(qf, K, V, wl.scale, starts_b, L)
+        else:
+            O.sharded_mtp_attention(qf, K, V, wl.scale, starts_b, L)
         nbytes += L * wl.kv_bytes_per_token
     return time.perf_counter() - t0, nbytes
 
@@ -181,9 +189,9 @@ def _cores() -> int:
     return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
 
 
-def oracle_sample(wl, seqs, budget_s: float):
+def oracle_sample(wl, seqs, budget_s: float, q_len: int = 1):
     """Oracle throughput over a bounded sample: repeat passes until budget_s."""
-    data = oracle_prepare(wl, seqs)
+    data = oracle_prepare(wl, seqs, q_len)
     t_total, nbytes, runs = 0.0, 0, 0
     while runs == 0 or t_total < budget_s:
         t, n = oracle_pass(wl, data)
@@ -201,7 +209,7 @@ def run_reference(args, wl):
     if int(os.environ.get("RANK", "0")) != 0:
         return 0
     seqs = [0]
-    data = oracle_prepare(wl, seqs)
+    data = oracle_prepare(wl, seqs, args.q_len)
     times, nbytes = [], 0
     for i in range(args.warmup + args.steps):
         t, n = oracle_pass(wl, data)
@@ -214,7 +222,7 @@ def run_reference(args, wl):
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * float(np.mean(times)), 3), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": _workload_config(wl),
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": _workload_config(wl, q_len=args.q_len),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": _cores(), "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -260,7 +268,7 @@ def run_ours(args, wl):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dcp.load()
-    st = DecodeState(wl, device=f"cuda:{local}")
+    st = DecodeState(wl, device=f"cuda:{local}", q_len=args.q_len)
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
 
@@ -305,7 +313,7 @@ def run_ours(args, wl):
     # step i+1's inputs come in and step i's result goes out while the GPU
     # computes: the timed region spans the first input copy to the last
     # result copy.
-    names_in = [n for n in ("q", "k_new", "v_new", "positions", "seq_lens") if getattr(st, n) is not None]
+    names_in = [n for n in ("q", "k_new", "v_new", "seq_ids", "positions", "seq_lens") if getattr(st, n) is not None]
     host_in = {n: getattr(st, n).cpu().pin_memory() for n in names_in}
     host_out = {n: torch.empty(getattr(st, n).shape, dtype=getattr(st, n).dtype).pin_memory() for n in ("o", "lse")}
     dev = [{n: torch.empty_like(getattr(st, n)) for n in names_in + ["o", "lse"]} for _ in range(2)]
@@ -375,13 +383,13 @@ def run_ours(args, wl):
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": _workload_config(wl, st) | {"parallelism": f"replicas x{world}"},
+            "config": _workload_config(wl, st, args.q_len) | {"parallelism": f"replicas x{world}"},
             "hbm_frac_of_peak": round(value / world / peak, 4),
-            "tokens_per_s_per_layer": round(world * wl.batch / (ms * 1e-3), 1),
+            "tokens_per_s_per_layer": round(world * wl.batch * args.q_len / (ms * 1e-3), 1),
             "roofline": {"bound": "hbm", "kernel": "dcp_decode_partial_all (plan + attention + combine)",
                          "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "traffic": _traffic_for(kern, wl.name),
+                         "traffic": _traffic_for(kern, wl.name) if args.q_len == 1 else None,
                          "algorithmic_bytes_per_launch": bytes_["partial"]},
             "step_bytes": bytes_,
             "e2e": {"value": round(whole_job_gbs(world, step_bytes, e2e_ms), 2), "unit": "GB/s",
@@ -391,7 +399,7 @@ def run_ours(args, wl):
         }
         if world == 1 and not args.no_cpu_baseline:
             gbs, secs, desc, cores = oracle_sample(wl, [0, min(1, wl.batch - 1)] if wl.batch > 1 else [0],
-                                                   args.cpu_seconds)
+                                                   args.cpu_seconds, args.q_len)
             line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                                     "sample": desc, "seconds": round(secs, 2)}
         print(json.dumps(line), flush=True)
@@ -412,9 +420,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override the preset's batch (profiling cases)")
     ap.add_argument("--shards", type=int, default=None, help="override the preset's shard count")
+    ap.add_argument("--q-len", type=int, default=1,
+                    help="query tokens per sequence per step (multi-token / speculative step)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if not 1 <= args.q_len <= 64:
+        ap.error("--q-len must be in [1, 64]")
     from sequence_sharded_decode_gb300 import configs
     wl = configs.get(args.workload)
     if args.batch is not None:

@@ -178,6 +178,36 @@ DCP_API int dcp_decode_partial_all(const dcp_attn_desc* desc, const void* q, con
                            float* o_parts, float* lses, void* workspace, size_t ws_bytes,
                            int32_t* dev_err_flag, void* stream);
 
+/* Most query tokens per sequence that dcp_decode_partial_all_mtp accepts. */
+#define DCP_MAX_QUERY_TOKENS 64
+
+/* Step 2 for all N shards when each sequence brings q_len new tokens at once
+ * (a speculative-decoding or multi-token-prediction step). The pages name
+ * speculative decoding and MTP as what DCP is combined with next (Qiita
+ * write-up "vLLMの-dcpが長文脈のKVキャッシュ重複を消して3倍速くする", section
+ * "実務でどう見るか"; "Inference Systems Infrastructure Notes (7): DCP",
+ * section 5) without a formula; this call takes the reading that query token
+ * j (0 <= j < q_len) of sequence b sits at global position
+ * seq_lens[b] - q_len + j and attends every token at or before it -- causal
+ * among the new tokens, as q_len consecutive one-token steps would. All q_len
+ * tokens' K/V are appended first (dcp_kv_append with T = B * q_len).
+ * Each shard's range is clipped to the query token's causal limit
+ * seq_lens[b] - q_len + j + 1; a query token before position 0, or with no
+ * token in a shard's range, gets o = 0 and lse = -inf there.
+ *   q        device bf16 [B, q_len, num_q_heads, head_dim_k]
+ *   seq_lens device int32 [B], global lengths including the q_len new tokens
+ *   o_parts  device fp32 [N, B, q_len, num_q_heads, head_dim_v] (out)
+ *   lses     device fp32 [N, B, q_len, num_q_heads] (out)
+ *   workspace >= dcp_workspace_size(desc, B * q_len, N) bytes
+ * The merge of step 3 is dcp_merge with B * q_len rows of sequences. q_len
+ * outside [1, DCP_MAX_QUERY_TOKENS] returns DCP_ERR_INVALID_ARG; q_len = 1 is
+ * dcp_decode_partial_all. The block tables are indexed by sequence: every
+ * query token of sequence b reads row b. */
+DCP_API int dcp_decode_partial_all_mtp(const dcp_attn_desc* desc, const void* q, const dcp_shard* shards,
+                                       int N, const int32_t* seq_lens, const int32_t* shard_starts, int B,
+                                       int q_len, float* o_parts, float* lses, void* workspace,
+                                       size_t ws_bytes, int32_t* dev_err_flag, void* stream);
+
 /* Same computation as dcp_decode_partial_all, for callers that cannot
  * allocate device memory at the point of the call: for example a plugin
  * running inside a serving engine that owns every byte of device memory

@@ -196,7 +196,7 @@ const char* dcp_status_string(int status) {
   }
 }
 
-int dcp_version(void) { return 100; }
+int dcp_version(void) { return 200; }
 
 int dcp_shard_plan(const int32_t* ctx_lens, int B, int N, int block_size, int reserve_tokens,
                    int32_t* shard_starts, int32_t* blocks_needed) {
@@ -263,23 +263,32 @@ int dcp_decode_partial(const dcp_attn_desc* desc, const void* q, const dcp_shard
   if (B == 0) return DCP_OK;
   if (!q || !seq_lens || !shard_range || !o_part || !lse) return DCP_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(o_part)) return DCP_ERR_INVALID_ARG;
-  RangeSpec rs{seq_lens, nullptr, shard_range, dev_err_flag, 1, B, 1};
+  RangeSpec rs{seq_lens, nullptr, shard_range, dev_err_flag, 1, B, 1, 1};
   return run_partial(desc, q, sh, rs, o_part, lse, workspace, ws_bytes, dev_err_flag, stream);
 }
 
 int dcp_decode_partial_all(const dcp_attn_desc* desc, const void* q, const dcp_shard* shards, int N,
                            const int32_t* seq_lens, const int32_t* shard_starts, int B, float* o_parts, float* lses,
                            void* workspace, size_t ws_bytes, int32_t* dev_err_flag, void* stream) {
+  return dcp_decode_partial_all_mtp(desc, q, shards, N, seq_lens, shard_starts, B, 1, o_parts, lses, workspace,
+                                    ws_bytes, dev_err_flag, stream);
+}
+
+int dcp_decode_partial_all_mtp(const dcp_attn_desc* desc, const void* q, const dcp_shard* shards, int N,
+                               const int32_t* seq_lens, const int32_t* shard_starts, int B, int q_len,
+                               float* o_parts, float* lses, void* workspace, size_t ws_bytes,
+                               int32_t* dev_err_flag, void* stream) {
   int rc = check_desc(desc);
   if (rc != DCP_OK) return rc;
   ShardSet sh;
   rc = check_shards(*desc, shards, N, &sh);
   if (rc != DCP_OK) return rc;
-  if (B < 0) return DCP_ERR_INVALID_ARG;
+  if (B < 0 || q_len < 1 || q_len > DCP_MAX_QUERY_TOKENS) return DCP_ERR_INVALID_ARG;
   if (B == 0) return DCP_OK;
   if (!q || !seq_lens || !shard_starts || !o_parts || !lses) return DCP_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(o_parts)) return DCP_ERR_INVALID_ARG;
-  RangeSpec rs{seq_lens, shard_starts, nullptr, dev_err_flag, 0, B, N};
+  if ((long long)B * q_len > INT32_MAX) return DCP_ERR_SHAPE;
+  RangeSpec rs{seq_lens, shard_starts, nullptr, dev_err_flag, 0, B * q_len, N, q_len};
   return run_partial(desc, q, sh, rs, o_parts, lses, workspace, ws_bytes, dev_err_flag, stream);
 }
 
@@ -303,7 +312,7 @@ int dcp_decode_partial_all_noalloc(const dcp_attn_desc* desc, const void* q, con
   void* ws = nullptr;
   rc = noalloc_scratch(&ws);
   if (rc != DCP_OK) return rc;
-  RangeSpec rs{seq_lens, shard_starts, nullptr, dev_err_flag, 0, B, N};
+  RangeSpec rs{seq_lens, shard_starts, nullptr, dev_err_flag, 0, B, N, 1};
   return run_partial(desc, q, sh, rs, o_parts, lses, ws, DCP_NOALLOC_SCRATCH_BYTES, dev_err_flag, stream);
 }
 

@@ -52,6 +52,7 @@ struct GqaParams {
   float* lses;
   int32_t* err;
   int B, Hq, Hkv, g, groups, Bs;
+  int qlen;   // query tokens per sequence (block-table row = query row / qlen)
   float sl2;  // scale * log2(e)
 };
 
@@ -127,7 +128,7 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const 
 
     const __nv_bfloat16* kpool = static_cast<const __nv_bfloat16*>(p.sh.k[shard]);
     const __nv_bfloat16* vpool = static_cast<const __nv_bfloat16*>(p.sh.v[shard]);
-    const int32_t* table = p.sh.table[shard] + (size_t)b * p.sh.max_blocks[shard];
+    const int32_t* table = p.sh.table[shard] + (size_t)(b / p.qlen) * p.sh.max_blocks[shard];
     const int max_blocks = p.sh.max_blocks[shard];
     const long long nblk = p.sh.nblk[shard];
 
@@ -388,6 +389,7 @@ cudaError_t launch_gqa(const dcp_attn_desc& d, const void* q, const ShardSet& sh
   p.lses = lses;
   p.err = err;
   p.B = rs.B;
+  p.qlen = rs.qlen;
   p.Hq = d.num_q_heads;
   p.Hkv = d.num_kv_heads;
   p.g = d.num_q_heads / d.num_kv_heads;

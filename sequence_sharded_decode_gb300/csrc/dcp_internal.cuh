@@ -30,17 +30,21 @@ struct ShardSet {
   int32_t max_blocks[kMaxShards];
 };
 
-// How a lane's token range is found: unit u = shard * B + b.
-//   mode 0 (all shards): [starts[b*N+i], i<N-1 ? starts[b*N+i+1] : inf) clipped to seq_lens[b]
-//   mode 1 (one shard) : [range[2b], range[2b+1]) clipped to seq_lens[b]
+// How a lane's token range is found: unit u = shard * B + r, where query row
+// r = b * qlen + j is query token j of sequence b (qlen = 1: r = b). Query
+// token j attends positions below its causal limit
+// lim = seq_lens[b] - (qlen - 1 - j):
+//   mode 0 (all shards): [starts[b*N+i], i<N-1 ? starts[b*N+i+1] : inf) clipped to lim
+//   mode 1 (one shard) : [range[2b], range[2b+1]) clipped to lim
 struct RangeSpec {
   const int32_t* seq_lens;
   const int32_t* starts;  // mode 0
   const int32_t* range;   // mode 1
   int32_t* err;           // device error flags (may be NULL)
   int mode;
-  int B;
+  int B;                  // query rows: sequences x qlen
   int N;
+  int qlen;               // query tokens per sequence
 };
 
 struct LaneRec {     // 32 bytes

@@ -100,7 +100,8 @@ struct MlaParams {
   float* o_parts;
   float* lses;
   int32_t* err;
-  int B;
+  int B;     // query rows: sequences x qlen
+  int qlen;  // query tokens per sequence (block-table row = query row / qlen)
   float sl2;
 };
 
@@ -288,7 +289,7 @@ __device__ __forceinline__ ItemGeom item_geom(const MlaParams& p, int k) {
 __device__ __forceinline__ int tile_block(const MlaParams& p, const ItemGeom& g, int t) {
   const int lb = (g.lo - g.start) / kTile + t;
   if (lb >= p.sh.max_blocks[g.shard]) return -1;
-  const int phys = p.sh.table[g.shard][(size_t)g.b * p.sh.max_blocks[g.shard] + lb];
+  const int phys = p.sh.table[g.shard][(size_t)(g.b / p.qlen) * p.sh.max_blocks[g.shard] + lb];
   return (phys < 0 || phys >= p.sh.nblk[g.shard]) ? -1 : phys;
 }
 
@@ -757,6 +758,7 @@ cudaError_t launch_mla(const dcp_attn_desc& d, const void* q, const ShardSet& sh
   p.lses = lses;
   p.err = err;
   p.B = rs.B;
+  p.qlen = rs.qlen;
   p.sl2 = d.scale * kLog2e;
   mla_partial_kernel<<<2 * n_ctas, kThreads, kSmemBytes, st>>>(p);
   return cudaGetLastError();

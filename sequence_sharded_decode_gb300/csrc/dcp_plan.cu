@@ -56,8 +56,9 @@ __device__ Scan2 block_exclusive_scan2(Scan2 v, Scan2* totals) {
 }
 
 __device__ __forceinline__ void unit_range(const RangeSpec& rs, int u, int* lo, int* hi, int* start) {
-  const int i = u / rs.B, b = u - i * rs.B;
-  int L = rs.seq_lens[b];
+  const int i = u / rs.B, r = u - i * rs.B;
+  const int b = r / rs.qlen, j = r - b * rs.qlen;
+  int L = rs.seq_lens[b] - (rs.qlen - 1 - j);  // causal limit of query token j
   if (L < 0) L = 0;
   int s, e;
   if (rs.mode == 0) {

@@ -32,11 +32,13 @@ DCP_DEVERR_POSITION = 4
 DCP_DEVERR_TIMEOUT = 8
 
 DCP_MAX_SHARDS = 32
+DCP_MAX_QUERY_TOKENS = 64
 DCP_KIND_GQA = 0
 DCP_KIND_MLA = 1
 
 EXPORTED = ("dcp_status_string", "dcp_version", "dcp_shard_plan", "dcp_kv_append", "dcp_workspace_size",
-            "dcp_decode_partial", "dcp_decode_partial_all", "dcp_decode_partial_all_noalloc", "dcp_merge")
+            "dcp_decode_partial", "dcp_decode_partial_all", "dcp_decode_partial_all_mtp",
+            "dcp_decode_partial_all_noalloc", "dcp_merge")
 
 
 class DcpError(RuntimeError):
@@ -115,6 +117,8 @@ def load() -> ctypes.CDLL:
     lib.dcp_decode_partial.argtypes = [pdesc, vp, pshard, vp, vp, i32, vp, vp, vp, sz, vp, vp]
     lib.dcp_decode_partial_all.restype = i32
     lib.dcp_decode_partial_all.argtypes = [pdesc, vp, pshard, i32, vp, vp, i32, vp, vp, vp, sz, vp, vp]
+    lib.dcp_decode_partial_all_mtp.restype = i32
+    lib.dcp_decode_partial_all_mtp.argtypes = [pdesc, vp, pshard, i32, vp, vp, i32, i32, vp, vp, vp, sz, vp, vp]
     lib.dcp_decode_partial_all_noalloc.restype = i32
     lib.dcp_decode_partial_all_noalloc.argtypes = [pdesc, vp, pshard, i32, vp, vp, i32, vp, vp, vp, vp]
     lib.dcp_merge.restype = i32
@@ -243,6 +247,31 @@ def dcp_decode_partial_all(desc: AttnDesc, q: torch.Tensor, shards, seq_lens: to
     _raise(rc, "dcp_decode_partial_all")
 
 
+def dcp_decode_partial_all_mtp(desc: AttnDesc, q: torch.Tensor, shards, seq_lens: torch.Tensor,
+                               shard_starts: torch.Tensor, o_parts: torch.Tensor, lses: torch.Tensor,
+                               workspace: torch.Tensor, err: torch.Tensor | None = None, stream=None):
+    """q [B, q_len, Hq, Dk] bf16: q_len new tokens per sequence, query token j
+    at position seq_lens[b] - q_len + j, causal among the new tokens.
+    o_parts [N, B, q_len, Hq, Dv], lses [N, B, q_len, Hq]; the workspace is
+    sized for B * q_len query rows."""
+    _check(q, torch.bfloat16, "q")
+    _check(seq_lens, torch.int32, "seq_lens")
+    _check(shard_starts, torch.int32, "shard_starts")
+    _check(o_parts, torch.float32, "o_parts")
+    _check(lses, torch.float32, "lses")
+    _check(workspace, torch.uint8, "workspace")
+    if err is not None:
+        _check(err, torch.int32, "err")
+    if q.dim() != 4:
+        raise ValueError("q must be [B, q_len, Hq, Dk]")
+    arr = _shards(shards)
+    rc = load().dcp_decode_partial_all_mtp(ctypes.byref(desc.c()), q.data_ptr(), arr, len(shards),
+                                           seq_lens.data_ptr(), shard_starts.data_ptr(), int(q.shape[0]),
+                                           int(q.shape[1]), o_parts.data_ptr(), lses.data_ptr(),
+                                           workspace.data_ptr(), workspace.numel(), _ptr(err), _stream(stream))
+    _raise(rc, "dcp_decode_partial_all_mtp")
+
+
 def dcp_decode_partial_all_noalloc(desc: AttnDesc, q: torch.Tensor, shards, seq_lens: torch.Tensor,
                                    shard_starts: torch.Tensor, o_parts: torch.Tensor, lses: torch.Tensor,
                                    err: torch.Tensor | None = None, stream=None):
@@ -264,13 +293,17 @@ def dcp_decode_partial_all_noalloc(desc: AttnDesc, q: torch.Tensor, shards, seq_
 
 def dcp_merge(o_parts: torch.Tensor, lses: torch.Tensor, o: torch.Tensor, lse_out: torch.Tensor | None = None,
               stream=None):
-    """o_parts [N, B, Hq, Dv] fp32, lses [N, B, Hq] fp32 -> o [B, Hq, Dv] (+ lse_out [B, Hq])."""
+    """o_parts [N, ..., Hq, Dv] fp32, lses [N, ..., Hq] fp32 -> o [..., Hq, Dv] (+ lse_out [..., Hq]);
+    the middle dimensions (sequences, or sequences x query tokens) are merged row by row."""
     _check(o_parts, torch.float32, "o_parts")
     _check(lses, torch.float32, "lses")
     _check(o, torch.float32, "o")
     if lse_out is not None:
         _check(lse_out, torch.float32, "lse_out")
-    N, B, Hq, Dv = (int(x) for x in o_parts.shape)
+    if o_parts.dim() < 4:
+        raise ValueError("o_parts must be [N, ..., Hq, Dv]")
+    N, Hq, Dv = int(o_parts.shape[0]), int(o_parts.shape[-2]), int(o_parts.shape[-1])
+    B = o_parts.numel() // max(1, N * Hq * Dv)
     rc = load().dcp_merge(o_parts.data_ptr(), lses.data_ptr(), N, B, Hq, Dv, o.data_ptr(), _ptr(lse_out),
                           _stream(stream))
     _raise(rc, "dcp_merge")

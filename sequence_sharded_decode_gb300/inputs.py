@@ -110,6 +110,19 @@ def query(seed: int, batch_ids, n_heads: int, width: int, device="cpu", stream: 
     return out.view(b.numel(), n_heads, width)
 
 
+def query_tokens(seed: int, batch_ids, q_len: int, n_heads: int, width: int, device="cpu",
+                 stream: int = STREAM_Q):
+    """Queries of q_len new tokens per sequence: [len(batch_ids), q_len, n_heads, width] bf16.
+
+    Query token j of sequence b draws from counter row b + j * 2**32, so token 0
+    is the one-token query of sequence b (query(seed, [b], ...))."""
+    b = torch.as_tensor(batch_ids, dtype=torch.int64, device=device).reshape(-1)
+    j = torch.arange(q_len, dtype=torch.int64, device=device)
+    rows = (b[:, None] + (j[None, :] << 32)).reshape(-1)
+    out = counter_normal_bf16(rows, _hd_index(n_heads, width, device), seed, stream)
+    return out.view(b.numel(), q_len, n_heads, width)
+
+
 def kv_tokens(seed: int, stream: int, batch_ids, positions, n_heads: int, width: int,
               device="cpu", chunk: int = 1 << 14) -> torch.Tensor:
     """Per-token KV rows [T, n_heads, width] bf16 for (batch_ids[j], positions[j])."""

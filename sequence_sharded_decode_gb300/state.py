@@ -15,13 +15,18 @@ from . import configs, dcp, inputs
 
 class DecodeState:
     def __init__(self, wl: configs.Workload, device: str = "cuda", fill: bool = True,
-                 canary: int | None = None, table_seed: int | None = None, fill_chunk: int = 1 << 18):
+                 canary: int | None = None, table_seed: int | None = None, fill_chunk: int = 1 << 18,
+                 q_len: int = 1):
+        """q_len > 1: every sequence brings q_len new tokens per step (a
+        speculative / multi-token step); query token j sits at position
+        ctx[b] + j and the partial pass is dcp_decode_partial_all_mtp."""
         self.wl = wl
         self.device = device
+        self.q_len = q_len
         self.ctx = wl.ctx_lens().astype(np.int64)
         B, N = wl.batch, wl.shards
         self.desc = dcp.AttnDesc(wl.kind, wl.q_heads, wl.kv_heads, wl.dk, wl.dv, wl.block_size, wl.scale)
-        starts, blocks = dcp.dcp_shard_plan(self.ctx, N, wl.block_size, 1)
+        starts, blocks = dcp.dcp_shard_plan(self.ctx, N, wl.block_size, q_len)
         self.starts_host, self.blocks_host = starts, blocks
         seed_t = wl.seed + 1 if table_seed is None else table_seed
         self.tables_host = inputs.block_tables(seed_t, blocks, wl.capacity_factor)
@@ -40,19 +45,28 @@ class DecodeState:
             self.shards.append(dcp.Shard(k, v, torch.from_numpy(tab).to(device)))
         self.starts = torch.from_numpy(starts).to(device)
         qstream = inputs.STREAM_Q_MLA if wl.kind == configs.MLA else inputs.STREAM_Q
-        self.q = inputs.query(wl.seed, np.arange(B), wl.q_heads, wl.dk, device, stream=qstream)
+        if q_len == 1:
+            self.q = inputs.query(wl.seed, np.arange(B), wl.q_heads, wl.dk, device, stream=qstream)
+            self.q0 = self.q
+        else:
+            self.q = inputs.query_tokens(wl.seed, np.arange(B), q_len, wl.q_heads, wl.dk, device, stream=qstream)
+            self.q0 = self.q[:, 0].contiguous()  # planted needles copy query token 0
         self.needles = wl.needle_plan()
-        self.positions = torch.from_numpy(self.ctx.astype(np.int32)).to(device)
-        self.seq_lens = torch.from_numpy((self.ctx + 1).astype(np.int32)).to(device)
-        self.k_new, self.v_new = self.token_rows(np.arange(B), self.ctx)
-        ws = dcp.dcp_workspace_size(self.desc, B, N)
+        new_b = np.repeat(np.arange(B), q_len)
+        new_t = (self.ctx[:, None] + np.arange(q_len)[None, :]).reshape(-1)
+        self.seq_ids = torch.from_numpy(new_b.astype(np.int32)).to(device) if q_len > 1 else None
+        self.positions = torch.from_numpy(new_t.astype(np.int32)).to(device)
+        self.seq_lens = torch.from_numpy((self.ctx + q_len).astype(np.int32)).to(device)
+        self.k_new, self.v_new = self.token_rows(new_b, new_t)
+        ws = dcp.dcp_workspace_size(self.desc, B * q_len, N)
         if ws <= 0:
             raise RuntimeError("dcp_workspace_size failed")
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=device)
-        self.o_parts = torch.empty((N, B, wl.q_heads, wl.dv), dtype=torch.float32, device=device)
-        self.lses = torch.empty((N, B, wl.q_heads), dtype=torch.float32, device=device)
-        self.o = torch.empty((B, wl.q_heads, wl.dv), dtype=torch.float32, device=device)
-        self.lse = torch.empty((B, wl.q_heads), dtype=torch.float32, device=device)
+        rows = (B,) if q_len == 1 else (B, q_len)
+        self.o_parts = torch.empty((N, *rows, wl.q_heads, wl.dv), dtype=torch.float32, device=device)
+        self.lses = torch.empty((N, *rows, wl.q_heads), dtype=torch.float32, device=device)
+        self.o = torch.empty((*rows, wl.q_heads, wl.dv), dtype=torch.float32, device=device)
+        self.lse = torch.empty((*rows, wl.q_heads), dtype=torch.float32, device=device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         if fill:
             self.fill_context(fill_chunk)
@@ -62,10 +76,10 @@ class DecodeState:
         wl = self.wl
         if wl.kind == configs.MLA:
             lat = inputs.kv_tokens(wl.seed, inputs.STREAM_LATENT, b, t, 1, wl.dk, self.device, chunk=1 << 18)
-            lat = inputs.plant_needles(lat.view(-1, wl.dk), b, t, self.q, self.needles, wl.q_heads)
+            lat = inputs.plant_needles(lat.view(-1, wl.dk), b, t, self.q0, self.needles, wl.q_heads)
             return lat, None
         k = inputs.kv_tokens(wl.seed, inputs.STREAM_K, b, t, wl.kv_heads, wl.dk, self.device, chunk=1 << 16)
-        k = inputs.plant_needles(k, b, t, self.q, self.needles, wl.q_heads)
+        k = inputs.plant_needles(k, b, t, self.q0, self.needles, wl.q_heads)
         v = inputs.kv_tokens(wl.seed, inputs.STREAM_V, b, t, wl.kv_heads, wl.dv, self.device, chunk=1 << 16)
         return k, v
 
@@ -86,11 +100,15 @@ class DecodeState:
     # -- the decode step through the C ABI ------------------------------------
     def append(self, stream=None):
         dcp.dcp_kv_append(self.desc, self.shards, self.starts, self.positions, self.k_new, self.v_new,
-                          err=self.err, stream=stream)
+                          seq_ids=self.seq_ids, err=self.err, stream=stream)
 
     def partial(self, stream=None):
-        dcp.dcp_decode_partial_all(self.desc, self.q, self.shards, self.seq_lens, self.starts, self.o_parts,
-                                   self.lses, self.workspace, err=self.err, stream=stream)
+        if self.q_len == 1:
+            dcp.dcp_decode_partial_all(self.desc, self.q, self.shards, self.seq_lens, self.starts, self.o_parts,
+                                       self.lses, self.workspace, err=self.err, stream=stream)
+        else:
+            dcp.dcp_decode_partial_all_mtp(self.desc, self.q, self.shards, self.seq_lens, self.starts,
+                                           self.o_parts, self.lses, self.workspace, err=self.err, stream=stream)
 
     def merge(self, stream=None):
         dcp.dcp_merge(self.o_parts, self.lses, self.o, self.lse, stream=stream)
@@ -102,7 +120,9 @@ class DecodeState:
 
     # -- algorithmic bytes ---------------------------------------------------
     def attended_tokens(self) -> int:
-        return int((self.ctx + 1).sum())
+        """Distinct tokens the step attends: the context plus the new tokens
+        (with several query tokens, each token is still read from HBM once)."""
+        return int((self.ctx + self.q_len).sum())
 
     def kv_bytes(self) -> int:
         """KV bytes the partial-attention pass must read (each attended token once)."""
@@ -111,7 +131,7 @@ class DecodeState:
     def step_bytes(self) -> dict:
         """Algorithmic HBM bytes of one step, by kernel."""
         wl = self.wl
-        B, N, Hq, dv, dk = wl.batch, wl.shards, wl.q_heads, wl.dv, wl.dk
+        B, N, Hq, dv, dk = wl.batch * self.q_len, wl.shards, wl.q_heads, wl.dv, wl.dk
         part = N * B * Hq * (dv + 1) * 4
         new_tok = B * (wl.kv_heads * (dk + dv) * 2 if wl.kind == configs.GQA else dk * 2)
         return {

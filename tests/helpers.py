@@ -59,6 +59,16 @@ def oracle_sequence(wl: configs.Workload, b: int, L: int, starts_b):
     return O.sharded_attention(q, K, V, wl.scale, starts_b, L)
 
 
+def oracle_mtp_sequence(wl: configs.Workload, b: int, ctx_b: int, q_len: int, starts_b):
+    """(O [q_len, Hq, Dv], LSE, O_parts [N, q_len, ...], LSE_parts) from the
+    oracle for sequence b with q_len new tokens after ctx_b context tokens."""
+    stream = inputs.STREAM_Q_MLA if wl.kind == configs.MLA else inputs.STREAM_Q
+    q = f64(inputs.query_tokens(wl.seed, [b], q_len, wl.q_heads, wl.dk, "cpu", stream=stream))[0]
+    L = int(ctx_b) + q_len
+    K, V = oracle_kv(wl, b, L)
+    return O.sharded_mtp_attention(q, K, V, wl.scale, starts_b, L)
+
+
 def assert_close(got, ref, what: str, atol: float = ATOL, rtol: float = RTOL):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)

@@ -148,3 +148,23 @@ def test_partial_and_merge_validation(lib):
     assert lib.dcp_merge(16, 16, 2, 1, 1, 6, 16, None, None) == dcp.DCP_ERR_UNSUPPORTED
     assert lib.dcp_merge(None, 16, 2, 1, 1, 4, 16, None, None) == dcp.DCP_ERR_INVALID_ARG
     assert lib.dcp_merge(16, 16, 2, 0, 1, 4, 16, None, None) == dcp.DCP_OK
+
+
+def test_multi_token_validation(lib):
+    d = _desc().c()
+    good = dcp._Shard(16, 16, 4, 16, 2)
+    mtp = lib.dcp_decode_partial_all_mtp
+    # q_len outside [1, DCP_MAX_QUERY_TOKENS], NULL outputs, N out of range: rejected on the host
+    for q_len in (0, -1, dcp.DCP_MAX_QUERY_TOKENS + 1):
+        assert mtp(ctypes.byref(d), 16, ctypes.byref(good), 1, 16, 16, 2, q_len, 16, 16, 256, 1 << 20, None,
+                   None) == dcp.DCP_ERR_INVALID_ARG
+    assert mtp(ctypes.byref(d), 16, ctypes.byref(good), 1, 16, 16, 2, 4, None, 16, 256, 1 << 20, None,
+               None) == dcp.DCP_ERR_INVALID_ARG
+    assert mtp(ctypes.byref(d), 16, ctypes.byref(good), 33, 16, 16, 2, 4, 16, 16, 256, 1 << 20, None,
+               None) == dcp.DCP_ERR_INVALID_ARG
+    # B * q_len must fit the int32 row count
+    assert mtp(ctypes.byref(d), 16, ctypes.byref(good), 1, 16, 16, 2 ** 30, 4, 16, 16, 256, 1 << 20, None,
+               None) == dcp.DCP_ERR_SHAPE
+    # no sequences: nothing to do, no launch
+    assert mtp(ctypes.byref(d), 16, ctypes.byref(good), 1, 16, 16, 0, 4, None, None, None, 0, None,
+               None) == dcp.DCP_OK

@@ -181,6 +181,12 @@ DCP_API int dcp_decode_partial_all(const dcp_attn_desc* desc, const void* q, con
 /* Most query tokens per sequence that dcp_decode_partial_all_mtp accepts. */
 #define DCP_MAX_QUERY_TOKENS 64
 
+/* Bytes of workspace dcp_decode_partial_all_mtp needs for B sequences with
+ * q_len query tokens each and N shards (0 on invalid input or q_len outside
+ * [1, DCP_MAX_QUERY_TOKENS]); dcp_workspace_size(desc, B, N) is the q_len = 1
+ * case. Same alignment and reuse rules as dcp_workspace_size. */
+DCP_API size_t dcp_workspace_size_mtp(const dcp_attn_desc* desc, int B, int q_len, int N);
+
 /* Step 2 for all N shards when each sequence brings q_len new tokens at once
  * (a speculative-decoding or multi-token-prediction step). The pages name
  * speculative decoding and MTP as what DCP is combined with next (Qiita
@@ -198,7 +204,7 @@ DCP_API int dcp_decode_partial_all(const dcp_attn_desc* desc, const void* q, con
  *   seq_lens device int32 [B], global lengths including the q_len new tokens
  *   o_parts  device fp32 [N, B, q_len, num_q_heads, head_dim_v] (out)
  *   lses     device fp32 [N, B, q_len, num_q_heads] (out)
- *   workspace >= dcp_workspace_size(desc, B * q_len, N) bytes
+ *   workspace >= dcp_workspace_size_mtp(desc, B, q_len, N) bytes
  * The merge of step 3 is dcp_merge with B * q_len rows of sequences. q_len
  * outside [1, DCP_MAX_QUERY_TOKENS] returns DCP_ERR_INVALID_ARG; q_len = 1 is
  * dcp_decode_partial_all. The block tables are indexed by sequence: every

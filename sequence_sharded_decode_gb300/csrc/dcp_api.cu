@@ -72,10 +72,17 @@ LaneGeom lane_geom(const dcp_attn_desc& d) {
   return g;
 }
 
-static int rows_per_lane(const dcp_attn_desc& d) {
+// Query rows of one lane: the heads of its group times the query tokens that
+// share its K/V tiles (GQA team of a multi-token step; 1 otherwise).
+static int rows_per_lane(const dcp_attn_desc& d, int team) {
   if (d.kind == DCP_KIND_MLA) return d.num_q_heads;
   const int grp = d.num_q_heads / d.num_kv_heads;
-  return grp < 16 ? grp : 16;
+  return (grp < 16 ? grp : 16) * team;
+}
+
+// Query tokens per row group for a step with q_len tokens per sequence.
+static int team_for(const dcp_attn_desc& d, int q_len) {
+  return d.kind == DCP_KIND_MLA ? 1 : gqa_team(q_len);
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -119,19 +126,20 @@ static int check_shards(const dcp_attn_desc& d, const dcp_shard* s, int N, Shard
   return DCP_OK;
 }
 
-static int work_ctas(const dcp_attn_desc& d, const DeviceInfo& di) {
-  return d.kind == DCP_KIND_MLA ? mla_ctas(d, di) : gqa_ctas(d, di);
+static int work_ctas(const dcp_attn_desc& d, const DeviceInfo& di, int team) {
+  return d.kind == DCP_KIND_MLA ? mla_ctas(d, di) : gqa_ctas(d, di, team);
 }
 
-static int layout_for(const dcp_attn_desc& d, int B, int N, WsLayout* L, int* n_ctas) {
+// Workspace layout for B row groups per shard (sequences x token groups).
+static int layout_for(const dcp_attn_desc& d, int B, int N, int team, WsLayout* L, int* n_ctas) {
   DeviceInfo di;
   if (device_info(&di) != 0) return DCP_ERR_CUDA;
-  const int c = work_ctas(d, di);
+  const int c = work_ctas(d, di, team);
   if (c <= 0) return DCP_ERR_CUDA;
   const LaneGeom g = lane_geom(d);
   const long long lanes = (long long)B * N * g.lanes_per_unit;
   if (lanes > (1 << 26)) return DCP_ERR_SHAPE;
-  *L = ws_layout((int)lanes, c, rows_per_lane(d), d.head_dim_v);
+  *L = ws_layout((int)lanes, c, rows_per_lane(d, team), d.head_dim_v);
   *n_ctas = c;
   return DCP_OK;
 }
@@ -141,7 +149,7 @@ static int run_partial(const dcp_attn_desc* desc, const void* q, const ShardSet&
   const dcp_attn_desc& d = *desc;
   WsLayout L;
   int n_ctas = 0;
-  int rc = layout_for(d, rs.B, rs.N, &L, &n_ctas);
+  int rc = layout_for(d, rs.B, rs.N, rs.tpr, &L, &n_ctas);
   if (rc != DCP_OK) return rc;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < L.total) return DCP_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -151,7 +159,7 @@ static int run_partial(const dcp_attn_desc* desc, const void* q, const ShardSet&
                                          : launch_gqa(d, q, sh, rs, o_parts, lses, ws, L, n_ctas, err, st);
   if (e == cudaErrorNotSupported) return DCP_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return DCP_ERR_CUDA;
-  if (launch_combine(d, rs.B, L.max_lanes, ws, L, o_parts, lses, st) != cudaSuccess) return DCP_ERR_CUDA;
+  if (launch_combine(d, rs, L.max_lanes, ws, L, o_parts, lses, st) != cudaSuccess) return DCP_ERR_CUDA;
   return DCP_OK;
 }
 
@@ -244,10 +252,18 @@ int dcp_kv_append(const dcp_attn_desc* desc, const dcp_shard* shards, int N, con
 }
 
 size_t dcp_workspace_size(const dcp_attn_desc* desc, int B, int N) {
+  return dcp_workspace_size_mtp(desc, B, 1, N);
+}
+
+size_t dcp_workspace_size_mtp(const dcp_attn_desc* desc, int B, int q_len, int N) {
   if (check_desc(desc) != DCP_OK || B < 0 || N < 1 || N > DCP_MAX_SHARDS) return 0;
+  if (q_len < 1 || q_len > DCP_MAX_QUERY_TOKENS) return 0;
+  const int team = team_for(*desc, q_len);
+  const long long rows = (long long)B * ((q_len + team - 1) / team);
+  if (rows > INT32_MAX) return 0;
   WsLayout L;
   int n_ctas = 0;
-  if (layout_for(*desc, B, N, &L, &n_ctas) != DCP_OK) return 0;
+  if (layout_for(*desc, (int)rows, N, team, &L, &n_ctas) != DCP_OK) return 0;
   return L.total;
 }
 
@@ -263,7 +279,7 @@ int dcp_decode_partial(const dcp_attn_desc* desc, const void* q, const dcp_shard
   if (B == 0) return DCP_OK;
   if (!q || !seq_lens || !shard_range || !o_part || !lse) return DCP_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(o_part)) return DCP_ERR_INVALID_ARG;
-  RangeSpec rs{seq_lens, nullptr, shard_range, dev_err_flag, 1, B, 1, 1};
+  RangeSpec rs{seq_lens, nullptr, shard_range, dev_err_flag, 1, B, 1, 1, 1};
   return run_partial(desc, q, sh, rs, o_part, lse, workspace, ws_bytes, dev_err_flag, stream);
 }
 
@@ -288,7 +304,9 @@ int dcp_decode_partial_all_mtp(const dcp_attn_desc* desc, const void* q, const d
   if (!q || !seq_lens || !shard_starts || !o_parts || !lses) return DCP_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(o_parts)) return DCP_ERR_INVALID_ARG;
   if ((long long)B * q_len > INT32_MAX) return DCP_ERR_SHAPE;
-  RangeSpec rs{seq_lens, shard_starts, nullptr, dev_err_flag, 0, B * q_len, N, q_len};
+  const int team = team_for(*desc, q_len);
+  const int groups = (q_len + team - 1) / team;
+  RangeSpec rs{seq_lens, shard_starts, nullptr, dev_err_flag, 0, B * groups, N, q_len, team};
   return run_partial(desc, q, sh, rs, o_parts, lses, workspace, ws_bytes, dev_err_flag, stream);
 }
 
@@ -306,13 +324,13 @@ int dcp_decode_partial_all_noalloc(const dcp_attn_desc* desc, const void* q, con
   if (!aligned16(q) || !aligned16(o_parts)) return DCP_ERR_INVALID_ARG;
   WsLayout L;
   int n_ctas = 0;
-  rc = layout_for(*desc, B, N, &L, &n_ctas);
+  rc = layout_for(*desc, B, N, 1, &L, &n_ctas);
   if (rc != DCP_OK) return rc;
   if (L.total > DCP_NOALLOC_SCRATCH_BYTES) return DCP_ERR_SCRATCH_LIMIT;
   void* ws = nullptr;
   rc = noalloc_scratch(&ws);
   if (rc != DCP_OK) return rc;
-  RangeSpec rs{seq_lens, shard_starts, nullptr, dev_err_flag, 0, B, N, 1};
+  RangeSpec rs{seq_lens, shard_starts, nullptr, dev_err_flag, 0, B, N, 1, 1};
   return run_partial(desc, q, sh, rs, o_parts, lses, ws, DCP_NOALLOC_SCRATCH_BYTES, dev_err_flag, stream);
 }
 

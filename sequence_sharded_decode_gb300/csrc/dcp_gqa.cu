@@ -51,9 +51,13 @@ struct GqaParams {
   float* o_parts;
   float* lses;
   int32_t* err;
-  int B, Hq, Hkv, g, groups, Bs;
-  int qlen;   // query tokens per sequence (block-table row = query row / qlen)
-  float sl2;  // scale * log2(e)
+  const int32_t* seq_lens;
+  int B;        // row groups per shard: sequences x token groups
+  int Bseq;     // sequences
+  int qlen;     // query tokens per sequence
+  int ngroups;  // token groups per sequence: ceil(qlen / T)
+  int Hq, Hkv, g, groups, Bs;
+  float sl2;    // scale * log2(e)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -97,17 +101,24 @@ __device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uin
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-template <int D>
+// T = warps per team = query tokens sharing each K/V tile (1, 2 or 4). The
+// kWarps / T teams of a CTA take the item's tiles in turn; a team's warps
+// copy each tile together into the team's ring (T * kStages stages) and then
+// each warp runs its own query token's 16 head rows over it, so a tile is
+// read once for T query tokens.
+template <int D, int T>
 __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const __grid_constant__ GqaParams p) {
   using C = GqaCfg<D>;
+  constexpr int kTeams = C::kWarps / T;
+  constexpr int kS = T * C::kStages;  // stages of a team's ring
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int team = warp / T, slot = warp - team * T;
   const int gr = lane >> 2, t4 = lane & 3;  // mma fragment row / column pair
-  unsigned char* wbase = smem + warp * C::kWarpBytes;
-  int* vcount = reinterpret_cast<int*>(smem + C::kWarps * C::kWarpBytes) + warp * C::kStages;
+  unsigned char* wbase = smem + warp * C::kWarpBytes;          // this warp's result area (after the item)
+  unsigned char* tbase = smem + team * T * C::kWarpBytes;      // the team's ring
+  int* vcount = reinterpret_cast<int*>(smem + C::kWarps * C::kWarpBytes) + team * kS;
 
-  const WsHeader* hdr = reinterpret_cast<const WsHeader*>(p.ws);
-  (void)hdr;
   const LaneRec* lanes = reinterpret_cast<const LaneRec*>(p.ws + p.L.lanes_off);
   const ItemRec* items = reinterpret_cast<const ItemRec*>(p.ws + p.L.items_off);
   const int* cta_begin = reinterpret_cast<const int*>(p.ws + p.L.cta_off);
@@ -116,26 +127,49 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const 
 
   const int k_begin = cta_begin[blockIdx.x], k_end = cta_begin[blockIdx.x + 1];
   const int lpu = p.Hkv * p.groups;
+  const int rpl = p.L.rows_per_lane / T;  // head rows of one query token in a lane
+
+  // the team's warps only: all of them have finished with what the barrier guards
+  // (named barrier 1 + team, immediate ids so that the kernel reserves only those)
+  auto team_sync = [&]() {
+    if (T == 1) {
+      __syncwarp();
+    } else if (T == 4) {
+      asm volatile("bar.sync 1, 128;\n" ::: "memory");
+    } else if (team == 0) {
+      asm volatile("bar.sync 1, 64;\n" ::: "memory");
+    } else {
+      asm volatile("bar.sync 2, 64;\n" ::: "memory");
+    }
+  };
+  static_assert(T == 1 || T == 2 || T == 4, "team of 1, 2 or 4 warps");
+  static_assert(C::kWarps == 4, "two teams of two or one team of four");
 
   for (int k = k_begin; k < k_end; ++k) {
     const ItemRec it = items[k];
     const LaneRec ln = lanes[it.lane];
     const int u = it.lane / lpu, j = it.lane - u * lpu;
     const int kvh = j / p.groups, hg = j - kvh * p.groups;
-    const int shard = u / p.B, b = u - shard * p.B;
+    const int shard = u / p.B, rg = u - shard * p.B;       // rg: row group = (sequence, token group)
+    const int b = rg / p.ngroups, tg = rg - b * p.ngroups;
+    const int jtok = tg * T + slot;                          // this warp's query token
+    const bool active = jtok < p.qlen;
+    const int qrow = b * p.qlen + (active ? jtok : 0);      // query row [sequence, token]
+    // causal limit of this warp's token (global positions); inactive warps attend nothing
+    const int hi_tok = active ? min(ln.hi, p.seq_lens[b] - (p.qlen - 1 - jtok)) : ln.lo;
     const int head0 = kvh * p.g + hg * 16;
     const int nheads = min(16, p.g - hg * 16);
 
     const __nv_bfloat16* kpool = static_cast<const __nv_bfloat16*>(p.sh.k[shard]);
     const __nv_bfloat16* vpool = static_cast<const __nv_bfloat16*>(p.sh.v[shard]);
-    const int32_t* table = p.sh.table[shard] + (size_t)(b / p.qlen) * p.sh.max_blocks[shard];
+    const int32_t* table = p.sh.table[shard] + (size_t)b * p.sh.max_blocks[shard];
     const int max_blocks = p.sh.max_blocks[shard];
     const long long nblk = p.sh.nblk[shard];
 
     // Query fragments (A operand, rows = query heads of the group).
     uint32_t qa[D / 16][4];
     {
-      const __nv_bfloat16* q0 = p.q + ((size_t)b * p.Hq + head0 + gr) * D;
+      const __nv_bfloat16* q0 = p.q + ((size_t)qrow * p.Hq + head0 + gr) * D;
       const __nv_bfloat16* q1 = q0 + 8 * D;
       const bool v0 = gr < nheads, v1 = gr + 8 < nheads;
 #pragma unroll
@@ -154,36 +188,37 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const 
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
     const int n_total = it.t1 - it.t0;
-    const int n_mine = n_total > warp ? (n_total - warp + C::kWarps - 1) / C::kWarps : 0;
+    const int n_mine = n_total > team ? (n_total - team + kTeams - 1) / kTeams : 0;
     const int local0 = ln.lo - ln.start;  // local position of the lane's first token
 
-    // Issue the loads of this warp's i-th tile into stage i % kStages.
+    // Issue the team's loads of its i-th tile into stage i % kS; each warp
+    // of the team copies every T-th 16-byte chunk.
     auto issue = [&](int i) {
-      const int st = i % C::kStages;
-      const int tile = it.t0 + warp + i * C::kWarps;
+      const int st = i % kS;
+      const int tile = it.t0 + team + i * kTeams;
       const int g0 = ln.lo + tile * C::kTile;  // global position of the tile's first token
       int ntok = min(C::kTile, ln.hi - g0);
       const int lp = local0 + tile * C::kTile;
-      const int lb = lp / p.Bs, slot = lp - lb * p.Bs;
+      const int lb = lp / p.Bs, slot_in_block = lp - lb * p.Bs;
       int phys = -1;
       if (lb < max_blocks) {
         phys = table[lb];
-      } else if (lane == 0) {
+      } else if (lane == 0 && slot == 0) {
         raise_flag(p.err, DCP_DEVERR_TABLE_RANGE);
       }
       if (phys < 0 || phys >= nblk) {
-        if (lane == 0 && lb < max_blocks) raise_flag(p.err, DCP_DEVERR_BLOCK_RANGE);
+        if (lane == 0 && slot == 0 && lb < max_blocks) raise_flag(p.err, DCP_DEVERR_BLOCK_RANGE);
         ntok = 0;
         phys = 0;
       }
-      if (lane == 0) vcount[st] = ntok;
-      const size_t off = (((size_t)phys * p.Hkv + kvh) * p.Bs + slot) * D;
+      if (lane == 0 && slot == 0) vcount[st] = ntok;
+      const size_t off = (((size_t)phys * p.Hkv + kvh) * p.Bs + slot_in_block) * D;
       const __nv_bfloat16* ks = kpool + off;
       const __nv_bfloat16* vs = vpool + off;
-      const uint32_t kd = smem_u32(wbase + st * C::kStageBytes);
+      const uint32_t kd = smem_u32(tbase + st * C::kStageBytes);
       const uint32_t vd = kd + C::kTileBytes;
 #pragma unroll
-      for (int c = lane; c < C::kTile * C::kChunks; c += 32) {
+      for (int c = slot * 32 + lane; c < C::kTile * C::kChunks; c += 32 * T) {
         const int r = c / C::kChunks, ch = c - r * C::kChunks;
         const uint32_t so = r * C::kRowBytes + ((ch ^ (r & 7)) << 4);
         const int bytes = r < ntok ? 16 : 0;
@@ -194,19 +229,29 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const 
     };
 
 #pragma unroll
-    for (int i = 0; i < C::kStages - 1; ++i) {
+    for (int i = 0; i < kS - 1; ++i) {
       if (i < n_mine) issue(i);
       cp_async_commit();
     }
 
     for (int i = 0; i < n_mine; ++i) {
-      if (i + C::kStages - 1 < n_mine) issue(i + C::kStages - 1);
-      cp_async_commit();
-      cp_async_wait<C::kStages - 1>();
-      __syncwarp();
-      const int st = i % C::kStages;
-      const int ntok = vcount[st];
-      const uint32_t kb = smem_u32(wbase + st * C::kStageBytes);
+      if (T == 1) {
+        if (i + kS - 1 < n_mine) issue(i + kS - 1);
+        cp_async_commit();
+        cp_async_wait<kS - 1>();
+        __syncwarp();
+      } else {
+        // tile i has landed (this warp's part); after the barrier every
+        // part is visible and no warp still reads the stage refilled next
+        cp_async_wait<kS - 2>();
+        team_sync();
+        if (i + kS - 1 < n_mine) issue(i + kS - 1);
+        cp_async_commit();
+      }
+      const int st = i % kS;
+      const int g0 = ln.lo + (it.t0 + team + i * kTeams) * C::kTile;
+      const int ntok = min(vcount[st], hi_tok - g0);  // this token's causal limit inside the tile
+      const uint32_t kb = smem_u32(tbase + st * C::kStageBytes);
       const uint32_t vb = kb + C::kTileBytes;
 
       // S = Q K^T for the 16 tokens (two 8-token halves)
@@ -285,7 +330,7 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const 
           mma16816(o[2 * n2 + 1], pl, b2, b3);
         }
       }
-      __syncwarp();
+      if (T == 1) __syncwarp();
     }
     cp_async_wait<0>();
 
@@ -295,8 +340,9 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const 
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
-    // this warp's (m, l, O) into its own stage area
-    __syncwarp();
+    // this warp's (m, l, O) into its own part of the team's ring, once no
+    // warp of the team reads the ring any more
+    team_sync();
     float* wo = reinterpret_cast<float*>(wbase);
     float* wm = wo + 16 * D;
     float* wl = wm + 16;
@@ -314,36 +360,43 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const 
     }
     __syncthreads();
 
-    // merge the warps' states and write the lane's partial
-    const int rows = nheads;
-    float* out_o;
-    float* out_l;
-    if (it.out_row >= 0) {
-      out_o = tmp_o + (size_t)it.out_row * p.L.rows_per_lane * D;
-      out_l = tmp_lse + (size_t)it.out_row * p.L.rows_per_lane;
-    } else {
-      out_o = p.o_parts + ((size_t)u * p.Hq + head0) * D;
-      out_l = p.lses + (size_t)u * p.Hq + head0;
-    }
+    // merge the teams' states of every query token and write the lane's
+    // partial: row R = (token slot js, head r) combines warps js, js + T, ...
+    const int rows = T * nheads;
+    const size_t tok_rows = (size_t)p.Bseq * p.qlen;  // query rows per shard
     for (int idx = threadIdx.x; idx < rows * D; idx += C::kThreads) {
-      const int r = idx / D, c = idx - r * D;
+      const int R = idx / D, c = idx - R * D;
+      const int js = R / nheads, r = R - js * nheads;
+      const int jt = tg * T + js;
+      if (jt >= p.qlen) continue;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < C::kWarps; ++w)
-        M = fmaxf(M, reinterpret_cast<const float*>(smem + w * C::kWarpBytes)[16 * D + r]);
+      for (int tm = 0; tm < kTeams; ++tm)
+        M = fmaxf(M, reinterpret_cast<const float*>(smem + (tm * T + js) * C::kWarpBytes)[16 * D + r]);
       float num = 0.f, den = 0.f;
       if (M != -INFINITY) {
 #pragma unroll
-        for (int w = 0; w < C::kWarps; ++w) {
-          const float* ws = reinterpret_cast<const float*>(smem + w * C::kWarpBytes);
+        for (int tm = 0; tm < kTeams; ++tm) {
+          const float* ws = reinterpret_cast<const float*>(smem + (tm * T + js) * C::kWarpBytes);
           const float mw = ws[16 * D + r];
           const float sc = mw == -INFINITY ? 0.f : exp2f(mw - M);
           num += sc * ws[r * D + c];
           den += sc * ws[16 * D + 16 + r];
         }
       }
-      out_o[(size_t)r * D + c] = den > 0.f ? num / den : 0.f;
-      if (c == 0) out_l[r] = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
+      float* out_o;
+      float* out_l;
+      if (it.out_row >= 0) {
+        const size_t row = (size_t)it.out_row * p.L.rows_per_lane + js * rpl + r;
+        out_o = tmp_o + row * D;
+        out_l = tmp_lse + row;
+      } else {
+        const size_t row = ((size_t)shard * tok_rows + (size_t)b * p.qlen + jt) * p.Hq + head0 + r;
+        out_o = p.o_parts + row * D;
+        out_l = p.lses + row;
+      }
+      out_o[c] = den > 0.f ? num / den : 0.f;
+      if (c == 0) *out_l = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
     }
     __syncthreads();
   }
@@ -351,7 +404,7 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const 
 
 // Resident CTAs per SM for the kernel, cached per device (the attribute is
 // set once per device, before the first launch there).
-template <int D>
+template <int D, int T>
 int occupancy() {
   static std::mutex mu;
   static int cache[64] = {};
@@ -360,26 +413,40 @@ int occupancy() {
   std::lock_guard<std::mutex> lock(mu);
   if (dev < 64 && cache[dev] > 0) return cache[dev];
   int occ = 0;
-  if (cudaFuncSetAttribute(gqa_partial_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(gqa_partial_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            GqaCfg<D>::kSmem) != cudaSuccess)
     return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gqa_partial_kernel<D>, GqaCfg<D>::kThreads,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gqa_partial_kernel<D, T>, GqaCfg<D>::kThreads,
                                                     GqaCfg<D>::kSmem) != cudaSuccess)
     return 0;
   if (dev < 64) cache[dev] = occ;
   return occ;
 }
 
+template <int D>
+int occupancy_for(int team) {
+  return team == 4 ? occupancy<D, 4>() : team == 2 ? occupancy<D, 2>() : occupancy<D, 1>();
+}
+
+template <int D, int T>
+void launch_t(const GqaParams& p, int n_ctas, cudaStream_t st) {
+  gqa_partial_kernel<D, T><<<n_ctas, GqaCfg<D>::kThreads, GqaCfg<D>::kSmem, st>>>(p);
+}
+
 }  // namespace
 
-int gqa_ctas(const dcp_attn_desc& d, const DeviceInfo& di) {
-  const int occ = d.head_dim_k == 128 ? occupancy<128>() : occupancy<64>();
+int gqa_team(int qlen) { return qlen >= 3 ? 4 : qlen; }
+
+int gqa_ctas(const dcp_attn_desc& d, const DeviceInfo& di, int team) {
+  const int occ = d.head_dim_k == 128 ? occupancy_for<128>(team) : occupancy_for<64>(team);
   return occ > 0 ? occ * di.sm_count : 0;
 }
 
 cudaError_t launch_gqa(const dcp_attn_desc& d, const void* q, const ShardSet& sh, const RangeSpec& rs,
                        float* o_parts, float* lses, void* ws, const WsLayout& L, int n_ctas, int32_t* err,
                        cudaStream_t st) {
+  const int team = rs.tpr;
+  if (team != 1 && team != 2 && team != 4) return cudaErrorInvalidValue;
   GqaParams p;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.sh = sh;
@@ -388,8 +455,11 @@ cudaError_t launch_gqa(const dcp_attn_desc& d, const void* q, const ShardSet& sh
   p.o_parts = o_parts;
   p.lses = lses;
   p.err = err;
+  p.seq_lens = rs.seq_lens;
   p.B = rs.B;
   p.qlen = rs.qlen;
+  p.ngroups = (rs.qlen + team - 1) / team;
+  p.Bseq = rs.B / p.ngroups;
   p.Hq = d.num_q_heads;
   p.Hkv = d.num_kv_heads;
   p.g = d.num_q_heads / d.num_kv_heads;
@@ -397,9 +467,13 @@ cudaError_t launch_gqa(const dcp_attn_desc& d, const void* q, const ShardSet& sh
   p.Bs = d.block_size;
   p.sl2 = d.scale * kLog2e;
   if (d.head_dim_k == 128) {
-    gqa_partial_kernel<128><<<n_ctas, GqaCfg<128>::kThreads, GqaCfg<128>::kSmem, st>>>(p);
+    if (team == 4) launch_t<128, 4>(p, n_ctas, st);
+    else if (team == 2) launch_t<128, 2>(p, n_ctas, st);
+    else launch_t<128, 1>(p, n_ctas, st);
   } else {
-    gqa_partial_kernel<64><<<n_ctas, GqaCfg<64>::kThreads, GqaCfg<64>::kSmem, st>>>(p);
+    if (team == 4) launch_t<64, 4>(p, n_ctas, st);
+    else if (team == 2) launch_t<64, 2>(p, n_ctas, st);
+    else launch_t<64, 1>(p, n_ctas, st);
   }
   return cudaGetLastError();
 }

@@ -30,10 +30,12 @@ struct ShardSet {
   int32_t max_blocks[kMaxShards];
 };
 
-// How a lane's token range is found: unit u = shard * B + r, where query row
-// r = b * qlen + j is query token j of sequence b (qlen = 1: r = b). Query
-// token j attends positions below its causal limit
-// lim = seq_lens[b] - (qlen - 1 - j):
+// How a lane's token range is found: unit u = shard * B + r, where row group
+// r = b * G + k holds query tokens [k*tpr, min(qlen, (k+1)*tpr)) of sequence
+// b (G = ceil(qlen / tpr); one-token decode: r = b). Query token j attends
+// positions below its causal limit lim_j = seq_lens[b] - (qlen - 1 - j); the
+// group's range is clipped to the limit of its last token (a kernel masks
+// each token at its own limit):
 //   mode 0 (all shards): [starts[b*N+i], i<N-1 ? starts[b*N+i+1] : inf) clipped to lim
 //   mode 1 (one shard) : [range[2b], range[2b+1]) clipped to lim
 struct RangeSpec {
@@ -42,9 +44,10 @@ struct RangeSpec {
   const int32_t* range;   // mode 1
   int32_t* err;           // device error flags (may be NULL)
   int mode;
-  int B;                  // query rows: sequences x qlen
+  int B;                  // row groups per shard: sequences x G
   int N;
   int qlen;               // query tokens per sequence
+  int tpr;                // query tokens per row group
 };
 
 struct LaneRec {     // 32 bytes
@@ -104,13 +107,15 @@ cudaError_t launch_plan(const RangeSpec& rs, int lanes_per_unit, int tile, int n
 cudaError_t launch_gqa(const dcp_attn_desc& d, const void* q, const ShardSet& sh, const RangeSpec& rs,
                        float* o_parts, float* lses, void* ws, const WsLayout& L, int n_ctas,
                        int32_t* err, cudaStream_t st);
-int gqa_ctas(const dcp_attn_desc& d, const DeviceInfo& di);
+// Query tokens that share each K/V tile in the GQA kernel (1, 2 or 4).
+int gqa_team(int qlen);
+int gqa_ctas(const dcp_attn_desc& d, const DeviceInfo& di, int team);
 cudaError_t launch_mla(const dcp_attn_desc& d, const void* q, const ShardSet& sh, const RangeSpec& rs,
                        float* o_parts, float* lses, void* ws, const WsLayout& L, int n_ctas,
                        int32_t* err, cudaStream_t st);
 int mla_ctas(const dcp_attn_desc& d, const DeviceInfo& di);
-cudaError_t launch_combine(const dcp_attn_desc& d, int B, int n_lanes, const void* ws, const WsLayout& L,
-                           float* o_parts, float* lses, cudaStream_t st);
+cudaError_t launch_combine(const dcp_attn_desc& d, const RangeSpec& rs, int n_lanes, const void* ws,
+                           const WsLayout& L, float* o_parts, float* lses, cudaStream_t st);
 cudaError_t launch_merge(const float* o_parts, const float* lses, int N, int rows, int dv, float* o,
                          float* lse_out, cudaStream_t st);
 cudaError_t launch_append(const dcp_attn_desc& d, const ShardSet& sh, int N, const int32_t* starts,

@@ -74,11 +74,18 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __res
 // output rows; writes O = 0, LSE = -inf for lanes with no tokens at all.
 // One warp per (lane, query-head row), float4 columns spread over the lanes;
 // warps of lanes written directly by the attention kernel return at once.
+struct CombineGeom {
+  int Hq, dv, lanes_per_unit, heads_per_lane, groups, g;
+  int B;     // row groups per shard (sequences x token groups)
+  int G;     // token groups per sequence
+  int tpr;   // query tokens per row group
+  int qlen;  // query tokens per sequence
+};
+
 __global__ void __launch_bounds__(kMergeThreads) combine_kernel(const char* __restrict__ ws, WsLayout L,
-                                                                int Hq, int dv, int lanes_per_unit,
-                                                                int heads_per_lane, int groups, int g,
-                                                                float* __restrict__ o_parts,
+                                                                CombineGeom cg, float* __restrict__ o_parts,
                                                                 float* __restrict__ lses) {
+  const int Hq = cg.Hq, dv = cg.dv, groups = cg.groups;
   const int lane = threadIdx.x & 31;
   const int rpl = L.rows_per_lane;
   const long long total = (long long)L.max_lanes * rpl;
@@ -91,19 +98,25 @@ __global__ void __launch_bounds__(kMergeThreads) combine_kernel(const char* __re
     const int lane_id = (int)(w / rpl), r = (int)(w - (long long)lane_id * rpl);
     const LaneRec ln = lrec[lane_id];
     if (ln.n_items == 1) continue;
-    const int u = lane_id / lanes_per_unit, j = lane_id - u * lanes_per_unit;
+    const int u = lane_id / cg.lanes_per_unit, j = lane_id - u * cg.lanes_per_unit;
     int head0, nheads;
     if (groups > 0) {  // GQA lane = (unit, kv head, head group)
       const int kvh = j / groups, hg = j - kvh * groups;
-      head0 = kvh * g + hg * heads_per_lane;
-      nheads = min(heads_per_lane, g - hg * heads_per_lane);
+      head0 = kvh * cg.g + hg * cg.heads_per_lane;
+      nheads = min(cg.heads_per_lane, cg.g - hg * cg.heads_per_lane);
     } else {
       head0 = 0;
       nheads = Hq;
     }
-    if (r >= nheads) continue;
-    float4* dst = reinterpret_cast<float4*>(o_parts + ((size_t)u * Hq + head0 + r) * dv);
-    float* dst_lse = lses + (size_t)u * Hq + head0 + r;
+    // row r of the lane = (query token slot js of the row group, head hr)
+    const int rpt = rpl / cg.tpr;
+    const int js = r / rpt, hr = r - js * rpt;
+    const int shard = u / cg.B, rg = u - shard * cg.B;
+    const int b = rg / cg.G, jt = (rg - b * cg.G) * cg.tpr + js;
+    if (hr >= nheads || jt >= cg.qlen) continue;
+    const size_t orow = ((size_t)shard * (cg.B / cg.G) * cg.qlen + (size_t)b * cg.qlen + jt) * Hq + head0 + hr;
+    float4* dst = reinterpret_cast<float4*>(o_parts + orow * dv);
+    float* dst_lse = lses + orow;
     const int n = ln.n_items;
     float M = -INFINITY;
     for (int i = lane; i < n; i += 32) M = fmaxf(M, tmp_lse[(size_t)(ln.tmp_begin + i) * rpl + r]);
@@ -152,19 +165,27 @@ cudaError_t launch_merge(const float* o_parts, const float* lses, int N, int row
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const dcp_attn_desc& d, int B, int n_lanes, const void* ws, const WsLayout& L,
-                           float* o_parts, float* lses, cudaStream_t st) {
+cudaError_t launch_combine(const dcp_attn_desc& d, const RangeSpec& rs, int n_lanes, const void* ws,
+                           const WsLayout& L, float* o_parts, float* lses, cudaStream_t st) {
   if (n_lanes <= 0) return cudaSuccess;
   const LaneGeom lg = lane_geom(d);
-  const int groups = d.kind == DCP_KIND_GQA ? lg.groups : 0;
-  const int g = d.num_q_heads / d.num_kv_heads;
+  CombineGeom cg;
+  cg.Hq = d.num_q_heads;
+  cg.dv = d.head_dim_v;
+  cg.lanes_per_unit = lg.lanes_per_unit;
+  cg.heads_per_lane = lg.heads_per_lane;
+  cg.groups = d.kind == DCP_KIND_GQA ? lg.groups : 0;
+  cg.g = d.num_q_heads / d.num_kv_heads;
+  cg.tpr = rs.tpr;
+  cg.qlen = rs.qlen;
+  cg.G = (rs.qlen + rs.tpr - 1) / rs.tpr;
+  cg.B = rs.B;
   DeviceInfo di;
   if (device_info(&di) != 0) return cudaErrorUnknown;
   const long long warps = (long long)n_lanes * L.rows_per_lane;
   const long long want = (warps + kMergeThreads / 32 - 1) / (kMergeThreads / 32);
   const int grid = (int)(want < di.sm_count * 16LL ? want : di.sm_count * 16LL);
-  combine_kernel<<<grid, kMergeThreads, 0, st>>>(static_cast<const char*>(ws), L, d.num_q_heads, d.head_dim_v,
-                                                 lg.lanes_per_unit, lg.heads_per_lane, groups, g, o_parts, lses);
+  combine_kernel<<<grid, kMergeThreads, 0, st>>>(static_cast<const char*>(ws), L, cg, o_parts, lses);
   return cudaGetLastError();
 }
 

@@ -57,8 +57,10 @@ __device__ Scan2 block_exclusive_scan2(Scan2 v, Scan2* totals) {
 
 __device__ __forceinline__ void unit_range(const RangeSpec& rs, int u, int* lo, int* hi, int* start) {
   const int i = u / rs.B, r = u - i * rs.B;
-  const int b = r / rs.qlen, j = r - b * rs.qlen;
-  int L = rs.seq_lens[b] - (rs.qlen - 1 - j);  // causal limit of query token j
+  const int G = (rs.qlen + rs.tpr - 1) / rs.tpr;
+  const int b = r / G, k = r - b * G;
+  const int j_last = min(rs.qlen, (k + 1) * rs.tpr) - 1;  // last query token of the group
+  int L = rs.seq_lens[b] - (rs.qlen - 1 - j_last);         // its causal limit
   if (L < 0) L = 0;
   int s, e;
   if (rs.mode == 0) {

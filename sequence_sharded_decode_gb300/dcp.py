@@ -37,7 +37,7 @@ DCP_KIND_GQA = 0
 DCP_KIND_MLA = 1
 
 EXPORTED = ("dcp_status_string", "dcp_version", "dcp_shard_plan", "dcp_kv_append", "dcp_workspace_size",
-            "dcp_decode_partial", "dcp_decode_partial_all", "dcp_decode_partial_all_mtp",
+            "dcp_workspace_size_mtp", "dcp_decode_partial", "dcp_decode_partial_all", "dcp_decode_partial_all_mtp",
             "dcp_decode_partial_all_noalloc", "dcp_merge")
 
 
@@ -113,6 +113,8 @@ def load() -> ctypes.CDLL:
     lib.dcp_kv_append.argtypes = [pdesc, pshard, i32, vp, i32, vp, vp, vp, vp, i32, vp, vp]
     lib.dcp_workspace_size.restype = sz
     lib.dcp_workspace_size.argtypes = [pdesc, i32, i32]
+    lib.dcp_workspace_size_mtp.restype = sz
+    lib.dcp_workspace_size_mtp.argtypes = [pdesc, i32, i32, i32]
     lib.dcp_decode_partial.restype = i32
     lib.dcp_decode_partial.argtypes = [pdesc, vp, pshard, vp, vp, i32, vp, vp, vp, sz, vp, vp]
     lib.dcp_decode_partial_all.restype = i32
@@ -210,6 +212,10 @@ def dcp_workspace_size(desc: AttnDesc, batch: int, n_shards: int) -> int:
     return int(load().dcp_workspace_size(ctypes.byref(desc.c()), batch, n_shards))
 
 
+def dcp_workspace_size_mtp(desc: AttnDesc, batch: int, q_len: int, n_shards: int) -> int:
+    return int(load().dcp_workspace_size_mtp(ctypes.byref(desc.c()), batch, q_len, n_shards))
+
+
 def dcp_decode_partial(desc: AttnDesc, q: torch.Tensor, shard: Shard, seq_lens: torch.Tensor,
                        shard_range: torch.Tensor, o_part: torch.Tensor, lse: torch.Tensor,
                        workspace: torch.Tensor, err: torch.Tensor | None = None, stream=None):
@@ -253,7 +259,7 @@ def dcp_decode_partial_all_mtp(desc: AttnDesc, q: torch.Tensor, shards, seq_lens
     """q [B, q_len, Hq, Dk] bf16: q_len new tokens per sequence, query token j
     at position seq_lens[b] - q_len + j, causal among the new tokens.
     o_parts [N, B, q_len, Hq, Dv], lses [N, B, q_len, Hq]; the workspace is
-    sized for B * q_len query rows."""
+    dcp_workspace_size_mtp(desc, B, q_len, N) bytes."""
     _check(q, torch.bfloat16, "q")
     _check(seq_lens, torch.int32, "seq_lens")
     _check(shard_starts, torch.int32, "shard_starts")

@@ -58,7 +58,7 @@ class DecodeState:
         self.positions = torch.from_numpy(new_t.astype(np.int32)).to(device)
         self.seq_lens = torch.from_numpy((self.ctx + q_len).astype(np.int32)).to(device)
         self.k_new, self.v_new = self.token_rows(new_b, new_t)
-        ws = dcp.dcp_workspace_size(self.desc, B * q_len, N)
+        ws = dcp.dcp_workspace_size_mtp(self.desc, B, q_len, N)
         if ws <= 0:
             raise RuntimeError("dcp_workspace_size failed")
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=device)

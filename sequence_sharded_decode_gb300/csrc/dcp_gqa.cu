@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const 
     const bool active = jtok < p.qlen;
     const int qrow = b * p.qlen + (active ? jtok : 0);      // query row [sequence, token]
     // causal limit of this warp's token (global positions); inactive warps attend nothing
-    const int hi_tok = active ? min(ln.hi, p.seq_lens[b] - (p.qlen - 1 - jtok)) : ln.lo;
+    const int hi_tok = p.qlen == 1 ? ln.hi : active ? min(ln.hi, p.seq_lens[b] - (p.qlen - 1 - jtok)) : ln.lo;
     const int head0 = kvh * p.g + hg * 16;
     const int nheads = min(16, p.g - hg * 16);
 
@@ -254,19 +254,28 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const 
       const uint32_t kb = smem_u32(tbase + st * C::kStageBytes);
       const uint32_t vb = kb + C::kTileBytes;
 
-      // S = Q K^T for the 16 tokens (two 8-token halves)
+      // S = Q K^T for the 16 tokens (two 8-token halves), even and odd
+      // k-steps in separate accumulators so that four MMA chains overlap
       float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       {
+        float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         const int mi = lane >> 3;
         const int r = ((mi >> 1) << 3) + (lane & 7);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; kk += 2) {
+          uint32_t b0, b1, b2, b3, c0, c1, c2, c3;
           const int ch = 2 * kk + (mi & 1);
-          uint32_t b0, b1, b2, b3;
           ldsm_x4(kb + r * C::kRowBytes + ((ch ^ (r & 7)) << 4), b0, b1, b2, b3);
+          ldsm_x4(kb + r * C::kRowBytes + (((ch + 2) ^ (r & 7)) << 4), c0, c1, c2, c3);
           mma16816(s[0], qa[kk], b0, b1);
           mma16816(s[1], qa[kk], b2, b3);
+          mma16816(s2[0], qa[kk + 1], c0, c1);
+          mma16816(s2[1], qa[kk + 1], c2, c3);
         }
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) s[h][e] += s2[h][e];
       }
       // scale to log2 units and mask tokens past the range
 #pragma unroll
@@ -300,12 +309,15 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const 
       }
       l0 = l0 * a0 + (p_[0][0] + p_[0][1] + p_[1][0] + p_[1][1]);
       l1 = l1 * a1 + (p_[0][2] + p_[0][3] + p_[1][2] + p_[1][3]);
+      // once the running maxima settle, a0 = a1 = 1 exactly: skip the rescale
+      if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
-      for (int nd = 0; nd < D / 8; ++nd) {
-        o[nd][0] *= a0;
-        o[nd][1] *= a0;
-        o[nd][2] *= a1;
-        o[nd][3] *= a1;
+        for (int nd = 0; nd < D / 8; ++nd) {
+          o[nd][0] *= a0;
+          o[nd][1] *= a0;
+          o[nd][2] *= a1;
+          o[nd][3] *= a1;
+        }
       }
       // P as the sum of two bf16 terms (hi + residual): the P.V product then
       // carries ~16 mantissa bits of P instead of bf16's 8, so the partial
@@ -363,12 +375,23 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const 
     // merge the teams' states of every query token and write the lane's
     // partial: row R = (token slot js, head r) combines warps js, js + T, ...
     const int rows = T * nheads;
-    const size_t tok_rows = (size_t)p.Bseq * p.qlen;  // query rows per shard
+    float* out_o;  // row (js, r) of the lane: out_o[(js * js_rows + r) * D], out_l[js * js_rows + r]
+    float* out_l;
+    int js_rows;
+    if (it.out_row >= 0) {
+      out_l = tmp_lse + (size_t)it.out_row * p.L.rows_per_lane;
+      out_o = tmp_o + (size_t)it.out_row * p.L.rows_per_lane * D;
+      js_rows = rpl;
+    } else {
+      const size_t row0 = ((size_t)shard * p.Bseq * p.qlen + (size_t)b * p.qlen + tg * T) * p.Hq + head0;
+      out_l = p.lses + row0;
+      out_o = p.o_parts + row0 * D;
+      js_rows = p.Hq;
+    }
     for (int idx = threadIdx.x; idx < rows * D; idx += C::kThreads) {
       const int R = idx / D, c = idx - R * D;
-      const int js = R / nheads, r = R - js * nheads;
-      const int jt = tg * T + js;
-      if (jt >= p.qlen) continue;
+      const int js = T == 1 ? 0 : R / nheads, r = R - js * nheads;
+      if (T > 1 && tg * T + js >= p.qlen) continue;
       float M = -INFINITY;
 #pragma unroll
       for (int tm = 0; tm < kTeams; ++tm)
@@ -384,19 +407,9 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const 
           den += sc * ws[16 * D + 16 + r];
         }
       }
-      float* out_o;
-      float* out_l;
-      if (it.out_row >= 0) {
-        const size_t row = (size_t)it.out_row * p.L.rows_per_lane + js * rpl + r;
-        out_o = tmp_o + row * D;
-        out_l = tmp_lse + row;
-      } else {
-        const size_t row = ((size_t)shard * tok_rows + (size_t)b * p.qlen + jt) * p.Hq + head0 + r;
-        out_o = p.o_parts + row * D;
-        out_l = p.lses + row;
-      }
-      out_o[c] = den > 0.f ? num / den : 0.f;
-      if (c == 0) *out_l = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
+      const size_t row = (size_t)js * js_rows + r;
+      out_o[row * D + c] = den > 0.f ? num / den : 0.f;
+      if (c == 0) out_l[row] = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
     }
     __syncthreads();
   }

@@ -323,3 +323,34 @@ def sharded_mtp_attention(q, K, V, scale: float, starts_b, seq_len: int):
     parts = np.stack([r[2] for r in res], axis=1)
     part_lses = np.stack([r[3] for r in res], axis=1)
     return O, lse, parts, part_lses
+
+
+# ---------------------------------------------------------------------------
+# 8-bit KV cache (e4m3 codes with one scale per tensor)
+# ---------------------------------------------------------------------------
+# P1 lists KV cache quantization among the techniques other serving stacks
+# pair with context parallelism ("KV cache quantization, offloading ..."); it
+# names no format. Reading taken: the cache holds FP8 E4M3 codes (the "fn"
+# variant of the OCP 8-bit floating-point formats: no infinities, one NaN
+# pattern per sign) and one float scale for all keys and one for all values
+# of a layer; a cached key is k_scale * decode(code), a value
+# v_scale * decode(code). Attention over the decoded cache is the plain
+# definition above.
+def e4m3_to_f64(codes) -> np.ndarray:
+    """Exact value of FP8 E4M3 codes (uint8): sign bit, 4 exponent bits with
+    bias 7, 3 mantissa bits. Exponent field 0 holds the subnormals
+    (m / 8) * 2**-6; exponent field 15 with mantissa 7 is NaN; there is no
+    infinity, so exponent 15 with mantissa 0..6 is an ordinary normal
+    (up to 1.75 * 2**8 = 448)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
+def fp8_kv(k_codes, v_codes, k_scale: float, v_scale: float):
+    """Float64 keys and values of an 8-bit cache: scale * decode(code)."""
+    return float(k_scale) * e4m3_to_f64(k_codes), float(v_scale) * e4m3_to_f64(v_codes)

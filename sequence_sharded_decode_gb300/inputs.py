@@ -148,6 +148,39 @@ def sequence_kv(seed: int, stream: int, b: int, lo: int, hi: int, n_heads: int, 
     return kv_tokens(seed, stream, torch.full_like(pos, b), pos, n_heads, width, device)
 
 
+def e4m3_codes(x: torch.Tensor) -> torch.Tensor:
+    """FP8 E4M3 codes (uint8) of bf16 values, rounded to nearest even, with
+    magnitudes above 448 saturated to +-448 and NaN mapped to 0.
+
+    Integer operations only on the bf16 bit patterns, so CPU and GPU give the
+    same codes for the same draws (an 8-bit cache is filled on the device
+    while the checker decodes the same codes on the host)."""
+    if x.dtype != torch.bfloat16:
+        raise TypeError("bf16 input expected")
+    b = x.contiguous().view(torch.int16).to(torch.int64) & 0xFFFF
+    sign = (b >> 8) & 0x80
+    e = (b >> 7) & 0xFF                    # bf16 exponent field (bias 127)
+    m = b & 0x7F                           # 7 mantissa bits
+    E = e - 127                            # unbiased exponent
+    # normal results: exponent field E + 7 in [1, 15], 3 mantissa bits
+    keep = m >> 4
+    rem = m & 0xF
+    up = (rem > 8) | ((rem == 8) & ((keep & 1) == 1))
+    normal = ((E + 7) << 3) + keep + up.to(torch.int64)      # a mantissa carry bumps the exponent
+    # subnormal results (E < -6): round (1.m) * 2^E / 2^-9 = (128 + m) >> (-E - 2)
+    sh = (-E - 2).clamp(min=5, max=40)
+    full = 128 + m
+    q = full >> sh
+    r = full - (q << sh)
+    half = torch.ones_like(sh) << (sh - 1)
+    q = q + ((r > half) | ((r == half) & ((q & 1) == 1))).to(torch.int64)
+    mag = torch.where(E >= -6, normal, q)
+    mag = torch.where(e == 0, torch.zeros_like(mag), mag)    # zeros and bf16 subnormals (< 2^-126) -> 0
+    mag = torch.where(mag > 0x7E, torch.full_like(mag, 0x7E), mag)   # saturate at 448 (0x7F is NaN)
+    mag = torch.where(e == 0xFF, torch.where(m == 0, torch.full_like(mag, 0x7E), torch.zeros_like(mag)), mag)
+    return (sign | mag).to(torch.uint8)
+
+
 def bf16_bits(x: torch.Tensor) -> np.ndarray:
     """Raw uint16 bit patterns of a bf16 tensor (as numpy, on the host)."""
     return x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)

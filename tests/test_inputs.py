@@ -62,3 +62,23 @@ def test_plant_needles_replaces_only_planned_rows():
     assert sorted(tuple(x) for x in changed) == want
     for t, h in plan[0]:
         assert torch.equal(k2[t, h // 4].float(), 4.0 * q[0, h].float())
+
+
+def test_e4m3_codes_match_torch_rounding_for_every_bf16_in_range():
+    # every bf16 bit pattern whose value is finite and at most 448 in magnitude
+    bits = torch.arange(65536, dtype=torch.int64).to(torch.int16)
+    x = bits.view(torch.bfloat16)
+    f = x.to(torch.float32)
+    ok = torch.isfinite(f) & (f.abs() <= 448)
+    ours = inputs.e4m3_codes(x[ok])
+    ref = f[ok].to(torch.float8_e4m3fn).view(torch.uint8)
+    # torch keeps the sign of values that round to zero; so do we
+    assert torch.equal(ours, ref)
+
+
+def test_e4m3_codes_saturate_and_clear_nan():
+    x = torch.tensor([1000.0, -1e30, float("inf"), float("-inf"), float("nan"), 449.0], dtype=torch.bfloat16)
+    c = inputs.e4m3_codes(x).tolist()
+    assert c[:4] == [0x7E, 0xFE, 0x7E, 0xFE]
+    assert c[4] & 0x7F == 0
+    assert c[5] == 0x7E

@@ -46,11 +46,14 @@ def _peaks():
 
 
 def _workload_config(wl, st=None, q_len: int = 1) -> dict:
-    cfg = {"workload": wl.name if q_len == 1 else f"{wl.name}, {q_len} query tokens per sequence", "batch": wl.batch, "q_heads": wl.q_heads, "kv_heads": wl.kv_heads,
+    name = wl.name + (", fp8 KV cache" if wl.kv_dtype == "fp8" else "")
+    cfg = {"workload": name if q_len == 1 else f"{name}, {q_len} query tokens per sequence", "batch": wl.batch, "q_heads": wl.q_heads, "kv_heads": wl.kv_heads,
            "head_dim_k": wl.dk, "head_dim_v": wl.dv, "block_size": wl.block_size, "shards": wl.shards,
            "context": (f"{wl.ctx_fixed}+{q_len}" if wl.ctx_kind == "fixed"
                        else f"lognormal(median {wl.median:g}, sigma {wl.sigma}) in [{wl.ctx_lo},{wl.ctx_hi}] +{q_len}"),
            "fragmented_pools": wl.capacity_factor > 1.0,
+           "kv_cache": ("fp8 e4m3 codes, k_scale %g, v_scale %g" % (wl.k_scale, wl.v_scale)
+                        if wl.kv_dtype == "fp8" else "bf16"),
            "l2": "inputs larger than L2 (KV read per step >> 129 MB); no flush"}
     if st is not None:
         cfg["attended_tokens"] = st.attended_tokens()
@@ -159,6 +162,9 @@ def oracle_prepare(wl, seqs, q_len: int = 1):
         if wl.kind == configs.MLA:
             kb = inputs.bf16_bits(inputs.sequence_kv(wl.seed, inputs.STREAM_LATENT, b, 0, L, 1, wl.dk))
             vb = None
+        elif wl.kv_dtype == "fp8":  # E4M3 codes (uint8) of the same draws
+            kb = inputs.e4m3_codes(inputs.sequence_kv(wl.seed, inputs.STREAM_K, b, 0, L, wl.kv_heads, wl.dk)).numpy()
+            vb = inputs.e4m3_codes(inputs.sequence_kv(wl.seed, inputs.STREAM_V, b, 0, L, wl.kv_heads, wl.dv)).numpy()
         else:
             kb = inputs.bf16_bits(inputs.sequence_kv(wl.seed, inputs.STREAM_K, b, 0, L, wl.kv_heads, wl.dk))
             vb = inputs.bf16_bits(inputs.sequence_kv(wl.seed, inputs.STREAM_V, b, 0, L, wl.kv_heads, wl.dv))
@@ -175,8 +181,11 @@ def oracle_pass(wl, data):
     nbytes = 0
     for b, L, q, kb, vb, starts_b in data:
         qf = O.bf16_bits_to_f64(q)
-        K = O.bf16_bits_to_f64(kb)
-        V = K[:, :, :wl.dv] if vb is None else O.bf16_bits_to_f64(vb)
+        if kb.dtype == np.uint8:
+            K, V = O.fp8_kv(kb, vb, wl.k_scale, wl.v_scale)
+        else:
+            K = O.bf16_bits_to_f64(kb)
+            V = K[:, :, :wl.dv] if vb is None else O.bf16_bits_to_f64(vb)
         if qf.ndim == 2:
             O.sharded_attention(qf, K, V, wl.scale, starts_b, L)
         else:
@@ -382,14 +391,17 @@ def run_ours(args, wl):
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "vs_baseline": None,
+            "dtype": "fp8 e4m3 KV (fp16 MMA, fp32 accumulate)" if wl.kv_dtype == "fp8" else "bf16",
+            "data": "synthetic",
             "config": _workload_config(wl, st, args.q_len) | {"parallelism": f"replicas x{world}"},
             "hbm_frac_of_peak": round(value / world / peak, 4),
             "tokens_per_s_per_layer": round(world * wl.batch * args.q_len / (ms * 1e-3), 1),
             "roofline": {"bound": "hbm", "kernel": "dcp_decode_partial_all (plan + attention + combine)",
                          "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "traffic": _traffic_for(kern, wl.name) if args.q_len == 1 else None,
+                         "traffic": (_traffic_for(kern, wl.name + ("_fp8" if wl.kv_dtype == "fp8" else ""))
+                                     if args.q_len == 1 else None),
                          "algorithmic_bytes_per_launch": bytes_["partial"]},
             "step_bytes": bytes_,
             "e2e": {"value": round(whole_job_gbs(world, step_bytes, e2e_ms), 2), "unit": "GB/s",
@@ -420,6 +432,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override the preset's batch (profiling cases)")
     ap.add_argument("--shards", type=int, default=None, help="override the preset's shard count")
+    ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
+                    help="KV cache element type (fp8: E4M3 codes with per-tensor scales, GQA only)")
     ap.add_argument("--q-len", type=int, default=1,
                     help="query tokens per sequence per step (multi-token / speculative step)")
     args = ap.parse_args()
@@ -433,6 +447,10 @@ def main():
         wl = wl.with_(batch=args.batch)
     if args.shards is not None:
         wl = wl.with_(shards=args.shards)
+    if args.kv_dtype == "fp8":
+        if wl.kind != configs.GQA:
+            ap.error("--kv-dtype fp8 is for GQA workloads")
+        wl = wl.with_(kv_dtype="fp8")
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)

@@ -29,8 +29,10 @@
  *    before shard 0 OR a DCP_DEVERR_* bit into *dev_err_flag (when the pointer
  *    is non-NULL) and skips that access; the caller reads the flag after the
  *    stream is synchronised and clears it itself.
- *  - Data types: KV, queries and appended tokens are bf16 (raw 16-bit
- *    patterns); outputs and partials are fp32; LSE is the natural logarithm.
+ *  - Data types: queries are bf16 (raw 16-bit patterns); the KV cache and
+ *    appended tokens are bf16, or for GQA optionally FP8 E4M3 codes with one
+ *    scale for all keys and one for all values (dcp_attn_desc.kv_dtype);
+ *    outputs and partials are fp32; LSE is the natural logarithm.
  */
 #ifndef DCP_H_
 #define DCP_H_
@@ -69,13 +71,23 @@ typedef enum {
 
 typedef enum { DCP_KIND_GQA = 0, DCP_KIND_MLA = 1 } dcp_kind;
 
+/* Element type of the KV cache. P1 names KV cache quantization among the
+ * techniques serving stacks pair with context parallelism, without a format;
+ * the 8-bit option here is FP8 E4M3 (OCP "fn" variant: bias 7, no
+ * infinities, 0x7F / 0xFF are NaN) with a per-tensor scale: a cached key is
+ * k_scale * decode(code), a value v_scale * decode(code). */
+typedef enum { DCP_KV_BF16 = 0, DCP_KV_FP8_E4M3 = 1 } dcp_kv_dtype;
+
 /* Shape of one attention layer's decode step.
  *  GQA: query head h reads KV head h / (num_q_heads / num_kv_heads);
  *       head_dim_k == head_dim_v in {64, 128}; block_size a multiple of 16.
  *  MLA (absorbed): num_kv_heads == 1; the cached row is the latent of width
  *       head_dim_k (576); the key is the whole row and the value is its first
- *       head_dim_v (512) entries; block_size == 64.
- *  scale multiplies q.k before the softmax (e.g. 1/sqrt(head_dim_k)). */
+ *       head_dim_v (512) entries; block_size == 64; kv_dtype bf16 only.
+ *  scale multiplies q.k before the softmax (e.g. 1/sqrt(head_dim_k)).
+ *  kv_dtype DCP_KV_FP8_E4M3 (GQA only): k_scale and v_scale must be finite
+ *  and > 0; the kernels widen the codes to fp16 exactly and convert q to
+ *  fp16 (|q| must stay below 65504). For bf16 the scales are ignored. */
 typedef struct {
   int kind;          /* dcp_kind */
   int num_q_heads;
@@ -84,11 +96,17 @@ typedef struct {
   int head_dim_v;
   int block_size;    /* tokens per paged block */
   float scale;
+  int kv_dtype;      /* dcp_kv_dtype */
+  float k_scale;     /* FP8 cache: key = k_scale * decode(code) */
+  float v_scale;     /* FP8 cache: value = v_scale * decode(code) */
 } dcp_attn_desc;
 
 /* One shard's paged KV pool and block table (all device memory).
  *  GQA: k_pool [num_blocks, num_kv_heads, block_size, head_dim_k] bf16,
- *       v_pool [num_blocks, num_kv_heads, block_size, head_dim_v] bf16.
+ *       v_pool [num_blocks, num_kv_heads, block_size, head_dim_v] bf16;
+ *       FP8 cache: k_pool [num_blocks, num_kv_heads, block_size, head_dim_k]
+ *       and v_pool [num_blocks, num_kv_heads, head_dim_v, block_size] E4M3
+ *       codes (the values of a block stored transposed, dims by tokens).
  *  MLA: k_pool [num_blocks, block_size, head_dim_k] bf16, v_pool NULL.
  *  block_table: int32 [B, max_blocks_per_seq]; row b maps the shard-local
  *  logical block index (local position / block_size) of sequence b to a
@@ -135,6 +153,8 @@ DCP_API int dcp_shard_plan(const int32_t* ctx_lens, int B, int N, int block_size
  *   seq_ids       device int32 [T] or NULL;   positions device int32 [T]
  *   k_new         device bf16: GQA [T, num_kv_heads, head_dim_k]; MLA [T, head_dim_k]
  *   v_new         device bf16: GQA [T, num_kv_heads, head_dim_v]; MLA NULL
+ *                 (FP8 cache: both E4M3 codes of the same shapes, already
+ *                 quantised by the caller; v_new rows land transposed)
  * Bytes are copied as they are (bit-exact). T == 0 is a no-op. */
 DCP_API int dcp_kv_append(const dcp_attn_desc* desc, const dcp_shard* shards, int N,
                   const int32_t* shard_starts, int B, const int32_t* seq_ids,

@@ -39,6 +39,9 @@ class Workload:
     capacity_factor: float = 1.0   # > 1: fragmented pools with holes
     seed: int = 0
     needles: int = 0               # planted q-aligned keys per sequence (structured parity cases)
+    kv_dtype: str = "bf16"         # "bf16" or "fp8" (E4M3 codes of the bf16 draws, GQA only)
+    k_scale: float = 1.0           # fp8: key = k_scale * decode(code)
+    v_scale: float = 1.0           # fp8: value = v_scale * decode(code)
 
     def ctx_lens(self) -> np.ndarray:
         """Context length of every sequence before the decode step."""
@@ -57,10 +60,11 @@ class Workload:
 
     @property
     def kv_bytes_per_token(self) -> int:
-        """Bytes of KV cache read per attended token (bf16)."""
+        """Bytes of KV cache read per attended token (2 per element, 1 for fp8)."""
+        elem = 1 if self.kv_dtype == "fp8" else 2
         if self.kind == MLA:
-            return 2 * self.dk                      # one latent row; V aliases its prefix
-        return 2 * self.kv_heads * (self.dk + self.dv)
+            return elem * self.dk                   # one latent row; V aliases its prefix
+        return elem * self.kv_heads * (self.dk + self.dv)
 
 
 def _preset(**kw) -> Workload:

@@ -94,6 +94,12 @@ static int check_desc(const dcp_attn_desc* d) {
     return DCP_ERR_SHAPE;
   if (d->num_q_heads % d->num_kv_heads) return DCP_ERR_SHAPE;
   if (!std::isfinite(d->scale)) return DCP_ERR_INVALID_ARG;
+  if (d->kv_dtype != DCP_KV_BF16 && d->kv_dtype != DCP_KV_FP8_E4M3) return DCP_ERR_INVALID_ARG;
+  if (d->kv_dtype == DCP_KV_FP8_E4M3) {
+    if (!std::isfinite(d->k_scale) || !std::isfinite(d->v_scale) || !(d->k_scale > 0.f) || !(d->v_scale > 0.f))
+      return DCP_ERR_INVALID_ARG;
+    if (d->kind != DCP_KIND_GQA) return DCP_ERR_UNSUPPORTED;
+  }
   if (d->kind == DCP_KIND_GQA) {
     if (d->head_dim_k != d->head_dim_v) return DCP_ERR_UNSUPPORTED;
     if (d->head_dim_k != 64 && d->head_dim_k != 128) return DCP_ERR_UNSUPPORTED;
@@ -204,7 +210,7 @@ const char* dcp_status_string(int status) {
   }
 }
 
-int dcp_version(void) { return 200; }
+int dcp_version(void) { return 300; }
 
 int dcp_shard_plan(const int32_t* ctx_lens, int B, int N, int block_size, int reserve_tokens,
                    int32_t* shard_starts, int32_t* blocks_needed) {

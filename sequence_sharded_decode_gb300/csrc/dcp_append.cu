@@ -28,6 +28,8 @@ struct AppendParams {
   int k_vec;  // 16-byte vectors per token row of K (GQA: one head; MLA: the latent)
   int v_vec;
   int mla;
+  int f8;     // 8-bit cache: values are stored transposed within a block
+  int dv;     // head_dim_v (transposed values)
 };
 
 __global__ void __launch_bounds__(kAppendThreads) append_kernel(const __grid_constant__ AppendParams p) {
@@ -73,6 +75,15 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const __grid_con
     const int h = c / p.k_vec, e = c - h * p.k_vec;
     kp[(((size_t)phys * p.Hkv + h) * p.Bs + slot) * p.k_vec + e] = p.k_new[(size_t)tok * p.Hkv * p.k_vec + c];
   }
+  if (p.f8) {  // value pool [nblk, Hkv, Dv, Bs]: byte d of head h goes to row d, column slot
+    unsigned char* vb = static_cast<unsigned char*>(const_cast<void*>(p.sh.v[owner]));
+    const unsigned char* src = reinterpret_cast<const unsigned char*>(p.v_new) + (size_t)tok * p.Hkv * p.dv;
+    for (int c = lane; c < p.Hkv * p.dv; c += 32) {
+      const int h = c / p.dv, d = c - h * p.dv;
+      vb[(((size_t)phys * p.Hkv + h) * p.dv + d) * p.Bs + slot] = src[c];
+    }
+    return;
+  }
   for (int c = lane; c < p.Hkv * p.v_vec; c += 32) {
     const int h = c / p.v_vec, e = c - h * p.v_vec;
     vp[(((size_t)phys * p.Hkv + h) * p.Bs + slot) * p.v_vec + e] = p.v_new[(size_t)tok * p.Hkv * p.v_vec + c];
@@ -98,9 +109,12 @@ cudaError_t launch_append(const dcp_attn_desc& d, const ShardSet& sh, int N, con
   p.T = T;
   p.Hkv = d.num_kv_heads;
   p.Bs = d.block_size;
-  p.k_vec = d.head_dim_k * 2 / 16;
-  p.v_vec = d.head_dim_v * 2 / 16;
+  const int elem = d.kv_dtype == DCP_KV_FP8_E4M3 ? 1 : 2;
+  p.k_vec = d.head_dim_k * elem / 16;
+  p.v_vec = d.head_dim_v * elem / 16;
   p.mla = d.kind == DCP_KIND_MLA;
+  p.f8 = d.kv_dtype == DCP_KV_FP8_E4M3;
+  p.dv = d.head_dim_v;
   const long long blocks = ((long long)T + kAppendThreads / 32 - 1) / (kAppendThreads / 32);
   append_kernel<<<(unsigned)blocks, kAppendThreads, 0, st>>>(p);
   return cudaGetLastError();

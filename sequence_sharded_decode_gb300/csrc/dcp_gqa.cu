@@ -16,6 +16,7 @@
 // (interleaved by warp); the warps' states are merged in shared memory at the
 // end of each item. Scores are kept in log2 units (exp2 on the SFU).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <cmath>
 #include <mutex>
@@ -28,14 +29,59 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int D>
+// F8: the cache holds FP8 E4M3 codes (1 byte per element) instead of bf16;
+// a stage is then half as large and a warp's ring twice as deep.
+__device__ __forceinline__ void mma16816_f16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// hi = fp16(x), lo = fp16(x - hi), packed in pairs for an A fragment
+__device__ __forceinline__ void split_f16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(x0, x1);
+  const float2 hf = __half22float2(h);
+  const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// two E4M3 codes (low byte first) -> fp16 pair (exact: every E4M3 value is an fp16 value)
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  uint32_t r;
+  asm("{\n .reg .b16 t;\n cvt.u16.u32 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}\n" : "=r"(r) : "r"(two_codes));
+  return r;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// bf16 pair -> fp16 pair
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+  const __half2 h = __floats2half2_rn(f.x, f.y);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <int D, bool F8 = false>
 struct GqaCfg {
   static constexpr int kWarps = 4;
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kTile = 16;
-  static constexpr int kStages = D == 128 ? 3 : 4;
-  static constexpr int kRowBytes = D * 2;
-  static constexpr int kChunks = D / 8;                 // 16-byte chunks per row
+  static constexpr int kElem = F8 ? 1 : 2;
+  static constexpr int kStages = (D == 128 ? 3 : 4) * (F8 ? 2 : 1);
+  static constexpr int kRowBytes = D * kElem;
+  static constexpr int kChunks = kRowBytes / 16;        // 16-byte chunks per K row
   static constexpr int kTileBytes = kTile * kRowBytes;  // one K or V tile
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kWarpBytes = kStages * kStageBytes;
@@ -45,6 +91,7 @@ struct GqaCfg {
 
 struct GqaParams {
   const __nv_bfloat16* q;
+  float v_scale;  // 8-bit cache: a value is v_scale * decode(code) (1 otherwise)
   ShardSet sh;
   const char* ws;
   WsLayout L;
@@ -106,9 +153,20 @@ __device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uin
 // copy each tile together into the team's ring (T * kStages stages) and then
 // each warp runs its own query token's 16 head rows over it, so a tile is
 // read once for T query tokens.
-template <int D, int T>
+//
+// F8 (8-bit cache: K as [blocks, Hkv, block_size, D] and V as
+// [blocks, Hkv, D, block_size] E4M3 codes): the codes are widened to fp16 in
+// registers (exactly) and the MMAs run on fp16 with the queries converted
+// to fp16. The score MMA's k-slots (2t, 2t+1, 2t+8, 2t+9) of block kk take
+// the head dims t*D/4 + 4kk .. +3 (the same order for q and K: the dot
+// product is unchanged), so a lane reads its dims of a key row with 128-bit
+// loads; its columns n take the tile's tokens 4*(n/2) + (n%2) (first half)
+// and 4*(n/2) + 2 + (n%2) (second half), so that in the P.V product the
+// tokens a lane holds, 4t .. 4t+3, are one 32-bit word of a transposed value
+// row.
+template <int D, int T, bool F8>
 __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const __grid_constant__ GqaParams p) {
-  using C = GqaCfg<D>;
+  using C = GqaCfg<D, F8>;
   constexpr int kTeams = C::kWarps / T;
   constexpr int kS = T * C::kStages;  // stages of a team's ring
   extern __shared__ __align__(128) unsigned char smem[];
@@ -160,8 +218,8 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const 
     const int head0 = kvh * p.g + hg * 16;
     const int nheads = min(16, p.g - hg * 16);
 
-    const __nv_bfloat16* kpool = static_cast<const __nv_bfloat16*>(p.sh.k[shard]);
-    const __nv_bfloat16* vpool = static_cast<const __nv_bfloat16*>(p.sh.v[shard]);
+    const unsigned char* kpool = static_cast<const unsigned char*>(p.sh.k[shard]);
+    const unsigned char* vpool = static_cast<const unsigned char*>(p.sh.v[shard]);
     const int32_t* table = p.sh.table[shard] + (size_t)b * p.sh.max_blocks[shard];
     const int max_blocks = p.sh.max_blocks[shard];
     const long long nblk = p.sh.nblk[shard];
@@ -174,11 +232,19 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const 
       const bool v0 = gr < nheads, v1 = gr + 8 < nheads;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const int c = kk * 16 + 2 * t4;
-        qa[kk][0] = v0 ? *reinterpret_cast<const uint32_t*>(q0 + c) : 0u;
-        qa[kk][1] = v1 ? *reinterpret_cast<const uint32_t*>(q1 + c) : 0u;
-        qa[kk][2] = v0 ? *reinterpret_cast<const uint32_t*>(q0 + c + 8) : 0u;
-        qa[kk][3] = v1 ? *reinterpret_cast<const uint32_t*>(q1 + c + 8) : 0u;
+        if constexpr (F8) {
+          const int c = t4 * (D / 4) + 4 * kk;  // this lane's four dims of block kk
+          qa[kk][0] = v0 ? bf16x2_to_f16x2(*reinterpret_cast<const uint32_t*>(q0 + c)) : 0u;
+          qa[kk][1] = v1 ? bf16x2_to_f16x2(*reinterpret_cast<const uint32_t*>(q1 + c)) : 0u;
+          qa[kk][2] = v0 ? bf16x2_to_f16x2(*reinterpret_cast<const uint32_t*>(q0 + c + 2)) : 0u;
+          qa[kk][3] = v1 ? bf16x2_to_f16x2(*reinterpret_cast<const uint32_t*>(q1 + c + 2)) : 0u;
+        } else {
+          const int c = kk * 16 + 2 * t4;
+          qa[kk][0] = v0 ? *reinterpret_cast<const uint32_t*>(q0 + c) : 0u;
+          qa[kk][1] = v1 ? *reinterpret_cast<const uint32_t*>(q1 + c) : 0u;
+          qa[kk][2] = v0 ? *reinterpret_cast<const uint32_t*>(q0 + c + 8) : 0u;
+          qa[kk][3] = v1 ? *reinterpret_cast<const uint32_t*>(q1 + c + 8) : 0u;
+        }
       }
     }
 
@@ -212,19 +278,34 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const 
         phys = 0;
       }
       if (lane == 0 && slot == 0) vcount[st] = ntok;
-      const size_t off = (((size_t)phys * p.Hkv + kvh) * p.Bs + slot_in_block) * D;
-      const __nv_bfloat16* ks = kpool + off;
-      const __nv_bfloat16* vs = vpool + off;
       const uint32_t kd = smem_u32(tbase + st * C::kStageBytes);
       const uint32_t vd = kd + C::kTileBytes;
+      if constexpr (F8) {
+        // K rows (16 tokens x D bytes, 16-byte chunks XOR-swizzled by row);
+        // V as D transposed rows of the tile's 16 token bytes, zero past ntok
+        const unsigned char* ks = kpool + (((size_t)phys * p.Hkv + kvh) * p.Bs + slot_in_block) * D;
+        const unsigned char* vs = vpool + ((size_t)phys * p.Hkv + kvh) * D * p.Bs + slot_in_block;
 #pragma unroll
-      for (int c = slot * 32 + lane; c < C::kTile * C::kChunks; c += 32 * T) {
-        const int r = c / C::kChunks, ch = c - r * C::kChunks;
-        const uint32_t so = r * C::kRowBytes + ((ch ^ (r & 7)) << 4);
-        const int bytes = r < ntok ? 16 : 0;
-        const int eo = bytes ? r * D + ch * 8 : 0;
-        cp_async16(kd + so, ks + eo, bytes);
-        cp_async16(vd + so, vs + eo, bytes);
+        for (int c = slot * 32 + lane; c < D; c += 32 * T) {
+          const int r = c / C::kChunks, ch = c - r * C::kChunks;
+          const uint32_t so = r * C::kRowBytes + ((ch ^ (r & (C::kChunks - 1))) << 4);
+          const int bytes = r < ntok ? 16 : 0;
+          cp_async16(kd + so, ks + (bytes ? r * D + ch * 16 : 0), bytes);
+          cp_async16(vd + c * 16, vs + (size_t)c * p.Bs, ntok);
+        }
+      } else {
+        const size_t off = (((size_t)phys * p.Hkv + kvh) * p.Bs + slot_in_block) * D;
+        const __nv_bfloat16* ks = reinterpret_cast<const __nv_bfloat16*>(kpool) + off;
+        const __nv_bfloat16* vs = reinterpret_cast<const __nv_bfloat16*>(vpool) + off;
+#pragma unroll
+        for (int c = slot * 32 + lane; c < C::kTile * C::kChunks; c += 32 * T) {
+          const int r = c / C::kChunks, ch = c - r * C::kChunks;
+          const uint32_t so = r * C::kRowBytes + ((ch ^ (r & 7)) << 4);
+          const int bytes = r < ntok ? 16 : 0;
+          const int eo = bytes ? r * D + ch * 8 : 0;
+          cp_async16(kd + so, ks + eo, bytes);
+          cp_async16(vd + so, vs + eo, bytes);
+        }
       }
     };
 
@@ -257,7 +338,31 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const 
       // S = Q K^T for the 16 tokens (two 8-token halves), even and odd
       // k-steps in separate accumulators so that four MMA chains overlap
       float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      {
+      if constexpr (F8) {
+        float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int row = 4 * (gr >> 1) + 2 * h + (gr & 1);  // the tile token of column gr of half h
+          const uint32_t rb = kb + row * C::kRowBytes;
+          uint32_t w[D / 16];  // word kk: this lane's dims t4*D/4 + 4kk .. +3
+#pragma unroll
+          for (int j = 0; j < D / 64; ++j) {
+            const uint4 v = lds128(rb + (((t4 * (D / 64) + j) ^ (row & (C::kChunks - 1))) << 4));
+            w[4 * j] = v.x;
+            w[4 * j + 1] = v.y;
+            w[4 * j + 2] = v.z;
+            w[4 * j + 3] = v.w;
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma16816_f16((kk & 1) ? s2[h] : s[h], qa[kk], e4m3x2_to_f16x2(w[kk] & 0xFFFFu),
+                         e4m3x2_to_f16x2(w[kk] >> 16));
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) s[h][e] += s2[h][e];
+      } else {
         float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         const int mi = lane >> 3;
         const int r = ((mi >> 1) << 3) + (lane & 7);
@@ -282,7 +387,7 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const 
       for (int h = 0; h < 2; ++h) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int tok = h * 8 + 2 * t4 + (e & 1);
+          const int tok = F8 ? 4 * t4 + 2 * h + (e & 1) : h * 8 + 2 * t4 + (e & 1);
           s[h][e] = tok < ntok ? s[h][e] * p.sl2 : -INFINITY;
         }
       }
@@ -323,12 +428,28 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const 
       // carries ~16 mantissa bits of P instead of bf16's 8, so the partial
       // of a short shard (few tokens, |O| ~ |v|) keeps fp32-level accuracy.
       uint32_t pa[4], pl[4];
-      split_bf16(p_[0][0], p_[0][1], pa[0], pl[0]);
-      split_bf16(p_[0][2], p_[0][3], pa[1], pl[1]);
-      split_bf16(p_[1][0], p_[1][1], pa[2], pl[2]);
-      split_bf16(p_[1][2], p_[1][3], pa[3], pl[3]);
+      if constexpr (F8) {
+        split_f16(p_[0][0], p_[0][1], pa[0], pl[0]);
+        split_f16(p_[0][2], p_[0][3], pa[1], pl[1]);
+        split_f16(p_[1][0], p_[1][1], pa[2], pl[2]);
+        split_f16(p_[1][2], p_[1][3], pa[3], pl[3]);
+      } else {
+        split_bf16(p_[0][0], p_[0][1], pa[0], pl[0]);
+        split_bf16(p_[0][2], p_[0][3], pa[1], pl[1]);
+        split_bf16(p_[1][0], p_[1][1], pa[2], pl[2]);
+        split_bf16(p_[1][2], p_[1][3], pa[3], pl[3]);
+      }
       // O += P V
-      {
+      if constexpr (F8) {
+        // a lane's tokens 4t4 .. 4t4+3 of value row (dim) 8nd + gr: one word
+#pragma unroll
+        for (int nd = 0; nd < D / 8; ++nd) {
+          const uint32_t w = lds32(vb + (nd * 8 + gr) * 16 + t4 * 4);
+          const uint32_t b0 = e4m3x2_to_f16x2(w & 0xFFFFu), b1 = e4m3x2_to_f16x2(w >> 16);
+          mma16816_f16(o[nd], pa, b0, b1);
+          mma16816_f16(o[nd], pl, b0, b1);
+        }
+      } else {
         const int mi = lane >> 3;
         const int r = ((mi & 1) << 3) + (lane & 7);
 #pragma unroll
@@ -408,7 +529,7 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const 
         }
       }
       const size_t row = (size_t)js * js_rows + r;
-      out_o[row * D + c] = den > 0.f ? num / den : 0.f;
+      out_o[row * D + c] = den > 0.f ? (F8 ? num / den * p.v_scale : num / den) : 0.f;
       if (c == 0) out_l[row] = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
     }
     __syncthreads();
@@ -417,7 +538,7 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const 
 
 // Resident CTAs per SM for the kernel, cached per device (the attribute is
 // set once per device, before the first launch there).
-template <int D, int T>
+template <int D, int T, bool F8>
 int occupancy() {
   static std::mutex mu;
   static int cache[64] = {};
@@ -426,24 +547,31 @@ int occupancy() {
   std::lock_guard<std::mutex> lock(mu);
   if (dev < 64 && cache[dev] > 0) return cache[dev];
   int occ = 0;
-  if (cudaFuncSetAttribute(gqa_partial_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           GqaCfg<D>::kSmem) != cudaSuccess)
+  using C = GqaCfg<D, F8>;
+  if (cudaFuncSetAttribute(gqa_partial_kernel<D, T, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
+      cudaSuccess)
     return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gqa_partial_kernel<D, T>, GqaCfg<D>::kThreads,
-                                                    GqaCfg<D>::kSmem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gqa_partial_kernel<D, T, F8>, C::kThreads, C::kSmem) !=
+      cudaSuccess)
     return 0;
   if (dev < 64) cache[dev] = occ;
   return occ;
 }
 
-template <int D>
+template <int D, bool F8>
 int occupancy_for(int team) {
-  return team == 4 ? occupancy<D, 4>() : team == 2 ? occupancy<D, 2>() : occupancy<D, 1>();
+  return team == 4 ? occupancy<D, 4, F8>() : team == 2 ? occupancy<D, 2, F8>() : occupancy<D, 1, F8>();
 }
 
-template <int D, int T>
-void launch_t(const GqaParams& p, int n_ctas, cudaStream_t st) {
-  gqa_partial_kernel<D, T><<<n_ctas, GqaCfg<D>::kThreads, GqaCfg<D>::kSmem, st>>>(p);
+template <int D, bool F8>
+void launch_t(const GqaParams& p, int team, int n_ctas, cudaStream_t st) {
+  using C = GqaCfg<D, F8>;
+  if (team == 4)
+    gqa_partial_kernel<D, 4, F8><<<n_ctas, C::kThreads, C::kSmem, st>>>(p);
+  else if (team == 2)
+    gqa_partial_kernel<D, 2, F8><<<n_ctas, C::kThreads, C::kSmem, st>>>(p);
+  else
+    gqa_partial_kernel<D, 1, F8><<<n_ctas, C::kThreads, C::kSmem, st>>>(p);
 }
 
 }  // namespace
@@ -451,7 +579,9 @@ void launch_t(const GqaParams& p, int n_ctas, cudaStream_t st) {
 int gqa_team(int qlen) { return qlen >= 3 ? 4 : qlen; }
 
 int gqa_ctas(const dcp_attn_desc& d, const DeviceInfo& di, int team) {
-  const int occ = d.head_dim_k == 128 ? occupancy_for<128>(team) : occupancy_for<64>(team);
+  const bool f8 = d.kv_dtype == DCP_KV_FP8_E4M3;
+  const int occ = d.head_dim_k == 128 ? (f8 ? occupancy_for<128, true>(team) : occupancy_for<128, false>(team))
+                                      : (f8 ? occupancy_for<64, true>(team) : occupancy_for<64, false>(team));
   return occ > 0 ? occ * di.sm_count : 0;
 }
 
@@ -460,8 +590,10 @@ cudaError_t launch_gqa(const dcp_attn_desc& d, const void* q, const ShardSet& sh
                        cudaStream_t st) {
   const int team = rs.tpr;
   if (team != 1 && team != 2 && team != 4) return cudaErrorInvalidValue;
+  const bool f8 = d.kv_dtype == DCP_KV_FP8_E4M3;
   GqaParams p;
   p.q = static_cast<const __nv_bfloat16*>(q);
+  p.v_scale = f8 ? d.v_scale : 1.f;
   p.sh = sh;
   p.ws = static_cast<const char*>(ws);
   p.L = L;
@@ -478,15 +610,13 @@ cudaError_t launch_gqa(const dcp_attn_desc& d, const void* q, const ShardSet& sh
   p.g = d.num_q_heads / d.num_kv_heads;
   p.groups = (p.g + 15) / 16;
   p.Bs = d.block_size;
-  p.sl2 = d.scale * kLog2e;
+  p.sl2 = d.scale * (f8 ? d.k_scale : 1.f) * kLog2e;
   if (d.head_dim_k == 128) {
-    if (team == 4) launch_t<128, 4>(p, n_ctas, st);
-    else if (team == 2) launch_t<128, 2>(p, n_ctas, st);
-    else launch_t<128, 1>(p, n_ctas, st);
+    if (f8) launch_t<128, true>(p, team, n_ctas, st);
+    else launch_t<128, false>(p, team, n_ctas, st);
   } else {
-    if (team == 4) launch_t<64, 4>(p, n_ctas, st);
-    else if (team == 2) launch_t<64, 2>(p, n_ctas, st);
-    else launch_t<64, 1>(p, n_ctas, st);
+    if (f8) launch_t<64, true>(p, team, n_ctas, st);
+    else launch_t<64, false>(p, team, n_ctas, st);
   }
   return cudaGetLastError();
 }

@@ -35,6 +35,8 @@ DCP_MAX_SHARDS = 32
 DCP_MAX_QUERY_TOKENS = 64
 DCP_KIND_GQA = 0
 DCP_KIND_MLA = 1
+DCP_KV_BF16 = 0
+DCP_KV_FP8_E4M3 = 1
 
 EXPORTED = ("dcp_status_string", "dcp_version", "dcp_shard_plan", "dcp_kv_append", "dcp_workspace_size",
             "dcp_workspace_size_mtp", "dcp_decode_partial", "dcp_decode_partial_all", "dcp_decode_partial_all_mtp",
@@ -50,7 +52,8 @@ class DcpError(RuntimeError):
 class _Desc(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("num_q_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
                 ("head_dim_k", ctypes.c_int), ("head_dim_v", ctypes.c_int), ("block_size", ctypes.c_int),
-                ("scale", ctypes.c_float)]
+                ("scale", ctypes.c_float), ("kv_dtype", ctypes.c_int), ("k_scale", ctypes.c_float),
+                ("v_scale", ctypes.c_float)]
 
 
 class _Shard(ctypes.Structure):
@@ -67,10 +70,18 @@ class AttnDesc:
     head_dim_v: int
     block_size: int
     scale: float
+    kv_dtype: int = DCP_KV_BF16
+    k_scale: float = 1.0
+    v_scale: float = 1.0
 
     def c(self) -> _Desc:
         return _Desc(self.kind, self.num_q_heads, self.num_kv_heads, self.head_dim_k, self.head_dim_v,
-                     self.block_size, self.scale)
+                     self.block_size, self.scale, self.kv_dtype, self.k_scale, self.v_scale)
+
+    @property
+    def kv_torch_dtype(self):
+        """torch dtype of pools and appended rows: bf16, or uint8 E4M3 codes."""
+        return torch.uint8 if self.kv_dtype == DCP_KV_FP8_E4M3 else torch.bfloat16
 
 
 @dataclass
@@ -81,9 +92,11 @@ class Shard:
     block_table: torch.Tensor
 
     def c(self) -> _Shard:
-        _check(self.k_pool, torch.bfloat16, "k_pool")
+        if self.k_pool.dtype not in (torch.bfloat16, torch.uint8):
+            raise TypeError("k_pool must be bf16 or uint8 (E4M3 codes)")
+        _check(self.k_pool, self.k_pool.dtype, "k_pool")
         if self.v_pool is not None:
-            _check(self.v_pool, torch.bfloat16, "v_pool")
+            _check(self.v_pool, self.k_pool.dtype, "v_pool")
         _check(self.block_table, torch.int32, "block_table")
         return _Shard(self.k_pool.data_ptr(), self.v_pool.data_ptr() if self.v_pool is not None else None,
                       int(self.k_pool.shape[0]), self.block_table.data_ptr(), int(self.block_table.shape[1]))
@@ -192,9 +205,9 @@ def dcp_kv_append(desc: AttnDesc, shards, shard_starts: torch.Tensor, positions:
                   err: torch.Tensor | None = None, stream=None):
     _check(shard_starts, torch.int32, "shard_starts")
     _check(positions, torch.int32, "positions")
-    _check(k_new, torch.bfloat16, "k_new")
+    _check(k_new, desc.kv_torch_dtype, "k_new")
     if v_new is not None:
-        _check(v_new, torch.bfloat16, "v_new")
+        _check(v_new, desc.kv_torch_dtype, "v_new")
     if seq_ids is not None:
         _check(seq_ids, torch.int32, "seq_ids")
     if err is not None:

@@ -25,7 +25,9 @@ class DecodeState:
         self.q_len = q_len
         self.ctx = wl.ctx_lens().astype(np.int64)
         B, N = wl.batch, wl.shards
-        self.desc = dcp.AttnDesc(wl.kind, wl.q_heads, wl.kv_heads, wl.dk, wl.dv, wl.block_size, wl.scale)
+        self.f8 = wl.kv_dtype == "fp8"
+        self.desc = dcp.AttnDesc(wl.kind, wl.q_heads, wl.kv_heads, wl.dk, wl.dv, wl.block_size, wl.scale,
+                                 dcp.DCP_KV_FP8_E4M3 if self.f8 else dcp.DCP_KV_BF16, wl.k_scale, wl.v_scale)
         starts, blocks = dcp.dcp_shard_plan(self.ctx, N, wl.block_size, q_len)
         self.starts_host, self.blocks_host = starts, blocks
         seed_t = wl.seed + 1 if table_seed is None else table_seed
@@ -35,13 +37,20 @@ class DecodeState:
             if wl.kind == configs.MLA:
                 k = torch.empty((cap, wl.block_size, wl.dk), dtype=torch.bfloat16, device=device)
                 v = None
+            elif self.f8:  # E4M3 codes; the values of a block stored transposed (dims x tokens)
+                k = torch.empty((cap, wl.kv_heads, wl.block_size, wl.dk), dtype=torch.uint8, device=device)
+                v = torch.empty((cap, wl.kv_heads, wl.dv, wl.block_size), dtype=torch.uint8, device=device)
             else:
                 k = torch.empty((cap, wl.kv_heads, wl.block_size, wl.dk), dtype=torch.bfloat16, device=device)
                 v = torch.empty((cap, wl.kv_heads, wl.block_size, wl.dv), dtype=torch.bfloat16, device=device)
             if canary is not None:
-                k.view(torch.int16).fill_(canary)
-                if v is not None:
-                    v.view(torch.int16).fill_(canary)
+                if self.f8:
+                    k.fill_(canary & 0xFF)
+                    v.fill_(canary & 0xFF)
+                else:
+                    k.view(torch.int16).fill_(canary)
+                    if v is not None:
+                        v.view(torch.int16).fill_(canary)
             self.shards.append(dcp.Shard(k, v, torch.from_numpy(tab).to(device)))
         self.starts = torch.from_numpy(starts).to(device)
         qstream = inputs.STREAM_Q_MLA if wl.kind == configs.MLA else inputs.STREAM_Q
@@ -81,6 +90,8 @@ class DecodeState:
         k = inputs.kv_tokens(wl.seed, inputs.STREAM_K, b, t, wl.kv_heads, wl.dk, self.device, chunk=1 << 16)
         k = inputs.plant_needles(k, b, t, self.q0, self.needles, wl.q_heads)
         v = inputs.kv_tokens(wl.seed, inputs.STREAM_V, b, t, wl.kv_heads, wl.dv, self.device, chunk=1 << 16)
+        if self.f8:  # the cache holds the E4M3 codes of the same draws
+            return inputs.e4m3_codes(k), inputs.e4m3_codes(v)
         return k, v
 
     def fill_context(self, chunk: int = 1 << 18):
@@ -133,7 +144,7 @@ class DecodeState:
         wl = self.wl
         B, N, Hq, dv, dk = wl.batch * self.q_len, wl.shards, wl.q_heads, wl.dv, wl.dk
         part = N * B * Hq * (dv + 1) * 4
-        new_tok = B * (wl.kv_heads * (dk + dv) * 2 if wl.kind == configs.GQA else dk * 2)
+        new_tok = B * (wl.kv_bytes_per_token if wl.kind == configs.GQA else dk * 2)
         return {
             "append": 2 * new_tok,                      # read the new rows, write them
             "partial": self.kv_bytes() + B * Hq * dk * 2 + part,

@@ -48,8 +48,10 @@ def oracle_kv(wl: configs.Workload, b: int, L: int):
     if plan_b:
         q = inputs.query(wl.seed, np.arange(b + 1), wl.q_heads, wl.dk)
         k = inputs.plant_needles(k, bids, pos, q, plan_b, wl.q_heads)
-    v = f64(inputs.sequence_kv(wl.seed, inputs.STREAM_V, b, 0, L, wl.kv_heads, wl.dv))
-    return f64(k), v
+    v = inputs.sequence_kv(wl.seed, inputs.STREAM_V, b, 0, L, wl.kv_heads, wl.dv)
+    if wl.kv_dtype == "fp8":  # the cache holds the E4M3 codes of the same draws
+        return O.fp8_kv(inputs.e4m3_codes(k).numpy(), inputs.e4m3_codes(v).numpy(), wl.k_scale, wl.v_scale)
+    return f64(k), f64(v)
 
 
 def oracle_sequence(wl: configs.Workload, b: int, L: int, starts_b):

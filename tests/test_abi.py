@@ -168,3 +168,23 @@ def test_multi_token_validation(lib):
     # no sequences: nothing to do, no launch
     assert mtp(ctypes.byref(d), 16, ctypes.byref(good), 1, 16, 16, 0, 4, None, None, None, 0, None,
                None) == dcp.DCP_OK
+
+
+def test_fp8_cache_validation(lib):
+    good = dcp._Shard(16, 16, 4, 16, 2)
+    ok = _desc(kv_dtype=dcp.DCP_KV_FP8_E4M3, k_scale=0.5, v_scale=2.0).c()
+    assert lib.dcp_kv_append(ctypes.byref(ok), ctypes.byref(good), 1, 16, 2, 16, 16, 16, 16, 0, None,
+                             None) == dcp.DCP_OK
+    for kw, status in [
+        (dict(kv_dtype=2), dcp.DCP_ERR_INVALID_ARG),
+        (dict(kv_dtype=dcp.DCP_KV_FP8_E4M3, k_scale=0.0), dcp.DCP_ERR_INVALID_ARG),
+        (dict(kv_dtype=dcp.DCP_KV_FP8_E4M3, v_scale=-1.0), dcp.DCP_ERR_INVALID_ARG),
+        (dict(kv_dtype=dcp.DCP_KV_FP8_E4M3, k_scale=float("inf")), dcp.DCP_ERR_INVALID_ARG),
+        (dict(kv_dtype=dcp.DCP_KV_FP8_E4M3, v_scale=float("nan")), dcp.DCP_ERR_INVALID_ARG),
+        (dict(kind=dcp.DCP_KIND_MLA, num_q_heads=128, num_kv_heads=1, head_dim_k=576, head_dim_v=512,
+              block_size=64, kv_dtype=dcp.DCP_KV_FP8_E4M3), dcp.DCP_ERR_UNSUPPORTED),
+    ]:
+        d = _desc(**kw).c()
+        assert lib.dcp_kv_append(ctypes.byref(d), ctypes.byref(good), 1, 16, 1, None, 16, 16, 16, 1, None,
+                                 None) == status, kw
+        assert lib.dcp_workspace_size(ctypes.byref(d), 1, 1) == 0

@@ -198,8 +198,9 @@ DCP_API int dcp_decode_partial_all(const dcp_attn_desc* desc, const void* q, con
                            float* o_parts, float* lses, void* workspace, size_t ws_bytes,
                            int32_t* dev_err_flag, void* stream);
 
-/* Most query tokens per sequence that dcp_decode_partial_all_mtp accepts. */
-#define DCP_MAX_QUERY_TOKENS 64
+/* Most query tokens per sequence that dcp_decode_partial_all_mtp accepts
+ * (a speculative step's few tokens, or a whole prefill chunk). */
+#define DCP_MAX_QUERY_TOKENS 8192
 
 /* Bytes of workspace dcp_decode_partial_all_mtp needs for B sequences with
  * q_len query tokens each and N shards (0 on invalid input or q_len outside
@@ -217,6 +218,11 @@ DCP_API size_t dcp_workspace_size_mtp(const dcp_attn_desc* desc, int B, int q_le
  * seq_lens[b] - q_len + j and attends every token at or before it -- causal
  * among the new tokens, as q_len consecutive one-token steps would. All q_len
  * tokens' K/V are appended first (dcp_kv_append with T = B * q_len).
+ * The same call is one chunk of a chunked or cached prefill against the
+ * sharded cache ("Inference Systems Infrastructure Notes (7): DCP", section
+ * 4: long inputs prefilled in chunks; already computed KV slices reused):
+ * the chunk's tokens are appended after the cached context and attend it and
+ * each other causally; only q_len differs.
  * Each shard's range is clipped to the query token's causal limit
  * seq_lens[b] - q_len + j + 1; a query token before position 0, or with no
  * token in a shard's range, gets o = 0 and lse = -inf there.

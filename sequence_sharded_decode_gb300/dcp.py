@@ -32,7 +32,7 @@ DCP_DEVERR_POSITION = 4
 DCP_DEVERR_TIMEOUT = 8
 
 DCP_MAX_SHARDS = 32
-DCP_MAX_QUERY_TOKENS = 64
+DCP_MAX_QUERY_TOKENS = 8192
 DCP_KIND_GQA = 0
 DCP_KIND_MLA = 1
 DCP_KV_BF16 = 0

@@ -135,6 +135,13 @@ class DecodeState:
         (with several query tokens, each token is still read from HBM once)."""
         return int((self.ctx + self.q_len).sum())
 
+    def attention_flops(self) -> int:
+        """Multiply-add flops of the partial pass: for every query token, q.k
+        and p.v over each token it attends (2 (Dk + Dv) per head and token)."""
+        wl = self.wl
+        per_seq = self.q_len * (self.ctx + 1) + self.q_len * (self.q_len - 1) // 2  # sum_j (ctx + j + 1)
+        return int(2 * wl.q_heads * (wl.dk + wl.dv) * per_seq.sum())
+
     def kv_bytes(self) -> int:
         """KV bytes the partial-attention pass must read (each attended token once)."""
         return self.attended_tokens() * self.wl.kv_bytes_per_token

@@ -44,7 +44,8 @@ def _masked_route(q, K, V, scale, seq_len):
     return o, lse
 
 
-@pytest.mark.parametrize("L,ql,hq,hkv,d", [(40, 4, 8, 2, 16), (300, 8, 16, 16, 32), (129, 2, 4, 1, 64)])
+@pytest.mark.parametrize("L,ql,hq,hkv,d", [(40, 4, 8, 2, 16), (300, 8, 16, 16, 32), (129, 2, 4, 1, 64),
+                                           (200, 150, 4, 2, 16), (96, 96, 4, 1, 8)])  # prefill chunks
 def test_matches_masked_sdpa(L, ql, hq, hkv, d):
     q, K, V = _rand(ql, hq, d), _rand(L, hkv, d), _rand(L, hkv, d)
     scale = 1.0 / math.sqrt(d)

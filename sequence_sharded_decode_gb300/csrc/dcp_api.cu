@@ -72,17 +72,43 @@ LaneGeom lane_geom(const dcp_attn_desc& d) {
   return g;
 }
 
-// Query rows of one lane: the heads of its group times the query tokens that
-// share its K/V tiles (GQA team of a multi-token step; 1 otherwise).
-static int rows_per_lane(const dcp_attn_desc& d, int team) {
-  if (d.kind == DCP_KIND_MLA) return d.num_q_heads;
+// Which kernel serves a step and how its lanes are cut.
+//  MLA: one lane per (shard, query row), 128 head rows, 64-token tiles.
+//  GQA, many rows per KV head (gqa_tc_eligible): one lane per (shard,
+//    sequence, group of 128/g query tokens, KV head), 128 rows, 64-token
+//    tiles, the tcgen05 kernel.
+//  GQA otherwise: one lane per (shard, sequence, group of `team` query
+//    tokens, KV head, group of up to 16 heads), 16-token tiles, the mma.sync
+//    kernel whose team of warps shares each tile.
+struct Path {
+  LaneGeom lg;
+  int tc;             // the tcgen05 GQA kernel
+  int tpr;            // query tokens per row group
+  int rows_per_lane;  // query rows of one lane
+};
+static Path path_for(const dcp_attn_desc& d, int q_len) {
+  Path p;
+  p.lg = lane_geom(d);
+  p.tc = 0;
+  if (d.kind == DCP_KIND_MLA) {
+    p.tpr = 1;
+    p.rows_per_lane = d.num_q_heads;
+    return p;
+  }
   const int grp = d.num_q_heads / d.num_kv_heads;
-  return (grp < 16 ? grp : 16) * team;
-}
-
-// Query tokens per row group for a step with q_len tokens per sequence.
-static int team_for(const dcp_attn_desc& d, int q_len) {
-  return d.kind == DCP_KIND_MLA ? 1 : gqa_team(q_len);
+  if (gqa_tc_eligible(d, q_len)) {
+    p.tc = 1;
+    p.tpr = gqa_tc_rows_tokens(d);
+    p.rows_per_lane = 128;
+    p.lg.heads_per_lane = grp;
+    p.lg.groups = 1;
+    p.lg.lanes_per_unit = d.num_kv_heads;
+    p.lg.tile = 64;
+    return p;
+  }
+  p.tpr = gqa_team(q_len);
+  p.rows_per_lane = (grp < 16 ? grp : 16) * p.tpr;
+  return p;
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -132,40 +158,43 @@ static int check_shards(const dcp_attn_desc& d, const dcp_shard* s, int N, Shard
   return DCP_OK;
 }
 
-static int work_ctas(const dcp_attn_desc& d, const DeviceInfo& di, int team) {
-  return d.kind == DCP_KIND_MLA ? mla_ctas(d, di) : gqa_ctas(d, di, team);
+static int work_ctas(const dcp_attn_desc& d, const DeviceInfo& di, const Path& p) {
+  if (d.kind == DCP_KIND_MLA) return mla_ctas(d, di);
+  return p.tc ? gqa_tc_ctas(d, di) : gqa_ctas(d, di, p.tpr);
 }
 
 // Workspace layout for B row groups per shard (sequences x token groups).
-static int layout_for(const dcp_attn_desc& d, int B, int N, int team, WsLayout* L, int* n_ctas) {
+static int layout_for(const dcp_attn_desc& d, int B, int N, const Path& p, WsLayout* L, int* n_ctas) {
   DeviceInfo di;
   if (device_info(&di) != 0) return DCP_ERR_CUDA;
-  const int c = work_ctas(d, di, team);
+  const int c = work_ctas(d, di, p);
   if (c <= 0) return DCP_ERR_CUDA;
-  const LaneGeom g = lane_geom(d);
-  const long long lanes = (long long)B * N * g.lanes_per_unit;
+  const long long lanes = (long long)B * N * p.lg.lanes_per_unit;
   if (lanes > (1 << 26)) return DCP_ERR_SHAPE;
-  *L = ws_layout((int)lanes, c, rows_per_lane(d, team), d.head_dim_v);
+  *L = ws_layout((int)lanes, c, p.rows_per_lane, d.head_dim_v);
   *n_ctas = c;
   return DCP_OK;
 }
 
-static int run_partial(const dcp_attn_desc* desc, const void* q, const ShardSet& sh, const RangeSpec& rs,
-                       float* o_parts, float* lses, void* ws, size_t ws_bytes, int32_t* err, void* stream) {
+static int run_partial(const dcp_attn_desc* desc, const Path& path, const void* q, const ShardSet& sh,
+                       const RangeSpec& rs, float* o_parts, float* lses, void* ws, size_t ws_bytes, int32_t* err,
+                       void* stream) {
   const dcp_attn_desc& d = *desc;
   WsLayout L;
   int n_ctas = 0;
-  int rc = layout_for(d, rs.B, rs.N, rs.tpr, &L, &n_ctas);
+  int rc = layout_for(d, rs.B, rs.N, path, &L, &n_ctas);
   if (rc != DCP_OK) return rc;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < L.total) return DCP_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const LaneGeom g = lane_geom(d);
+  const LaneGeom& g = path.lg;
   if (launch_plan(rs, g.lanes_per_unit, g.tile, n_ctas, ws, L, st) != cudaSuccess) return DCP_ERR_CUDA;
-  cudaError_t e = d.kind == DCP_KIND_MLA ? launch_mla(d, q, sh, rs, o_parts, lses, ws, L, n_ctas, err, st)
-                                         : launch_gqa(d, q, sh, rs, o_parts, lses, ws, L, n_ctas, err, st);
+  cudaError_t e;
+  if (d.kind == DCP_KIND_MLA) e = launch_mla(d, q, sh, rs, o_parts, lses, ws, L, n_ctas, err, st);
+  else if (path.tc) e = launch_gqa_tc(d, q, sh, rs, o_parts, lses, ws, L, n_ctas, err, st);
+  else e = launch_gqa(d, q, sh, rs, o_parts, lses, ws, L, n_ctas, err, st);
   if (e == cudaErrorNotSupported) return DCP_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return DCP_ERR_CUDA;
-  if (launch_combine(d, rs, L.max_lanes, ws, L, o_parts, lses, st) != cudaSuccess) return DCP_ERR_CUDA;
+  if (launch_combine(d, g, rs, L.max_lanes, ws, L, o_parts, lses, st) != cudaSuccess) return DCP_ERR_CUDA;
   return DCP_OK;
 }
 
@@ -264,12 +293,12 @@ size_t dcp_workspace_size(const dcp_attn_desc* desc, int B, int N) {
 size_t dcp_workspace_size_mtp(const dcp_attn_desc* desc, int B, int q_len, int N) {
   if (check_desc(desc) != DCP_OK || B < 0 || N < 1 || N > DCP_MAX_SHARDS) return 0;
   if (q_len < 1 || q_len > DCP_MAX_QUERY_TOKENS) return 0;
-  const int team = team_for(*desc, q_len);
-  const long long rows = (long long)B * ((q_len + team - 1) / team);
+  const Path path = path_for(*desc, q_len);
+  const long long rows = (long long)B * ((q_len + path.tpr - 1) / path.tpr);
   if (rows > INT32_MAX) return 0;
   WsLayout L;
   int n_ctas = 0;
-  if (layout_for(*desc, (int)rows, N, team, &L, &n_ctas) != DCP_OK) return 0;
+  if (layout_for(*desc, (int)rows, N, path, &L, &n_ctas) != DCP_OK) return 0;
   return L.total;
 }
 
@@ -286,7 +315,7 @@ int dcp_decode_partial(const dcp_attn_desc* desc, const void* q, const dcp_shard
   if (!q || !seq_lens || !shard_range || !o_part || !lse) return DCP_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(o_part)) return DCP_ERR_INVALID_ARG;
   RangeSpec rs{seq_lens, nullptr, shard_range, dev_err_flag, 1, B, 1, 1, 1};
-  return run_partial(desc, q, sh, rs, o_part, lse, workspace, ws_bytes, dev_err_flag, stream);
+  return run_partial(desc, path_for(*desc, 1), q, sh, rs, o_part, lse, workspace, ws_bytes, dev_err_flag, stream);
 }
 
 int dcp_decode_partial_all(const dcp_attn_desc* desc, const void* q, const dcp_shard* shards, int N,
@@ -310,10 +339,11 @@ int dcp_decode_partial_all_mtp(const dcp_attn_desc* desc, const void* q, const d
   if (!q || !seq_lens || !shard_starts || !o_parts || !lses) return DCP_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(o_parts)) return DCP_ERR_INVALID_ARG;
   if ((long long)B * q_len > INT32_MAX) return DCP_ERR_SHAPE;
-  const int team = team_for(*desc, q_len);
-  const int groups = (q_len + team - 1) / team;
-  RangeSpec rs{seq_lens, shard_starts, nullptr, dev_err_flag, 0, B * groups, N, q_len, team};
-  return run_partial(desc, q, sh, rs, o_parts, lses, workspace, ws_bytes, dev_err_flag, stream);
+  const Path path = path_for(*desc, q_len);
+  const long long groups = (q_len + path.tpr - 1) / path.tpr;
+  if ((long long)B * groups > INT32_MAX) return DCP_ERR_SHAPE;
+  RangeSpec rs{seq_lens, shard_starts, nullptr, dev_err_flag, 0, (int)(B * groups), N, q_len, path.tpr};
+  return run_partial(desc, path, q, sh, rs, o_parts, lses, workspace, ws_bytes, dev_err_flag, stream);
 }
 
 int dcp_decode_partial_all_noalloc(const dcp_attn_desc* desc, const void* q, const dcp_shard* shards, int N,
@@ -330,14 +360,15 @@ int dcp_decode_partial_all_noalloc(const dcp_attn_desc* desc, const void* q, con
   if (!aligned16(q) || !aligned16(o_parts)) return DCP_ERR_INVALID_ARG;
   WsLayout L;
   int n_ctas = 0;
-  rc = layout_for(*desc, B, N, 1, &L, &n_ctas);
+  const Path path = path_for(*desc, 1);
+  rc = layout_for(*desc, B, N, path, &L, &n_ctas);
   if (rc != DCP_OK) return rc;
   if (L.total > DCP_NOALLOC_SCRATCH_BYTES) return DCP_ERR_SCRATCH_LIMIT;
   void* ws = nullptr;
   rc = noalloc_scratch(&ws);
   if (rc != DCP_OK) return rc;
   RangeSpec rs{seq_lens, shard_starts, nullptr, dev_err_flag, 0, B, N, 1, 1};
-  return run_partial(desc, q, sh, rs, o_parts, lses, ws, DCP_NOALLOC_SCRATCH_BYTES, dev_err_flag, stream);
+  return run_partial(desc, path, q, sh, rs, o_parts, lses, ws, DCP_NOALLOC_SCRATCH_BYTES, dev_err_flag, stream);
 }
 
 int dcp_merge(const float* o_parts, const float* lses, int N, int B, int Hq, int Dv, float* o, float* lse_out,

@@ -1,0 +1,716 @@
+// Partial attention of many query rows per KV head (GQA, head dim 128) on
+// the 5th-generation tensor cores (tcgen05 + TMEM + TMA) of sm_103a: the
+// multi-token steps and prefill chunks whose query rows fill the 128 rows of
+// the MMA.
+//
+// What it computes is step 2 of the method for every query token of the
+// step (each shard attends the queries against its own KV slice only and
+// emits a partial output plus LSE -- Qiita write-up "vLLMの-dcpが長文脈のKV
+// キャッシュ重複を消して3倍速くする", section "トークンの区間でGPUに割り振る"),
+// applied to the chunked / cached prefill of "Inference Systems
+// Infrastructure Notes (7): DCP", section 4: query token j of sequence b sits
+// at position seq_len - q_len + j and attends every token at or before it.
+//
+// Layout of the work: a lane is (shard, sequence, token group, KV head); its
+// 128 query rows are the 128/g tokens of the group times the g query heads of
+// the KV head (row r = token slot r / g, head r % g). Per 64-token tile of the
+// lane's range:
+//   1. S = Q . K^T (M=128 rows, N=64 tokens, K=128) into TMEM, the queries
+//      being the MMA's A operand in TMEM
+//   2. online softmax per row (thread r owns TMEM lane r), causal at the
+//      row's own token, in log2 units, lazy rescale of O (only when the
+//      running max grows by more than 2^8)
+//   3. P is written to shared memory as two bf16 terms, hi = bf16(p) and
+//      lo = bf16(p - hi); the P_lo . V product is issued only for tiles that
+//      carry more than 1/32 of some row's running weight (elsewhere dropping
+//      it changes O by at most 2^-9 x that share x max|v|), the residual
+//      itself being stored for every row on every tile
+//   4. O += P_hi . V (M=128, N=128, K=64) into TMEM, V being read by the MMA
+//      straight from the copy of the tile (dims contiguous)
+// TMA brings the K and V rows of a tile from the paged pools (boxes of
+// min(block_size, 64) rows x 64 columns, 128-byte swizzle) into a 4-stage
+// ring. One warp schedules the MMAs (non-blocking barrier polls, uniform
+// control flow, one elect.sync-chosen lane issues); one warp copies; four
+// warps run the softmax and the epilogue. Every barrier's phases are
+// observed in order and never more than one phase late; every wait is
+// bounded: on expiry the kernel raises DCP_DEVERR_TIMEOUT, stops all roles,
+// drains what it issued and frees TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "dcp_internal.cuh"
+
+namespace dcp {
+namespace {
+
+constexpr int kRows = 128;                 // query rows of a lane (MMA M)
+constexpr int kD = 128;                    // head dim (K and V)
+constexpr int kTile = 64;                  // tokens per tile (MMA N of S, K of P.V)
+constexpr int kStages = 4;
+constexpr int kThreads = 192;              // 4 softmax warps, copy warp, MMA warp
+constexpr int kChunkBytes = kTile * 128;   // 64 rows x 64 bf16 (one 128-byte-swizzled box column)
+constexpr int kKBytes = 2 * kChunkBytes;   // K rows of a tile: dims 0-63 | 64-127
+constexpr int kStageBytes = 2 * kKBytes;   // K then V
+constexpr int kPBytes = kRows * 128;       // 128 rows x 64 tokens bf16 (one term)
+
+constexpr int kOffKv = 0;
+constexpr int kOffP = kOffKv + kStages * kStageBytes;  // hi at kOffP, lo at kOffP + kPBytes
+constexpr int kOffBar = kOffP + 2 * kPBytes;
+constexpr int kNumBars = 16;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag, lo flags
+constexpr int kSmemUsed = kOffMisc + 32;
+constexpr int kSmemBytes = kSmemUsed + 1024;      // slack to align the base to 1024
+
+constexpr int BQ_FULL = 0, BQ_EMPTY = 1, BS_FULL = 2, BS_EMPTY = 3, BP_FULL = 4, BP_EMPTY = 5, BDRAIN = 6,
+              BKV_FULL = 7, BKV_EMPTY = 7 + kStages;
+static_assert(BKV_EMPTY + kStages <= kNumBars, "barrier slots");
+
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColO = 0;    // 128 columns: O, fp32
+constexpr uint32_t kColS = 128;  // 64 columns: S, fp32
+constexpr uint32_t kColQ = 192;  // 64 columns: Q, bf16 pairs
+constexpr uint32_t kSpinLimit = 1u << 24;
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+constexpr float kLoFraction = 1.0f / 32.0f;  // tile share of the row sum above which P_lo . V is issued
+
+struct TcParams {
+  CUtensorMap tm_k[kMaxShards];
+  CUtensorMap tm_v[kMaxShards];
+  ShardSet sh;
+  const __nv_bfloat16* q;
+  const int32_t* seq_lens;
+  const char* ws;
+  WsLayout L;
+  float* o_parts;
+  float* lses;
+  int32_t* err;
+  int B;      // row groups per shard: sequences x token groups
+  int qlen;   // query tokens per sequence
+  int G;      // token groups per sequence
+  int tpr;    // query tokens per lane (128 / g)
+  int g;      // query heads per KV head
+  int Hq, Hkv, Bs;
+  int box;    // rows of a copy box: min(block_size, 64)
+  float sl2;  // scale * log2(e)
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t saddr(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+__device__ __forceinline__ void bar_init(uint32_t b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(b), "r"(count));
+}
+__device__ __forceinline__ void bar_arrive(uint32_t b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(b) : "memory");
+}
+__device__ __forceinline__ void bar_arrive_tx(uint32_t b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(b), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool bar_try(uint32_t b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok) : "r"(b), "r"(parity) : "memory");
+  return ok != 0;
+}
+// Non-blocking probe (never suspends the thread), polled by a whole warp.
+__device__ __forceinline__ bool bar_test(uint32_t b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok) : "r"(b), "r"(parity) : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool bar_test_warp(uint32_t b, uint32_t parity) {
+  return __all_sync(0xffffffffu, bar_test(b, parity));
+}
+// Bounded wait; false if the kernel is aborting.
+__device__ __noinline__ bool wait_bar(uint32_t b, uint32_t parity, volatile int* abort_flag, int32_t* err) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (bar_try(b, parity)) return true;
+    if ((i & 63u) == 63u && *abort_flag) return false;
+  }
+  *abort_flag = 1;
+  raise_flag(err, DCP_DEVERR_TIMEOUT);
+  return false;
+}
+// Warp-uniform bounded wait (the .sync.aligned TMEM accesses that follow
+// always run with the whole warp).
+__device__ __forceinline__ bool wait_warp(uint32_t b, uint32_t parity, volatile int* abort_flag, int32_t* err) {
+  const bool ok = wait_bar(b, parity, abort_flag, err);
+  return __all_sync(0xffffffffu, ok);
+}
+// Bounded wait that ignores the abort flag (teardown drains).
+__device__ __forceinline__ void drain_bar(uint32_t b, uint32_t parity) {
+  for (uint32_t i = 0; i < (1u << 22); ++i)
+    if (bar_try(b, parity)) return;
+}
+__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar) : "memory");
+}
+// Shared-memory matrix descriptor: 128-byte swizzle, 8-row groups 1024 B
+// apart; lbo = byte stride between 64-element atoms along M/N (MN-major).
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo) {
+  uint64_t d = (uint64_t)((addr >> 4) & 0x3FFF);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= 1ull << 46;  // descriptor version for tcgen05
+  d |= 2ull << 61;  // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor, kind::f16: bf16 A/B, fp32 accumulate.
+__host__ __device__ constexpr uint32_t idesc(int M, int N, int b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn_major << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id, int accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+      ::"r"(d), "l"(a), "l"(b), "r"(id), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id, int accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+      ::"r"(d), "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+               " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n"
+               :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]) : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+// 2^x on the SFU, denormal results flushed to zero
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t pack_bf16(float x0, float x1) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t residual_bf16(float x0, float x1) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  return pack_bf16(x0 - hf.x, x1 - hf.y);
+}
+
+// Geometry of one work item, derived identically by every role.
+struct ItemGeom {
+  int lane, shard, b, tg, kvh, t0, t1, out_row, lo, hi, start;
+};
+__device__ __forceinline__ ItemGeom item_geom(const TcParams& p, int k) {
+  const ItemRec it = reinterpret_cast<const ItemRec*>(p.ws + p.L.items_off)[k];
+  const LaneRec ln = reinterpret_cast<const LaneRec*>(p.ws + p.L.lanes_off)[it.lane];
+  ItemGeom g;
+  g.lane = it.lane;
+  const int u = it.lane / p.Hkv;
+  g.kvh = it.lane - u * p.Hkv;
+  g.shard = u / p.B;
+  const int rg = u - g.shard * p.B;
+  g.b = rg / p.G;
+  g.tg = rg - g.b * p.G;
+  g.t0 = it.t0;
+  g.t1 = it.t1;
+  g.out_row = it.out_row;
+  g.lo = ln.lo;
+  g.hi = ln.hi;
+  g.start = ln.start;
+  return g;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) gqa_tc_kernel(const __grid_constant__ TcParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = saddr(smem_raw);
+  unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  const uint32_t sbase = saddr(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto bar = [&](int i) { return sbase + kOffBar + 8u * i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* lo_flags = reinterpret_cast<volatile int*>(smem + kOffMisc + 16);  // one per softmax warp
+
+  if (threadIdx.x == 0) {
+    bar_init(bar(BQ_FULL), kRows);  // every softmax thread wrote its query row into TMEM
+    bar_init(bar(BQ_EMPTY), 1);
+    bar_init(bar(BS_FULL), 1);
+    bar_init(bar(BS_EMPTY), kRows);
+    bar_init(bar(BP_FULL), kRows);
+    bar_init(bar(BP_EMPTY), 1);
+    bar_init(bar(BDRAIN), 1);
+    for (int s = 0; s < kStages; ++s) {
+      bar_init(bar(BKV_FULL + s), 1);
+      bar_init(bar(BKV_EMPTY + s), 1);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if (warp == 5) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(saddr(tmem_slot)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int* cta_begin = reinterpret_cast<const int*>(p.ws + p.L.cta_off);
+  const int k_begin = cta_begin[blockIdx.x], k_end = cta_begin[blockIdx.x + 1];
+  const int pieces = kTile / p.box;  // copy boxes per tile (1, 2 or 4)
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ copy
+    // Lane i < pieces looks up the block of piece i of the tile; lane 0
+    // issues the boxes (K and V, two 64-column halves each).
+    uint32_t fills = 0;
+    bool stop = false;
+    for (int k = k_begin; k < k_end && !stop; ++k) {
+      const ItemGeom g = item_geom(p, k);
+      const int32_t* table = p.sh.table[g.shard] + (size_t)g.b * p.sh.max_blocks[g.shard];
+      const int local_hi = g.hi - g.start;
+      for (int j = 0; j < g.t1 - g.t0; ++j) {
+        const int lp0 = (g.lo - g.start) + (g.t0 + j) * kTile;  // local position of the tile's first token
+        int row = -p.box;  // out of range: the box reads zeros
+        if (lane < pieces) {
+          const int lp = lp0 + lane * p.box;
+          if (lp < local_hi) {  // a piece with tokens of the range
+            const int lb = lp / p.Bs, off = lp - lb * p.Bs;
+            if (lb >= p.sh.max_blocks[g.shard]) {
+              raise_flag(p.err, DCP_DEVERR_TABLE_RANGE);
+            } else {
+              const int phys = table[lb];
+              if (phys < 0 || phys >= p.sh.nblk[g.shard]) {
+                raise_flag(p.err, DCP_DEVERR_BLOCK_RANGE);
+              } else {
+                row = (phys * p.Hkv + g.kvh) * p.Bs + off;
+              }
+            }
+          }
+        }
+        int rows[4];  // the pieces' first pool rows, gathered by the whole warp
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rows[i] = __shfl_sync(0xffffffffu, row, i);
+        bool ok = true;
+        if (lane == 0) {
+          const uint32_t s = fills % kStages, use = fills / kStages;
+          if (use > 0 && !wait_bar(bar(BKV_EMPTY + s), (use - 1) & 1u, abort_flag, p.err)) ok = false;
+        }
+        if (lane == 0 && ok) {
+          const uint32_t s = fills % kStages;
+          const uint32_t st = sbase + kOffKv + s * kStageBytes;
+          bar_arrive_tx(bar(BKV_FULL + s), kStageBytes);  // pieces x box rows x (2 + 2) x 128 B
+          for (int i = 0; i < pieces; ++i) {
+            const uint32_t dst = st + i * p.box * 128;
+            tma_load(dst, &p.tm_k[g.shard], 0, rows[i], bar(BKV_FULL + s));
+            tma_load(dst + kChunkBytes, &p.tm_k[g.shard], 64, rows[i], bar(BKV_FULL + s));
+            tma_load(dst + kKBytes, &p.tm_v[g.shard], 0, rows[i], bar(BKV_FULL + s));
+            tma_load(dst + kKBytes + kChunkBytes, &p.tm_v[g.shard], 64, rows[i], bar(BKV_FULL + s));
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) { stop = true; break; }
+        ++fills;
+      }
+    }
+    if (lane == 0 && *abort_flag) {  // copies in flight must land before the CTA may exit
+      const uint32_t f0 = fills > (uint32_t)kStages ? fills - kStages : 0;
+      for (uint32_t f = f0; f < fills; ++f) drain_bar(bar(BKV_FULL + f % kStages), (f / kStages) & 1u);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issue
+    const uint32_t id_s = idesc(kRows, kTile, 0);
+    const uint32_t id_pv = idesc(kRows, kD, 1);
+    const uint64_t pdesc0 = sdesc(sbase + kOffP, 0);
+    auto n_tiles = [&](int k) {
+      const ItemRec it = reinterpret_cast<const ItemRec*>(p.ws + p.L.items_off)[k];
+      return it.t1 - it.t0;
+    };
+    int ks = k_begin, js = 0, nts = ks < k_end ? n_tiles(ks) : 0;  // next score tile
+    int kp = k_begin, jp = 0, ntp = nts;                            // next P.V tile
+    uint32_t g_s = 0, g_p = 0, q_loads = 0;
+    bool q_ready = false;
+    uint32_t idle = 0;
+    while (kp < k_end) {
+      bool progressed = false;
+      if (ks < k_end) {
+        if (!q_ready && bar_test_warp(bar(BQ_FULL), q_loads & 1u)) {
+          q_ready = true;
+          tc_fence_after();
+        }
+        const uint32_t s = g_s % kStages;
+        if (q_ready && bar_test_warp(bar(BKV_FULL + s), (g_s / kStages) & 1u) &&
+            (g_s == 0 || bar_test_warp(bar(BS_EMPTY), (g_s - 1) & 1u))) {
+          tc_fence_after();
+          const uint64_t kd = sdesc(sbase + kOffKv + s * kStageBytes, 0);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            mma_ts(tmem + kColS, tmem + kColQ + 8 * kk,
+                   kd + (uint64_t)((((kk >> 2) * kChunkBytes) + 32 * (kk & 3)) >> 4), id_s, kk > 0);
+          mma_commit(bar(BS_FULL));
+          if (++js == nts) {  // last score tile of the item: its queries may be replaced
+            mma_commit(bar(BQ_EMPTY));
+            ++ks;
+            js = 0;
+            nts = ks < k_end ? n_tiles(ks) : 0;
+            ++q_loads;
+            q_ready = false;
+          }
+          ++g_s;
+          progressed = true;
+        }
+      }
+      if (g_p < g_s && bar_test_warp(bar(BP_FULL), g_p & 1u)) {
+        tc_fence_after();
+        const uint32_t s = g_p % kStages;
+        const uint64_t vd = sdesc(sbase + kOffKv + s * kStageBytes + kKBytes, kChunkBytes);
+        const int terms = (lo_flags[0] | lo_flags[1] | lo_flags[2] | lo_flags[3]) ? 2 : 1;
+#pragma unroll
+        for (int term = 0; term < 2; ++term) {
+          if (term >= terms) break;
+#pragma unroll
+          for (int kt = 0; kt < kTile / 16; ++kt)
+            mma_ss(tmem + kColO, pdesc0 + (uint64_t)((term * kPBytes + 32 * kt) >> 4),
+                   vd + (uint64_t)((2048 * kt) >> 4), id_pv, (jp == 0 && term == 0 && kt == 0) ? 0 : 1);
+        }
+        mma_commit(bar(BKV_EMPTY + s));
+        mma_commit(bar(BP_EMPTY));
+        if (++jp == ntp) {
+          ++kp;
+          jp = 0;
+          ntp = kp < k_end ? n_tiles(kp) : 0;
+        }
+        ++g_p;
+        progressed = true;
+      }
+      if (progressed) {
+        idle = 0;
+      } else if (++idle >= kSpinLimit) {
+        *abort_flag = 1;
+        raise_flag(p.err, DCP_DEVERR_TIMEOUT);
+        break;
+      } else if ((idle & 63u) == 0 && __any_sync(0xffffffffu, *abort_flag != 0)) {
+        break;
+      }
+    }
+    mma_commit(bar(BDRAIN));  // all issued MMAs complete before TMEM may be freed
+    drain_bar(bar(BDRAIN), 0);
+  } else {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int r = threadIdx.x;  // query row = TMEM lane
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const int js_row = r / p.g, h = r - js_row * p.g;  // token slot and head of the row
+    uint32_t gt = 0;
+    int n_items = 0;
+    bool ok = true;
+    for (int k = k_begin; k < k_end && ok; ++k) {
+      const ItemGeom g = item_geom(p, k);
+      const int nt = g.t1 - g.t0;
+      const int jt = g.tg * p.tpr + js_row;  // this row's query token
+      const bool active = jt < p.qlen;
+      // causal limit of the row's token (global positions); inactive rows attend nothing
+      const int hi_r = active ? min(g.hi, p.seq_lens[g.b] - (p.qlen - 1 - jt)) : g.lo;
+      const size_t qrow = ((size_t)g.b * p.qlen + (active ? jt : 0)) * p.Hq + (size_t)g.kvh * p.g + h;
+      // the row's query into TMEM (after the previous item's score MMAs)
+      if (n_items > 0 && !wait_warp(bar(BQ_EMPTY), (n_items - 1) & 1, abort_flag, p.err)) break;
+      tc_fence_after();
+      {
+        const uint4* qr = reinterpret_cast<const uint4*>(p.q + qrow * kD);
+        uint32_t qv[32];
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint4 v = active ? qr[8 * c + i] : make_uint4(0u, 0u, 0u, 0u);
+            qv[4 * i] = v.x;
+            qv[4 * i + 1] = v.y;
+            qv[4 * i + 2] = v.z;
+            qv[4 * i + 3] = v.w;
+          }
+          tmem_st32(tmem + lane_off + kColQ + 32 * c, qv);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      bar_arrive(bar(BQ_FULL));
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < nt; ++j) {
+        const uint32_t gi = gt + j, s = gi % kStages;
+        const int tstart = g.lo + kTile * (g.t0 + j);  // global position of the tile's first token
+        const int n_tile = min(kTile, g.hi - tstart);  // tokens of the range in the tile
+        const int n_valid = max(0, min(n_tile, hi_r - tstart));
+        // 1. scores of the tile
+        if (!wait_warp(bar(BS_FULL), gi & 1u, abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t sv[64];
+        __syncwarp();
+        tmem_ld32(tmem + lane_off + kColS, sv);
+        tmem_ld32(tmem + lane_off + kColS + 32, sv + 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        bar_arrive(bar(BS_EMPTY));
+        // 2. online softmax over the tile's tokens (log2 units), causal per row
+        float sc[64];
+        float mx;
+        if (n_valid == kTile) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) sc[i] = __uint_as_float(sv[i]) * p.sl2;
+          float m8[8];
+#pragma unroll
+          for (int j8 = 0; j8 < 8; ++j8)
+            m8[j8] = fmaxf(fmaxf(fmaxf(sc[8 * j8], sc[8 * j8 + 1]), fmaxf(sc[8 * j8 + 2], sc[8 * j8 + 3])),
+                           fmaxf(fmaxf(sc[8 * j8 + 4], sc[8 * j8 + 5]), fmaxf(sc[8 * j8 + 6], sc[8 * j8 + 7])));
+          mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        } else {
+          mx = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            sc[i] = i < n_valid ? __uint_as_float(sv[i]) * p.sl2 : -INFINITY;
+            mx = fmaxf(mx, sc[i]);
+          }
+        }
+        float m_new = m_run, alpha = 1.f;
+        bool rescale = false;
+        if (m_run == -INFINITY) {
+          m_new = mx;
+        } else if (mx > m_run + kRescaleThreshold) {
+          m_new = mx;
+          alpha = exp2f(m_run - m_new);
+          rescale = true;
+        }
+        const float ref = m_new == -INFINITY ? 0.f : m_new;
+        float lsum;
+        {
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            sc[i] = ex2_ftz(sc[i] - ref);  // masked entries: 2^-inf = 0
+            ls[i & 3] += sc[i];
+          }
+          lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        }
+        l_run = l_run * alpha + lsum;
+        m_run = m_new;
+        const bool any_lo = __any_sync(0xffffffffu, lsum > kLoFraction * l_run);
+        // 3. the P buffer and O are free once the previous tile's P.V has finished
+        if (gi >= 1 && !wait_warp(bar(BP_EMPTY), (gi - 1) & 1u, abort_flag, p.err)) { ok = false; break; }
+        {
+          const uint32_t hrow = sbase + kOffP + r * 128;
+          const uint32_t lrow = hrow + kPBytes;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t hi4[4], lo4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              hi4[e] = pack_bf16(sc[8 * c + 2 * e], sc[8 * c + 2 * e + 1]);
+              lo4[e] = residual_bf16(sc[8 * c + 2 * e], sc[8 * c + 2 * e + 1]);
+            }
+            st_shared_v4(hrow + (((uint32_t)c ^ (uint32_t)(r & 7)) << 4), hi4[0], hi4[1], hi4[2], hi4[3]);
+            st_shared_v4(lrow + (((uint32_t)c ^ (uint32_t)(r & 7)) << 4), lo4[0], lo4[1], lo4[2], lo4[3]);
+          }
+          if (lane == 0) lo_flags[warp] = any_lo ? 1 : 0;
+        }
+        // 4. value rows past the range's last token may hold anything: zero them
+        if (n_tile < kTile) {
+          const int zrows = kTile - n_tile;
+          const uint32_t vbase = sbase + kOffKv + s * kStageBytes + kKBytes;
+          for (int e = r; e < zrows * 16; e += kRows) {  // 16 pieces of 16 bytes per row (two halves)
+            const int row = n_tile + e / 16, c = (e >> 3) & 1, piece = e & 7;
+            st_shared_v4(vbase + c * kChunkBytes + row * 128 + piece * 16, 0u, 0u, 0u, 0u);
+          }
+        }
+        // 5. lazy rescale of O (warp-wide: TMEM access is per warp; the others multiply by 1)
+        if (__any_sync(0xffffffffu, rescale)) {
+          tc_fence_after();
+          uint32_t ov[32];
+          __syncwarp();
+#pragma unroll 1
+          for (int c = 0; c < kD / 32; ++c) {
+            tmem_ld32(tmem + lane_off + kColO + 32 * c, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st32(tmem + lane_off + kColO + 32 * c, ov);
+          }
+          tmem_wait_st();
+        }
+        // 6. publish P to the MMA issuer
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        tc_fence_before();
+        bar_arrive(bar(BP_FULL));
+      }
+      if (!ok) break;
+      // epilogue: wait for the last P.V, then write O / l and the LSE of the row
+      const uint32_t glast = gt + nt - 1;
+      if (!wait_warp(bar(BP_EMPTY), glast & 1u, abort_flag, p.err)) break;
+      tc_fence_after();
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      float* out = nullptr;
+      float* out_lse = nullptr;
+      if (g.out_row >= 0) {
+        const size_t row = (size_t)g.out_row * kRows + r;
+        out = reinterpret_cast<float*>(const_cast<char*>(p.ws) + p.L.tmp_o_off) + row * kD;
+        out_lse = reinterpret_cast<float*>(const_cast<char*>(p.ws) + p.L.tmp_lse_off) + row;
+      } else if (active) {
+        const size_t row = ((size_t)g.shard * (p.B / p.G) * p.qlen + (size_t)g.b * p.qlen + jt) * p.Hq +
+                           (size_t)g.kvh * p.g + h;
+        out = p.o_parts + row * kD;
+        out_lse = p.lses + row;
+      }
+      uint32_t ov[32];
+      __syncwarp();
+#pragma unroll 1
+      for (int c = 0; c < kD / 32; ++c) {
+        tmem_ld32(tmem + lane_off + kColO + 32 * c, ov);
+        tmem_wait_ld();
+        if (out) {
+          float4* o4 = reinterpret_cast<float4*>(out + 32 * c);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            o4[i] = make_float4(__uint_as_float(ov[4 * i]) * inv, __uint_as_float(ov[4 * i + 1]) * inv,
+                                __uint_as_float(ov[4 * i + 2]) * inv, __uint_as_float(ov[4 * i + 3]) * inv);
+        }
+      }
+      if (out_lse) *out_lse = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+      tc_fence_before();
+      gt += nt;
+      ++n_items;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 2-D bf16 map over the rows of a GQA pool ([blocks x Hkv x block_size] rows
+// of 128 columns); boxes of 64 columns (128 bytes, 128-byte swizzle) by
+// box_rows rows; out-of-range rows read 0.
+bool pool_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {kD, rows};
+  cuuint64_t strides[1] = {kD * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Resident CTAs (one per SM), cached per device.
+int tc_ctas_cached() {
+  static std::mutex mu;
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] > 0) return cache[dev];
+  if (cudaFuncSetAttribute(gqa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+    return 0;
+  int occ = 0, sms = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gqa_tc_kernel, kThreads, kSmemBytes) != cudaSuccess ||
+      occ <= 0)
+    return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  cache[dev] = occ * sms;
+  return cache[dev];
+}
+
+}  // namespace
+
+bool gqa_tc_eligible(const dcp_attn_desc& d, int qlen) {
+  if (d.kind != DCP_KIND_GQA || d.kv_dtype != DCP_KV_BF16) return false;
+  if (d.head_dim_k != kD || d.head_dim_v != kD) return false;
+  const int g = d.num_q_heads / d.num_kv_heads;
+  if (g < 1 || kRows % g != 0) return false;
+  if (!(d.block_size % kTile == 0 || kTile % d.block_size == 0)) return false;
+  return qlen * g >= kRows;  // the lanes' 128 rows are (nearly) full
+}
+
+int gqa_tc_rows_tokens(const dcp_attn_desc& d) { return kRows / (d.num_q_heads / d.num_kv_heads); }
+
+int gqa_tc_ctas(const dcp_attn_desc&, const DeviceInfo&) { return tc_ctas_cached(); }
+
+cudaError_t launch_gqa_tc(const dcp_attn_desc& d, const void* q, const ShardSet& sh, const RangeSpec& rs,
+                          float* o_parts, float* lses, void* ws, const WsLayout& L, int n_ctas, int32_t* err,
+                          cudaStream_t st) {
+  if (n_ctas <= 0 || tc_ctas_cached() <= 0) return cudaErrorNotSupported;
+  static_assert(sizeof(TcParams) <= 32000, "kernel parameters");
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  const int box = d.block_size < kTile ? d.block_size : kTile;
+  for (int i = 0; i < rs.N; ++i) {
+    const uint64_t rows = (uint64_t)sh.nblk[i] * d.num_kv_heads * d.block_size;
+    if (!pool_map(&p.tm_k[i], sh.k[i], rows, box) || !pool_map(&p.tm_v[i], sh.v[i], rows, box))
+      return cudaErrorNotSupported;
+  }
+  p.sh = sh;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.seq_lens = rs.seq_lens;
+  p.ws = static_cast<const char*>(ws);
+  p.L = L;
+  p.o_parts = o_parts;
+  p.lses = lses;
+  p.err = err;
+  p.B = rs.B;
+  p.qlen = rs.qlen;
+  p.tpr = rs.tpr;
+  p.G = (rs.qlen + rs.tpr - 1) / rs.tpr;
+  p.g = d.num_q_heads / d.num_kv_heads;
+  p.Hq = d.num_q_heads;
+  p.Hkv = d.num_kv_heads;
+  p.Bs = d.block_size;
+  p.box = box;
+  p.sl2 = d.scale * kLog2e;
+  gqa_tc_kernel<<<n_ctas, kThreads, kSmemBytes, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace dcp

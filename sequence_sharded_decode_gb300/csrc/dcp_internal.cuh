@@ -114,8 +114,16 @@ cudaError_t launch_mla(const dcp_attn_desc& d, const void* q, const ShardSet& sh
                        float* o_parts, float* lses, void* ws, const WsLayout& L, int n_ctas,
                        int32_t* err, cudaStream_t st);
 int mla_ctas(const dcp_attn_desc& d, const DeviceInfo& di);
-cudaError_t launch_combine(const dcp_attn_desc& d, const RangeSpec& rs, int n_lanes, const void* ws,
-                           const WsLayout& L, float* o_parts, float* lses, cudaStream_t st);
+// Many query rows per KV head (GQA, head dim 128, bf16 cache, q_len * g >= 128):
+// 128-row lanes of 128/g tokens x g heads on the tcgen05 tensor cores.
+bool gqa_tc_eligible(const dcp_attn_desc& d, int qlen);
+int gqa_tc_rows_tokens(const dcp_attn_desc& d);  // query tokens per lane: 128 / g
+int gqa_tc_ctas(const dcp_attn_desc& d, const DeviceInfo& di);
+cudaError_t launch_gqa_tc(const dcp_attn_desc& d, const void* q, const ShardSet& sh, const RangeSpec& rs,
+                          float* o_parts, float* lses, void* ws, const WsLayout& L, int n_ctas, int32_t* err,
+                          cudaStream_t st);
+cudaError_t launch_combine(const dcp_attn_desc& d, const LaneGeom& lg, const RangeSpec& rs, int n_lanes,
+                           const void* ws, const WsLayout& L, float* o_parts, float* lses, cudaStream_t st);
 cudaError_t launch_merge(const float* o_parts, const float* lses, int N, int rows, int dv, float* o,
                          float* lse_out, cudaStream_t st);
 cudaError_t launch_append(const dcp_attn_desc& d, const ShardSet& sh, int N, const int32_t* starts,

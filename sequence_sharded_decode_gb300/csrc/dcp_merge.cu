@@ -165,10 +165,9 @@ cudaError_t launch_merge(const float* o_parts, const float* lses, int N, int row
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const dcp_attn_desc& d, const RangeSpec& rs, int n_lanes, const void* ws,
-                           const WsLayout& L, float* o_parts, float* lses, cudaStream_t st) {
+cudaError_t launch_combine(const dcp_attn_desc& d, const LaneGeom& lg, const RangeSpec& rs, int n_lanes,
+                           const void* ws, const WsLayout& L, float* o_parts, float* lses, cudaStream_t st) {
   if (n_lanes <= 0) return cudaSuccess;
-  const LaneGeom lg = lane_geom(d);
   CombineGeom cg;
   cg.Hq = d.num_q_heads;
   cg.dv = d.head_dim_v;

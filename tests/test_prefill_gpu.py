@@ -26,3 +26,29 @@ def test_prefill_chunk_matches_oracle(name, chunk, over):
     st = DecodeState(wl, q_len=chunk)
     st.step()
     _check(st, wl, chunk)
+
+
+# Steps with q_len * g >= 128 query rows per KV head (GQA, head dim 128)
+# take the tcgen05 kernel: lanes of 128 rows = 128/g tokens x g heads.
+TC_CASES = [
+    ("gqa_mid", 8, dict(batch=2, ctx_fixed=700, shards=2)),                             # g=16: 8 tokens per lane
+    ("gqa_mid", 20, dict(batch=2, ctx_fixed=1000, shards=3)),                           # a partial last token group
+    ("gqa_mid", 64, dict(batch=3, ctx_kind="lognormal", median=600, sigma=1.0, ctx_lo=0, ctx_hi=3000, shards=4)),
+    ("gqa_mid", 4, dict(batch=2, q_heads=64, kv_heads=2, ctx_fixed=900, shards=3)),     # g=32: 4 tokens per lane
+    ("gqa_mid", 16, dict(batch=2, q_heads=32, kv_heads=4, ctx_fixed=500, shards=2)),    # g=8
+    ("gqa_mid", 128, dict(batch=1, q_heads=8, kv_heads=8, ctx_fixed=300, shards=3)),    # g=1: 128 tokens per lane
+    ("gqa_mid", 32, dict(batch=2, ctx_fixed=800, shards=2, block_size=32)),
+    ("gqa_mid", 32, dict(batch=2, ctx_fixed=800, shards=2, block_size=64)),
+    ("gqa_mid", 32, dict(batch=2, ctx_fixed=900, shards=2, block_size=128)),
+    ("gqa_mid", 16, dict(batch=2, ctx_fixed=1500, shards=4, needles=3)),
+    ("gqa_mid", 24, dict(batch=2, ctx_fixed=1200, shards=3, scale=1.0)),                # peaky softmax
+    ("gqa_mid", 40, dict(batch=2, ctx_fixed=0, shards=2)),                              # the first chunk only
+]
+
+
+@pytest.mark.parametrize("name,chunk,over", TC_CASES)
+def test_tc_rows_match_oracle(name, chunk, over):
+    wl = configs.get(name).with_(**over)
+    st = DecodeState(wl, q_len=chunk)
+    st.step()
+    _check(st, wl, chunk)

@@ -60,14 +60,14 @@ constexpr int kPBytes = kRows * 128;       // 128 rows x 64 tokens bf16 (one ter
 constexpr int kOffKv = 0;
 constexpr int kOffP = kOffKv + kStages * kStageBytes;  // hi at kOffP, lo at kOffP + kPBytes
 constexpr int kOffBar = kOffP + 2 * kPBytes;
-constexpr int kNumBars = 16;
+constexpr int kNumBars = 18;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag, lo flags
-constexpr int kSmemUsed = kOffMisc + 32;
+constexpr int kSmemUsed = kOffMisc + 64;  // TMEM slot, abort flag, 4 lo flags, 2 x 4 votes
 constexpr int kSmemBytes = kSmemUsed + 1024;      // slack to align the base to 1024
 
 constexpr int BQ_FULL = 0, BQ_EMPTY = 1, BS_FULL = 2, BS_EMPTY = 3, BP_FULL = 4, BP_EMPTY = 5, BDRAIN = 6,
-              BKV_FULL = 7, BKV_EMPTY = 7 + kStages;
-static_assert(BKV_EMPTY + kStages <= kNumBars, "barrier slots");
+              BKV_FULL = 7, BKV_EMPTY = 7 + kStages, BVOTE = 7 + 2 * kStages /* 2, by tile parity */;
+static_assert(BVOTE + 2 <= kNumBars, "barrier slots");
 
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColO = 0;    // 128 columns: O, fp32
@@ -269,6 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_tc_kernel(const __grid_consta
       bar_init(bar(BKV_FULL + s), 1);
       bar_init(bar(BKV_EMPTY + s), 1);
     }
+    bar_init(bar(BVOTE), 4);      // one arrival per softmax warp
+    bar_init(bar(BVOTE + 1), 4);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
@@ -476,24 +478,37 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_tc_kernel(const __grid_consta
         tmem_wait_ld();
         tc_fence_before();
         bar_arrive(bar(BS_EMPTY));
-        // 2. online softmax over the tile's tokens (log2 units), causal per row
+        // 2. online softmax over the tile's tokens (log2 units), causal per row.
+        //    The scale is applied inside the exponent (one FMA per score):
+        //    the row max of the scaled scores is sl2 times the raw max (or
+        //    the raw min for a negative scale).
         float sc[64];
         float mx;
         if (n_valid == kTile) {
 #pragma unroll
-          for (int i = 0; i < 64; ++i) sc[i] = __uint_as_float(sv[i]) * p.sl2;
+          for (int i = 0; i < 64; ++i) sc[i] = __uint_as_float(sv[i]);
           float m8[8];
+          if (p.sl2 >= 0.f) {
 #pragma unroll
-          for (int j8 = 0; j8 < 8; ++j8)
-            m8[j8] = fmaxf(fmaxf(fmaxf(sc[8 * j8], sc[8 * j8 + 1]), fmaxf(sc[8 * j8 + 2], sc[8 * j8 + 3])),
-                           fmaxf(fmaxf(sc[8 * j8 + 4], sc[8 * j8 + 5]), fmaxf(sc[8 * j8 + 6], sc[8 * j8 + 7])));
-          mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            for (int j8 = 0; j8 < 8; ++j8)
+              m8[j8] = fmaxf(fmaxf(fmaxf(sc[8 * j8], sc[8 * j8 + 1]), fmaxf(sc[8 * j8 + 2], sc[8 * j8 + 3])),
+                             fmaxf(fmaxf(sc[8 * j8 + 4], sc[8 * j8 + 5]), fmaxf(sc[8 * j8 + 6], sc[8 * j8 + 7])));
+            mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+          } else {
+#pragma unroll
+            for (int j8 = 0; j8 < 8; ++j8)
+              m8[j8] = fminf(fminf(fminf(sc[8 * j8], sc[8 * j8 + 1]), fminf(sc[8 * j8 + 2], sc[8 * j8 + 3])),
+                             fminf(fminf(sc[8 * j8 + 4], sc[8 * j8 + 5]), fminf(sc[8 * j8 + 6], sc[8 * j8 + 7])));
+            mx = fminf(fminf(fminf(m8[0], m8[1]), fminf(m8[2], m8[3])), fminf(fminf(m8[4], m8[5]), fminf(m8[6], m8[7])));
+          }
+          mx *= p.sl2;
         } else {
+          // a partial tile: masked scores become -inf after the scaling
           mx = -INFINITY;
 #pragma unroll
           for (int i = 0; i < 64; ++i) {
-            sc[i] = i < n_valid ? __uint_as_float(sv[i]) * p.sl2 : -INFINITY;
-            mx = fmaxf(mx, sc[i]);
+            sc[i] = i < n_valid ? __uint_as_float(sv[i]) : 0.f;
+            mx = fmaxf(mx, i < n_valid ? sc[i] * p.sl2 : -INFINITY);
           }
         }
         float m_new = m_run, alpha = 1.f;
@@ -509,16 +524,37 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_tc_kernel(const __grid_consta
         float lsum;
         {
           float ls[4] = {0.f, 0.f, 0.f, 0.f};
+          if (n_valid == kTile) {
 #pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            sc[i] = ex2_ftz(sc[i] - ref);  // masked entries: 2^-inf = 0
-            ls[i & 3] += sc[i];
+            for (int i = 0; i < 64; ++i) {
+              sc[i] = ex2_ftz(fmaf(sc[i], p.sl2, -ref));
+              ls[i & 3] += sc[i];
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+              sc[i] = i < n_valid ? ex2_ftz(fmaf(sc[i], p.sl2, -ref)) : 0.f;
+              ls[i & 3] += sc[i];
+            }
           }
           lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
         }
         l_run = l_run * alpha + lsum;
         m_run = m_new;
-        const bool any_lo = __any_sync(0xffffffffu, lsum > kLoFraction * l_run);
+        // The residual P_lo matters only where this tile carries more than
+        // kLoFraction of some row's weight; the four softmax warps vote (the
+        // P.V covers all 128 rows, so the residual is formed for all or none).
+        bool any_lo;
+        {
+          const bool warp_lo = __any_sync(0xffffffffu, lsum > kLoFraction * l_run);
+          volatile int* vote = lo_flags + 4 + 4 * (gi & 1u);  // double-buffered by tile parity
+          if (lane == 0) {
+            vote[warp] = warp_lo ? 1 : 0;
+            bar_arrive(bar(BVOTE + (gi & 1u)));
+          }
+          if (!wait_warp(bar(BVOTE + (gi & 1u)), (gi >> 1) & 1u, abort_flag, p.err)) { ok = false; break; }
+          any_lo = (vote[0] | vote[1] | vote[2] | vote[3]) != 0;
+        }
         // 3. the P buffer and O are free once the previous tile's P.V has finished
         if (gi >= 1 && !wait_warp(bar(BP_EMPTY), (gi - 1) & 1u, abort_flag, p.err)) { ok = false; break; }
         {
@@ -526,14 +562,19 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_tc_kernel(const __grid_consta
           const uint32_t lrow = hrow + kPBytes;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            uint32_t hi4[4], lo4[4];
+            uint32_t hi4[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              hi4[e] = pack_bf16(sc[8 * c + 2 * e], sc[8 * c + 2 * e + 1]);
-              lo4[e] = residual_bf16(sc[8 * c + 2 * e], sc[8 * c + 2 * e + 1]);
-            }
+            for (int e = 0; e < 4; ++e) hi4[e] = pack_bf16(sc[8 * c + 2 * e], sc[8 * c + 2 * e + 1]);
             st_shared_v4(hrow + (((uint32_t)c ^ (uint32_t)(r & 7)) << 4), hi4[0], hi4[1], hi4[2], hi4[3]);
-            st_shared_v4(lrow + (((uint32_t)c ^ (uint32_t)(r & 7)) << 4), lo4[0], lo4[1], lo4[2], lo4[3]);
+          }
+          if (any_lo) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              uint32_t lo4[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) lo4[e] = residual_bf16(sc[8 * c + 2 * e], sc[8 * c + 2 * e + 1]);
+              st_shared_v4(lrow + (((uint32_t)c ^ (uint32_t)(r & 7)) << 4), lo4[0], lo4[1], lo4[2], lo4[3]);
+            }
           }
           if (lane == 0) lo_flags[warp] = any_lo ? 1 : 0;
         }

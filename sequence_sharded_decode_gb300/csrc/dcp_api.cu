@@ -85,11 +85,13 @@ struct Path {
   int tc;             // the tcgen05 GQA kernel
   int tpr;            // query tokens per row group
   int rows_per_lane;  // query rows of one lane
+  int qlen;           // query tokens per sequence of the step
 };
 static Path path_for(const dcp_attn_desc& d, int q_len) {
   Path p;
   p.lg = lane_geom(d);
   p.tc = 0;
+  p.qlen = q_len;
   if (d.kind == DCP_KIND_MLA) {
     p.tpr = 1;
     p.rows_per_lane = d.num_q_heads;
@@ -98,8 +100,8 @@ static Path path_for(const dcp_attn_desc& d, int q_len) {
   const int grp = d.num_q_heads / d.num_kv_heads;
   if (gqa_tc_eligible(d, q_len)) {
     p.tc = 1;
-    p.tpr = gqa_tc_rows_tokens(d);
-    p.rows_per_lane = 128;
+    p.tpr = gqa_tc_rows_tokens(d, q_len);
+    p.rows_per_lane = p.tpr * grp;
     p.lg.heads_per_lane = grp;
     p.lg.groups = 1;
     p.lg.lanes_per_unit = d.num_kv_heads;
@@ -160,7 +162,7 @@ static int check_shards(const dcp_attn_desc& d, const dcp_shard* s, int N, Shard
 
 static int work_ctas(const dcp_attn_desc& d, const DeviceInfo& di, const Path& p) {
   if (d.kind == DCP_KIND_MLA) return mla_ctas(d, di);
-  return p.tc ? gqa_tc_ctas(d, di) : gqa_ctas(d, di, p.tpr);
+  return p.tc ? gqa_tc_ctas(d, di, p.qlen) : gqa_ctas(d, di, p.tpr);
 }
 
 // Workspace layout for B row groups per shard (sequences x token groups).

@@ -12,9 +12,12 @@
 // at position seq_len - q_len + j and attends every token at or before it.
 //
 // Layout of the work: a lane is (shard, sequence, token group, KV head); its
-// 128 query rows are the 128/g tokens of the group times the g query heads of
-// the KV head (row r = token slot r / g, head r % g). Per 64-token tile of the
-// lane's range:
+// NB x 128 query rows are the NB*128/g tokens of the group times the g query
+// heads of the KV head (row r = token slot r / g, head r % g), taken as NB
+// blocks of 128 rows that share every K/V tile (NB = 2 once a step has 256
+// rows per KV head: two groups of four softmax warps then work on the two
+// blocks in turn while the tensor cores serve the other). Per 64-token tile
+// of the lane's range, for each block:
 //   1. S = Q . K^T (M=128 rows, N=64 tokens, K=128) into TMEM, the queries
 //      being the MMA's A operand in TMEM
 //   2. online softmax per row (thread r owns TMEM lane r), causal at the
@@ -31,7 +34,7 @@
 // min(block_size, 64) rows x 64 columns, 128-byte swizzle) into a 4-stage
 // ring. One warp schedules the MMAs (non-blocking barrier polls, uniform
 // control flow, one elect.sync-chosen lane issues); one warp copies; four
-// warps run the softmax and the epilogue. Every barrier's phases are
+// warps per block run the softmax and the epilogue. Every barrier's phases are
 // observed in order and never more than one phase late; every wait is
 // bounded: on expiry the kernel raises DCP_DEVERR_TIMEOUT, stops all roles,
 // drains what it issued and frees TMEM.
@@ -47,38 +50,43 @@
 namespace dcp {
 namespace {
 
-constexpr int kRows = 128;                 // query rows of a lane (MMA M)
+constexpr int kRows = 128;                 // query rows of a block (MMA M)
 constexpr int kD = 128;                    // head dim (K and V)
 constexpr int kTile = 64;                  // tokens per tile (MMA N of S, K of P.V)
 constexpr int kStages = 4;
-constexpr int kThreads = 192;              // 4 softmax warps, copy warp, MMA warp
 constexpr int kChunkBytes = kTile * 128;   // 64 rows x 64 bf16 (one 128-byte-swizzled box column)
 constexpr int kKBytes = 2 * kChunkBytes;   // K rows of a tile: dims 0-63 | 64-127
 constexpr int kStageBytes = 2 * kKBytes;   // K then V
 constexpr int kPBytes = kRows * 128;       // 128 rows x 64 tokens bf16 (one term)
-
-constexpr int kOffKv = 0;
-constexpr int kOffP = kOffKv + kStages * kStageBytes;  // hi at kOffP, lo at kOffP + kPBytes
-constexpr int kOffBar = kOffP + 2 * kPBytes;
-constexpr int kNumBars = 18;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag, lo flags
-constexpr int kSmemUsed = kOffMisc + 64;  // TMEM slot, abort flag, 4 lo flags, 2 x 4 votes
-constexpr int kSmemBytes = kSmemUsed + 1024;      // slack to align the base to 1024
-
-constexpr int BQ_FULL = 0, BQ_EMPTY = 1, BS_FULL = 2, BS_EMPTY = 3, BP_FULL = 4, BP_EMPTY = 5, BDRAIN = 6,
-              BKV_FULL = 7, BKV_EMPTY = 7 + kStages, BVOTE = 7 + 2 * kStages /* 2, by tile parity */;
-static_assert(BVOTE + 2 <= kNumBars, "barrier slots");
-
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColO = 0;    // 128 columns: O, fp32
-constexpr uint32_t kColS = 128;  // 64 columns: S, fp32
-constexpr uint32_t kColQ = 192;  // 64 columns: Q, bf16 pairs
 constexpr uint32_t kSpinLimit = 1u << 24;
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr float kLoFraction = 1.0f / 32.0f;  // tile share of the row sum above which P_lo . V is issued
+
+// Barriers: shared ones, then seven per block.
+constexpr int BQ_EMPTY = 0, BDRAIN = 1, BKV_FULL = 2, BKV_EMPTY = 2 + kStages, BBLK = 2 + 2 * kStages;
+constexpr int B_QF = 0, B_SF = 1, B_SE = 2, B_PF = 3, B_PE = 4, B_V0 = 5 /* 2, by tile parity */, kBlkBars = 7;
+
+template <int NB>
+struct TcCfg {
+  static constexpr int kSoftmaxWarps = 4 * NB;
+  static constexpr int kThreads = 32 * (kSoftmaxWarps + 2);  // + copy warp + MMA warp
+  static constexpr int kCopyWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1;
+  static constexpr int kOffKv = 0;
+  static constexpr int kOffP = kOffKv + kStages * kStageBytes;  // block b: hi at kOffP + 2b kPBytes, lo after it
+  static constexpr int kNumBars = BBLK + kBlkBars * NB;
+  static constexpr int kOffBar = kOffP + 2 * NB * kPBytes;
+  static constexpr int kOffMisc = kOffBar + 8 * kNumBars;         // TMEM slot, abort flag, per block: 4 lo flags + 2 x 4 votes
+  static constexpr int kSmemUsed = kOffMisc + 16 + NB * 48;
+  static constexpr int kSmemBytes = kSmemUsed + 1024;              // slack to align the base to 1024
+  // TMEM: O of block b at 128 b, S at 128 NB + 64 b, Q at 192 NB + 64 b
+  static constexpr uint32_t kTmemCols = 256 * NB;
+  __host__ __device__ static constexpr uint32_t col_o(int b) { return 128u * b; }
+  __host__ __device__ static constexpr uint32_t col_s(int b) { return 128u * NB + 64u * b; }
+  __host__ __device__ static constexpr uint32_t col_q(int b) { return 192u * NB + 64u * b; }
+};
 
 struct TcParams {
   CUtensorMap tm_k[kMaxShards];
@@ -94,7 +102,7 @@ struct TcParams {
   int B;      // row groups per shard: sequences x token groups
   int qlen;   // query tokens per sequence
   int G;      // token groups per sequence
-  int tpr;    // query tokens per lane (128 / g)
+  int tpr;    // query tokens per lane (NB * 128 / g)
   int g;      // query heads per KV head
   int Hq, Hkv, Bs;
   int box;    // rows of a copy box: min(block_size, 64)
@@ -246,37 +254,43 @@ __device__ __forceinline__ ItemGeom item_geom(const TcParams& p, int k) {
   return g;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) gqa_tc_kernel(const __grid_constant__ TcParams p) {
+template <int NB>
+__global__ void __launch_bounds__(TcCfg<NB>::kThreads, 1) gqa_tc_kernel(const __grid_constant__ TcParams p) {
+  using C = TcCfg<NB>;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = saddr(smem_raw);
   unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   const uint32_t sbase = saddr(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  auto bar = [&](int i) { return sbase + kOffBar + 8u * i; };
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 8);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  volatile int* lo_flags = reinterpret_cast<volatile int*>(smem + kOffMisc + 16);  // one per softmax warp
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
+  auto bbar = [&](int blk, int i) { return sbase + C::kOffBar + 8u * (BBLK + kBlkBars * blk + i); };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  // per block: lo flags [4] (read by the MMA warp), then votes [2][4]
+  auto lo_flags = [&](int blk) { return reinterpret_cast<volatile int*>(smem + C::kOffMisc + 16 + 48 * blk); };
 
   if (threadIdx.x == 0) {
-    bar_init(bar(BQ_FULL), kRows);  // every softmax thread wrote its query row into TMEM
     bar_init(bar(BQ_EMPTY), 1);
-    bar_init(bar(BS_FULL), 1);
-    bar_init(bar(BS_EMPTY), kRows);
-    bar_init(bar(BP_FULL), kRows);
-    bar_init(bar(BP_EMPTY), 1);
     bar_init(bar(BDRAIN), 1);
     for (int s = 0; s < kStages; ++s) {
       bar_init(bar(BKV_FULL + s), 1);
       bar_init(bar(BKV_EMPTY + s), 1);
     }
-    bar_init(bar(BVOTE), 4);      // one arrival per softmax warp
-    bar_init(bar(BVOTE + 1), 4);
+    for (int blk = 0; blk < NB; ++blk) {
+      bar_init(bbar(blk, B_QF), kRows);  // every softmax thread of the block wrote its query row
+      bar_init(bbar(blk, B_SF), 1);
+      bar_init(bbar(blk, B_SE), kRows);
+      bar_init(bbar(blk, B_PF), kRows);
+      bar_init(bbar(blk, B_PE), 1);
+      bar_init(bbar(blk, B_V0), 4);      // one arrival per softmax warp of the block
+      bar_init(bbar(blk, B_V0 + 1), 4);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
-  if (warp == 5) {
+  if (warp == C::kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(saddr(tmem_slot)),
-                 "r"(kTmemCols));
+                 "r"(C::kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
   }
   tc_fence_before();
@@ -288,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_tc_kernel(const __grid_consta
   const int k_begin = cta_begin[blockIdx.x], k_end = cta_begin[blockIdx.x + 1];
   const int pieces = kTile / p.box;  // copy boxes per tile (1, 2 or 4)
 
-  if (warp == 4) {
+  if (warp == C::kCopyWarp) {
     // ------------------------------------------------------------ copy
     // Lane i < pieces looks up the block of piece i of the tile; lane 0
     // issues the boxes (K and V, two 64-column halves each).
@@ -327,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_tc_kernel(const __grid_consta
         }
         if (lane == 0 && ok) {
           const uint32_t s = fills % kStages;
-          const uint32_t st = sbase + kOffKv + s * kStageBytes;
+          const uint32_t st = sbase + C::kOffKv + s * kStageBytes;
           bar_arrive_tx(bar(BKV_FULL + s), kStageBytes);  // pieces x box rows x (2 + 2) x 128 B
           for (int i = 0; i < pieces; ++i) {
             const uint32_t dst = st + i * p.box * 128;
@@ -345,71 +359,119 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_tc_kernel(const __grid_consta
       const uint32_t f0 = fills > (uint32_t)kStages ? fills - kStages : 0;
       for (uint32_t f = f0; f < fills; ++f) drain_bar(bar(BKV_FULL + f % kStages), (f / kStages) & 1u);
     }
-  } else if (warp == 5) {
+  } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
+    // Per block: the score MMA of its next tile and the P.V of its oldest
+    // tile whose P is ready go out as soon as their inputs are. A K/V stage
+    // is released once every block's P.V of the tile has been issued.
     const uint32_t id_s = idesc(kRows, kTile, 0);
     const uint32_t id_pv = idesc(kRows, kD, 1);
-    const uint64_t pdesc0 = sdesc(sbase + kOffP, 0);
     auto n_tiles = [&](int k) {
       const ItemRec it = reinterpret_cast<const ItemRec*>(p.ws + p.L.items_off)[k];
       return it.t1 - it.t0;
     };
-    int ks = k_begin, js = 0, nts = ks < k_end ? n_tiles(ks) : 0;  // next score tile
-    int kp = k_begin, jp = 0, ntp = nts;                            // next P.V tile
-    uint32_t g_s = 0, g_p = 0, q_loads = 0;
+    int ks[NB], js[NB], nts[NB], kp[NB], jp[NB], ntp[NB];
+    uint32_t gs[NB], gp[NB];
+    const int nt0 = k_begin < k_end ? n_tiles(k_begin) : 0;
+#pragma unroll
+    for (int blk = 0; blk < NB; ++blk) {
+      ks[blk] = kp[blk] = k_begin;
+      js[blk] = jp[blk] = 0;
+      nts[blk] = ntp[blk] = nt0;
+      gs[blk] = gp[blk] = 0;
+    }
+    uint32_t q_loads = 0, released = 0;  // items whose queries were taken; tiles whose stage was released
     bool q_ready = false;
+    int s_done_items = 0;                // items whose last score MMAs all blocks issued
     uint32_t idle = 0;
-    while (kp < k_end) {
+    auto pv_left = [&]() {
+      bool left = false;
+#pragma unroll
+      for (int blk = 0; blk < NB; ++blk) left |= kp[blk] < k_end;
+      return left;
+    };
+    while (pv_left()) {
       bool progressed = false;
-      if (ks < k_end) {
-        if (!q_ready && bar_test_warp(bar(BQ_FULL), q_loads & 1u)) {
+      // queries of the next item (all blocks)
+      if (!q_ready && (int)q_loads < k_end - k_begin) {
+        bool all = true;
+#pragma unroll
+        for (int blk = 0; blk < NB; ++blk) all = all && bar_test_warp(bbar(blk, B_QF), q_loads & 1u);
+        if (all) {
           q_ready = true;
           tc_fence_after();
         }
-        const uint32_t s = g_s % kStages;
-        if (q_ready && bar_test_warp(bar(BKV_FULL + s), (g_s / kStages) & 1u) &&
-            (g_s == 0 || bar_test_warp(bar(BS_EMPTY), (g_s - 1) & 1u))) {
-          tc_fence_after();
-          const uint64_t kd = sdesc(sbase + kOffKv + s * kStageBytes, 0);
+      }
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk)
-            mma_ts(tmem + kColS, tmem + kColQ + 8 * kk,
-                   kd + (uint64_t)((((kk >> 2) * kChunkBytes) + 32 * (kk & 3)) >> 4), id_s, kk > 0);
-          mma_commit(bar(BS_FULL));
-          if (++js == nts) {  // last score tile of the item: its queries may be replaced
-            mma_commit(bar(BQ_EMPTY));
-            ++ks;
-            js = 0;
-            nts = ks < k_end ? n_tiles(ks) : 0;
-            ++q_loads;
-            q_ready = false;
+      for (int blk = 0; blk < NB; ++blk) {
+        // scores of this block's next tile (the item whose queries are loaded)
+        if (q_ready && ks[blk] < k_end && ks[blk] - k_begin == (int)q_loads) {
+          const uint32_t g = gs[blk], s = g % kStages;
+          if (bar_test_warp(bar(BKV_FULL + s), (g / kStages) & 1u) &&
+              (g == 0 || bar_test_warp(bbar(blk, B_SE), (g - 1) & 1u))) {
+            tc_fence_after();
+            const uint64_t kd = sdesc(sbase + C::kOffKv + s * kStageBytes, 0);
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk)
+              mma_ts(tmem + C::col_s(blk), tmem + C::col_q(blk) + 8 * kk,
+                     kd + (uint64_t)((((kk >> 2) * kChunkBytes) + 32 * (kk & 3)) >> 4), id_s, kk > 0);
+            mma_commit(bbar(blk, B_SF));
+            if (++js[blk] == nts[blk]) {
+              ++ks[blk];
+              js[blk] = 0;
+              nts[blk] = ks[blk] < k_end ? n_tiles(ks[blk]) : 0;
+            }
+            ++gs[blk];
+            progressed = true;
           }
-          ++g_s;
+        }
+        // P.V of this block's oldest tile whose P is ready
+        if (gp[blk] < gs[blk] && bar_test_warp(bbar(blk, B_PF), gp[blk] & 1u)) {
+          tc_fence_after();
+          const uint32_t s = gp[blk] % kStages;
+          const uint64_t vd = sdesc(sbase + C::kOffKv + s * kStageBytes + kKBytes, kChunkBytes);
+          const uint64_t pd = sdesc(sbase + C::kOffP + 2 * blk * kPBytes, 0);
+          volatile int* lf = lo_flags(blk);
+          const int terms = (lf[0] | lf[1] | lf[2] | lf[3]) ? 2 : 1;
+#pragma unroll
+          for (int term = 0; term < 2; ++term) {
+            if (term >= terms) break;
+#pragma unroll
+            for (int kt = 0; kt < kTile / 16; ++kt)
+              mma_ss(tmem + C::col_o(blk), pd + (uint64_t)((term * kPBytes + 32 * kt) >> 4),
+                     vd + (uint64_t)((2048 * kt) >> 4), id_pv, (jp[blk] == 0 && term == 0 && kt == 0) ? 0 : 1);
+          }
+          mma_commit(bbar(blk, B_PE));
+          if (++jp[blk] == ntp[blk]) {
+            ++kp[blk];
+            jp[blk] = 0;
+            ntp[blk] = kp[blk] < k_end ? n_tiles(kp[blk]) : 0;
+          }
+          ++gp[blk];
           progressed = true;
         }
       }
-      if (g_p < g_s && bar_test_warp(bar(BP_FULL), g_p & 1u)) {
-        tc_fence_after();
-        const uint32_t s = g_p % kStages;
-        const uint64_t vd = sdesc(sbase + kOffKv + s * kStageBytes + kKBytes, kChunkBytes);
-        const int terms = (lo_flags[0] | lo_flags[1] | lo_flags[2] | lo_flags[3]) ? 2 : 1;
+      // a stage is free once every block's P.V of its tile was issued
+      {
+        uint32_t gmin = gp[0];
 #pragma unroll
-        for (int term = 0; term < 2; ++term) {
-          if (term >= terms) break;
+        for (int blk = 1; blk < NB; ++blk) gmin = gp[blk] < gmin ? gp[blk] : gmin;
+        while (released < gmin) {
+          mma_commit(bar(BKV_EMPTY + released % kStages));
+          ++released;
+        }
+      }
+      // the queries of an item may be replaced once every block issued its last score MMA
+      if (q_ready) {
+        bool all = true;
 #pragma unroll
-          for (int kt = 0; kt < kTile / 16; ++kt)
-            mma_ss(tmem + kColO, pdesc0 + (uint64_t)((term * kPBytes + 32 * kt) >> 4),
-                   vd + (uint64_t)((2048 * kt) >> 4), id_pv, (jp == 0 && term == 0 && kt == 0) ? 0 : 1);
+        for (int blk = 0; blk < NB; ++blk) all = all && (ks[blk] - k_begin > (int)q_loads);
+        if (all) {
+          mma_commit(bar(BQ_EMPTY));
+          ++q_loads;
+          ++s_done_items;
+          q_ready = false;
         }
-        mma_commit(bar(BKV_EMPTY + s));
-        mma_commit(bar(BP_EMPTY));
-        if (++jp == ntp) {
-          ++kp;
-          jp = 0;
-          ntp = kp < k_end ? n_tiles(kp) : 0;
-        }
-        ++g_p;
-        progressed = true;
       }
       if (progressed) {
         idle = 0;
@@ -421,13 +483,20 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_tc_kernel(const __grid_consta
         break;
       }
     }
+    (void)s_done_items;
     mma_commit(bar(BDRAIN));  // all issued MMAs complete before TMEM may be freed
     drain_bar(bar(BDRAIN), 0);
   } else {
     // ------------------------------------------------------------ softmax / epilogue
-    const int r = threadIdx.x;  // query row = TMEM lane
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const int js_row = r / p.g, h = r - js_row * p.g;  // token slot and head of the row
+    const int blk = warp >> 2;                  // the block this warp serves
+    const int wq = warp & 3;                    // its TMEM lane quarter
+    const int r = wq * 32 + lane;               // row of the block = TMEM lane
+    const int rl = blk * kRows + r;             // row of the lane
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t col_o = C::col_o(blk), col_s = C::col_s(blk), col_q = C::col_q(blk);
+    const uint32_t poff = sbase + C::kOffP + 2 * blk * kPBytes;
+    volatile int* lf = lo_flags(blk);
+    const int js_row = rl / p.g, h = rl - js_row * p.g;  // token slot and head of the row
     uint32_t gt = 0;
     int n_items = 0;
     bool ok = true;
@@ -456,12 +525,12 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_tc_kernel(const __grid_consta
             qv[4 * i + 2] = v.z;
             qv[4 * i + 3] = v.w;
           }
-          tmem_st32(tmem + lane_off + kColQ + 32 * c, qv);
+          tmem_st32(tmem + lane_off + col_q + 32 * c, qv);
         }
         tmem_wait_st();
       }
       tc_fence_before();
-      bar_arrive(bar(BQ_FULL));
+      bar_arrive(bbar(blk, B_QF));
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < nt; ++j) {
         const uint32_t gi = gt + j, s = gi % kStages;
@@ -469,15 +538,15 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_tc_kernel(const __grid_consta
         const int n_tile = min(kTile, g.hi - tstart);  // tokens of the range in the tile
         const int n_valid = max(0, min(n_tile, hi_r - tstart));
         // 1. scores of the tile
-        if (!wait_warp(bar(BS_FULL), gi & 1u, abort_flag, p.err)) { ok = false; break; }
+        if (!wait_warp(bbar(blk, B_SF), gi & 1u, abort_flag, p.err)) { ok = false; break; }
         tc_fence_after();
         uint32_t sv[64];
         __syncwarp();
-        tmem_ld32(tmem + lane_off + kColS, sv);
-        tmem_ld32(tmem + lane_off + kColS + 32, sv + 32);
+        tmem_ld32(tmem + lane_off + col_s, sv);
+        tmem_ld32(tmem + lane_off + col_s + 32, sv + 32);
         tmem_wait_ld();
         tc_fence_before();
-        bar_arrive(bar(BS_EMPTY));
+        bar_arrive(bbar(blk, B_SE));
         // 2. online softmax over the tile's tokens (log2 units), causal per row.
         //    The scale is applied inside the exponent (one FMA per score):
         //    the row max of the scaled scores is sl2 times the raw max (or
@@ -542,23 +611,23 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_tc_kernel(const __grid_consta
         l_run = l_run * alpha + lsum;
         m_run = m_new;
         // The residual P_lo matters only where this tile carries more than
-        // kLoFraction of some row's weight; the four softmax warps vote (the
-        // P.V covers all 128 rows, so the residual is formed for all or none).
+        // kLoFraction of some row's weight; the block's four softmax warps vote
+        // (its P.V covers all 128 rows, so the residual is formed for all or none).
         bool any_lo;
         {
           const bool warp_lo = __any_sync(0xffffffffu, lsum > kLoFraction * l_run);
-          volatile int* vote = lo_flags + 4 + 4 * (gi & 1u);  // double-buffered by tile parity
+          volatile int* vote = lf + 4 + 4 * (gi & 1u);  // double-buffered by tile parity
           if (lane == 0) {
-            vote[warp] = warp_lo ? 1 : 0;
-            bar_arrive(bar(BVOTE + (gi & 1u)));
+            vote[wq] = warp_lo ? 1 : 0;
+            bar_arrive(bbar(blk, B_V0 + (gi & 1u)));
           }
-          if (!wait_warp(bar(BVOTE + (gi & 1u)), (gi >> 1) & 1u, abort_flag, p.err)) { ok = false; break; }
+          if (!wait_warp(bbar(blk, B_V0 + (gi & 1u)), (gi >> 1) & 1u, abort_flag, p.err)) { ok = false; break; }
           any_lo = (vote[0] | vote[1] | vote[2] | vote[3]) != 0;
         }
         // 3. the P buffer and O are free once the previous tile's P.V has finished
-        if (gi >= 1 && !wait_warp(bar(BP_EMPTY), (gi - 1) & 1u, abort_flag, p.err)) { ok = false; break; }
+        if (gi >= 1 && !wait_warp(bbar(blk, B_PE), (gi - 1) & 1u, abort_flag, p.err)) { ok = false; break; }
         {
-          const uint32_t hrow = sbase + kOffP + r * 128;
+          const uint32_t hrow = poff + r * 128;
           const uint32_t lrow = hrow + kPBytes;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
@@ -576,12 +645,14 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_tc_kernel(const __grid_consta
               st_shared_v4(lrow + (((uint32_t)c ^ (uint32_t)(r & 7)) << 4), lo4[0], lo4[1], lo4[2], lo4[3]);
             }
           }
-          if (lane == 0) lo_flags[warp] = any_lo ? 1 : 0;
+          if (lane == 0) lf[wq] = any_lo ? 1 : 0;
         }
-        // 4. value rows past the range's last token may hold anything: zero them
+        // 4. value rows past the range's last token may hold anything: zero
+        //    them (block 0's warps; a block's P.V waits for its own P only,
+        //    so every block's softmax zeroes them: the stores are idempotent)
         if (n_tile < kTile) {
           const int zrows = kTile - n_tile;
-          const uint32_t vbase = sbase + kOffKv + s * kStageBytes + kKBytes;
+          const uint32_t vbase = sbase + C::kOffKv + s * kStageBytes + kKBytes;
           for (int e = r; e < zrows * 16; e += kRows) {  // 16 pieces of 16 bytes per row (two halves)
             const int row = n_tile + e / 16, c = (e >> 3) & 1, piece = e & 7;
             st_shared_v4(vbase + c * kChunkBytes + row * 128 + piece * 16, 0u, 0u, 0u, 0u);
@@ -594,29 +665,29 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_tc_kernel(const __grid_consta
           __syncwarp();
 #pragma unroll 1
           for (int c = 0; c < kD / 32; ++c) {
-            tmem_ld32(tmem + lane_off + kColO + 32 * c, ov);
+            tmem_ld32(tmem + lane_off + col_o + 32 * c, ov);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-            tmem_st32(tmem + lane_off + kColO + 32 * c, ov);
+            tmem_st32(tmem + lane_off + col_o + 32 * c, ov);
           }
           tmem_wait_st();
         }
         // 6. publish P to the MMA issuer
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
         tc_fence_before();
-        bar_arrive(bar(BP_FULL));
+        bar_arrive(bbar(blk, B_PF));
       }
       if (!ok) break;
       // epilogue: wait for the last P.V, then write O / l and the LSE of the row
       const uint32_t glast = gt + nt - 1;
-      if (!wait_warp(bar(BP_EMPTY), glast & 1u, abort_flag, p.err)) break;
+      if (!wait_warp(bbar(blk, B_PE), glast & 1u, abort_flag, p.err)) break;
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       float* out = nullptr;
       float* out_lse = nullptr;
       if (g.out_row >= 0) {
-        const size_t row = (size_t)g.out_row * kRows + r;
+        const size_t row = (size_t)g.out_row * (NB * kRows) + rl;
         out = reinterpret_cast<float*>(const_cast<char*>(p.ws) + p.L.tmp_o_off) + row * kD;
         out_lse = reinterpret_cast<float*>(const_cast<char*>(p.ws) + p.L.tmp_lse_off) + row;
       } else if (active) {
@@ -629,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_tc_kernel(const __grid_consta
       __syncwarp();
 #pragma unroll 1
       for (int c = 0; c < kD / 32; ++c) {
-        tmem_ld32(tmem + lane_off + kColO + 32 * c, ov);
+        tmem_ld32(tmem + lane_off + col_o + 32 * c, ov);
         tmem_wait_ld();
         if (out) {
           float4* o4 = reinterpret_cast<float4*>(out + 32 * c);
@@ -648,9 +719,9 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_tc_kernel(const __grid_consta
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == C::kMmaWarp) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(C::kTmemCols));
   }
 }
 
@@ -686,22 +757,32 @@ bool pool_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows
 }
 
 // Resident CTAs (one per SM), cached per device.
+template <int NB>
 int tc_ctas_cached() {
+  using C = TcCfg<NB>;
   static std::mutex mu;
   static int cache[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
   if (cache[dev] > 0) return cache[dev];
-  if (cudaFuncSetAttribute(gqa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+  if (cudaFuncSetAttribute(gqa_tc_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+      cudaSuccess)
     return 0;
   int occ = 0, sms = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gqa_tc_kernel, kThreads, kSmemBytes) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gqa_tc_kernel<NB>, C::kThreads, C::kSmemBytes) !=
+          cudaSuccess ||
       occ <= 0)
     return 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
   cache[dev] = occ * sms;
   return cache[dev];
+}
+
+// Blocks of 128 rows per lane for a step: 2 once it has 256 rows per KV head.
+int blocks_for(const dcp_attn_desc& d, int qlen) {
+  const int g = d.num_q_heads / d.num_kv_heads;
+  return (qlen * g >= 2 * kRows && (2 * kRows) % g == 0) ? 2 : 1;
 }
 
 }  // namespace
@@ -715,14 +796,19 @@ bool gqa_tc_eligible(const dcp_attn_desc& d, int qlen) {
   return qlen * g >= kRows;  // the lanes' 128 rows are (nearly) full
 }
 
-int gqa_tc_rows_tokens(const dcp_attn_desc& d) { return kRows / (d.num_q_heads / d.num_kv_heads); }
+int gqa_tc_rows_tokens(const dcp_attn_desc& d, int qlen) {
+  return blocks_for(d, qlen) * kRows / (d.num_q_heads / d.num_kv_heads);
+}
 
-int gqa_tc_ctas(const dcp_attn_desc&, const DeviceInfo&) { return tc_ctas_cached(); }
+int gqa_tc_ctas(const dcp_attn_desc& d, const DeviceInfo&, int qlen) {
+  return blocks_for(d, qlen) == 2 ? tc_ctas_cached<2>() : tc_ctas_cached<1>();
+}
 
 cudaError_t launch_gqa_tc(const dcp_attn_desc& d, const void* q, const ShardSet& sh, const RangeSpec& rs,
                           float* o_parts, float* lses, void* ws, const WsLayout& L, int n_ctas, int32_t* err,
                           cudaStream_t st) {
-  if (n_ctas <= 0 || tc_ctas_cached() <= 0) return cudaErrorNotSupported;
+  const int nb = blocks_for(d, rs.qlen);
+  if (n_ctas <= 0 || (nb == 2 ? tc_ctas_cached<2>() : tc_ctas_cached<1>()) <= 0) return cudaErrorNotSupported;
   static_assert(sizeof(TcParams) <= 32000, "kernel parameters");
   TcParams p;
   memset(&p, 0, sizeof(p));
@@ -750,7 +836,10 @@ cudaError_t launch_gqa_tc(const dcp_attn_desc& d, const void* q, const ShardSet&
   p.Bs = d.block_size;
   p.box = box;
   p.sl2 = d.scale * kLog2e;
-  gqa_tc_kernel<<<n_ctas, kThreads, kSmemBytes, st>>>(p);
+  if (nb == 2)
+    gqa_tc_kernel<2><<<n_ctas, TcCfg<2>::kThreads, TcCfg<2>::kSmemBytes, st>>>(p);
+  else
+    gqa_tc_kernel<1><<<n_ctas, TcCfg<1>::kThreads, TcCfg<1>::kSmemBytes, st>>>(p);
   return cudaGetLastError();
 }
 

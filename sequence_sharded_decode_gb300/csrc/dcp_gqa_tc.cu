@@ -497,6 +497,10 @@ __global__ void __launch_bounds__(TcCfg<NB>::kThreads, 1) gqa_tc_kernel(const __
     const uint32_t poff = sbase + C::kOffP + 2 * blk * kPBytes;
     volatile int* lf = lo_flags(blk);
     const int js_row = rl / p.g, h = rl - js_row * p.g;  // token slot and head of the row
+    // A negative scale is taken as q -> -q (exact in bf16) with |scale|, so
+    // that the row max of the scaled scores is always |sl2| x the raw max.
+    const uint32_t qflip = p.sl2 < 0.f ? 0x80008000u : 0u;
+    const float sl2 = fabsf(p.sl2);
     uint32_t gt = 0;
     int n_items = 0;
     bool ok = true;
@@ -520,10 +524,10 @@ __global__ void __launch_bounds__(TcCfg<NB>::kThreads, 1) gqa_tc_kernel(const __
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const uint4 v = active ? qr[8 * c + i] : make_uint4(0u, 0u, 0u, 0u);
-            qv[4 * i] = v.x;
-            qv[4 * i + 1] = v.y;
-            qv[4 * i + 2] = v.z;
-            qv[4 * i + 3] = v.w;
+            qv[4 * i] = v.x ^ qflip;
+            qv[4 * i + 1] = v.y ^ qflip;
+            qv[4 * i + 2] = v.z ^ qflip;
+            qv[4 * i + 3] = v.w ^ qflip;
           }
           tmem_st32(tmem + lane_off + col_q + 32 * c, qv);
         }
@@ -549,35 +553,27 @@ __global__ void __launch_bounds__(TcCfg<NB>::kThreads, 1) gqa_tc_kernel(const __
         bar_arrive(bbar(blk, B_SE));
         // 2. online softmax over the tile's tokens (log2 units), causal per row.
         //    The scale is applied inside the exponent (one FMA per score):
-        //    the row max of the scaled scores is sl2 times the raw max (or
-        //    the raw min for a negative scale).
+        //    the row max of the scaled scores is sl2 times the raw max.
         float sc[64];
         float mx;
         if (n_valid == kTile) {
 #pragma unroll
           for (int i = 0; i < 64; ++i) sc[i] = __uint_as_float(sv[i]);
           float m8[8];
-          if (p.sl2 >= 0.f) {
 #pragma unroll
-            for (int j8 = 0; j8 < 8; ++j8)
-              m8[j8] = fmaxf(fmaxf(fmaxf(sc[8 * j8], sc[8 * j8 + 1]), fmaxf(sc[8 * j8 + 2], sc[8 * j8 + 3])),
-                             fmaxf(fmaxf(sc[8 * j8 + 4], sc[8 * j8 + 5]), fmaxf(sc[8 * j8 + 6], sc[8 * j8 + 7])));
-            mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-          } else {
-#pragma unroll
-            for (int j8 = 0; j8 < 8; ++j8)
-              m8[j8] = fminf(fminf(fminf(sc[8 * j8], sc[8 * j8 + 1]), fminf(sc[8 * j8 + 2], sc[8 * j8 + 3])),
-                             fminf(fminf(sc[8 * j8 + 4], sc[8 * j8 + 5]), fminf(sc[8 * j8 + 6], sc[8 * j8 + 7])));
-            mx = fminf(fminf(fminf(m8[0], m8[1]), fminf(m8[2], m8[3])), fminf(fminf(m8[4], m8[5]), fminf(m8[6], m8[7])));
-          }
-          mx *= p.sl2;
+          for (int j8 = 0; j8 < 8; ++j8)
+            m8[j8] = fmaxf(fmaxf(fmaxf(sc[8 * j8], sc[8 * j8 + 1]), fmaxf(sc[8 * j8 + 2], sc[8 * j8 + 3])),
+                           fmaxf(fmaxf(sc[8 * j8 + 4], sc[8 * j8 + 5]), fmaxf(sc[8 * j8 + 6], sc[8 * j8 + 7])));
+          mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+          mx *= sl2;
         } else {
-          // a partial tile: masked scores become -inf after the scaling
+          // a partial tile (the last of a range, or cut by the row's token):
+          // masked scores become -inf after the scaling
           mx = -INFINITY;
 #pragma unroll
           for (int i = 0; i < 64; ++i) {
             sc[i] = i < n_valid ? __uint_as_float(sv[i]) : 0.f;
-            mx = fmaxf(mx, i < n_valid ? sc[i] * p.sl2 : -INFINITY);
+            mx = fmaxf(mx, i < n_valid ? sc[i] * sl2 : -INFINITY);
           }
         }
         float m_new = m_run, alpha = 1.f;
@@ -596,13 +592,13 @@ __global__ void __launch_bounds__(TcCfg<NB>::kThreads, 1) gqa_tc_kernel(const __
           if (n_valid == kTile) {
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
-              sc[i] = ex2_ftz(fmaf(sc[i], p.sl2, -ref));
+              sc[i] = ex2_ftz(fmaf(sc[i], sl2, -ref));
               ls[i & 3] += sc[i];
             }
           } else {
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
-              sc[i] = i < n_valid ? ex2_ftz(fmaf(sc[i], p.sl2, -ref)) : 0.f;
+              sc[i] = i < n_valid ? ex2_ftz(fmaf(sc[i], sl2, -ref)) : 0.f;
               ls[i & 3] += sc[i];
             }
           }
@@ -636,7 +632,7 @@ __global__ void __launch_bounds__(TcCfg<NB>::kThreads, 1) gqa_tc_kernel(const __
             for (int e = 0; e < 4; ++e) hi4[e] = pack_bf16(sc[8 * c + 2 * e], sc[8 * c + 2 * e + 1]);
             st_shared_v4(hrow + (((uint32_t)c ^ (uint32_t)(r & 7)) << 4), hi4[0], hi4[1], hi4[2], hi4[3]);
           }
-          if (any_lo) {
+          if (any_lo) {  // rare: the first tiles of a range, dominant tokens
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
               uint32_t lo4[4];

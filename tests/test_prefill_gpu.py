@@ -43,6 +43,8 @@ TC_CASES = [
     ("gqa_mid", 16, dict(batch=2, ctx_fixed=1500, shards=4, needles=3)),
     ("gqa_mid", 24, dict(batch=2, ctx_fixed=1200, shards=3, scale=1.0)),                # peaky softmax
     ("gqa_mid", 40, dict(batch=2, ctx_fixed=0, shards=2)),                              # the first chunk only
+    ("gqa_mid", 32, dict(batch=2, ctx_fixed=1000, shards=3, scale=-0.0884)),            # negative scale, two blocks
+    ("gqa_mid", 8, dict(batch=2, ctx_fixed=700, shards=2, scale=0.0)),                  # zero scale: prefix means
 ]
 
 

@@ -45,6 +45,10 @@ TC_CASES = [
     ("gqa_mid", 40, dict(batch=2, ctx_fixed=0, shards=2)),                              # the first chunk only
     ("gqa_mid", 32, dict(batch=2, ctx_fixed=1000, shards=3, scale=-0.0884)),            # negative scale, two blocks
     ("gqa_mid", 8, dict(batch=2, ctx_fixed=700, shards=2, scale=0.0)),                  # zero scale: prefix means
+    ("gqa_mid", 2, dict(batch=2, q_heads=128, kv_heads=2, ctx_fixed=600, shards=2)),    # g=64: 2 tokens per block
+    ("gqa_mid", 3, dict(batch=2, q_heads=128, kv_heads=1, ctx_fixed=500, shards=3)),    # g=128: one token per block
+    ("gqa_mid", 32, dict(batch=2, ctx_kind="lognormal", median=400, sigma=1.0, ctx_lo=0, ctx_hi=2000,
+                         shards=32)),                                                   # the most shards, many empty
 ]
 
 

@@ -21,13 +21,14 @@
 //   1. S = Q . K^T (M=128 rows, N=64 tokens, K=128) into TMEM, the queries
 //      being the MMA's A operand in TMEM
 //   2. online softmax per row (thread r owns TMEM lane r), causal at the
-//      row's own token, in log2 units, lazy rescale of O (only when the
-//      running max grows by more than 2^8)
-//   3. P is written to shared memory as two bf16 terms, hi = bf16(p) and
-//      lo = bf16(p - hi); the P_lo . V product is issued only for tiles that
-//      carry more than 1/32 of some row's running weight (elsewhere dropping
-//      it changes O by at most 2^-9 x that share x max|v|), the residual
-//      itself being stored for every row on every tile
+//      row's own token, in log2 units with the scale folded into one FMA per
+//      score (a negative scale is taken as q -> -q, exact in bf16), lazy
+//      rescale of O (only when the running max grows by more than 2^8)
+//   3. P is written to shared memory as bf16, hi = bf16(p); where the tile
+//      carries more than 1/32 of some row's running weight (the block's four
+//      warps vote through an mbarrier) the residual lo = bf16(p - hi) is
+//      written too and P_lo . V issued (elsewhere dropping it changes O by
+//      at most 2^-9 x that share x max|v|)
 //   4. O += P_hi . V (M=128, N=128, K=64) into TMEM, V being read by the MMA
 //      straight from the copy of the tile (dims contiguous)
 // TMA brings the K and V rows of a tile from the paged pools (boxes of
@@ -261,7 +262,6 @@ __global__ void __launch_bounds__(TcCfg<NB>::kThreads, 1) gqa_tc_kernel(const __
     }
     uint32_t q_loads = 0, released = 0;  // items whose queries were taken; tiles whose stage was released
     bool q_ready = false;
-    int s_done_items = 0;                // items whose last score MMAs all blocks issued
     uint32_t idle = 0;
     auto pv_left = [&]() {
       bool left = false;
@@ -348,7 +348,6 @@ __global__ void __launch_bounds__(TcCfg<NB>::kThreads, 1) gqa_tc_kernel(const __
         if (all) {
           mma_commit(bar(BQ_EMPTY));
           ++q_loads;
-          ++s_done_items;
           q_ready = false;
         }
       }
@@ -362,7 +361,6 @@ __global__ void __launch_bounds__(TcCfg<NB>::kThreads, 1) gqa_tc_kernel(const __
         break;
       }
     }
-    (void)s_done_items;
     mma_commit(bar(BDRAIN));  // all issued MMAs complete before TMEM may be freed
     drain_bar(bar(BDRAIN), 0);
   } else {

@@ -386,6 +386,11 @@ __global__ void __launch_bounds__(TcCfg<NB>::kThreads, 1) gqa_tc_kernel(const __
       const int nt = g.t1 - g.t0;
       const int jt = g.tg * p.tpr + js_row;  // this row's query token
       const bool active = jt < p.qlen;
+      // a warp whose rows all lie past the last query token (a partial token
+      // group) keeps the per-tile barrier protocol but does no softmax: the
+      // P.V rows it would feed belong to rows whose outputs are not written.
+      // (One block per CTA only: with two, the extra live range costs spills.)
+      const bool idle = NB == 1 && __all_sync(0xffffffffu, !active);
       // causal limit of the row's token (global positions); inactive rows attend nothing
       const int hi_r = active ? min(g.hi, p.seq_lens[g.b] - (p.qlen - 1 - jt)) : g.lo;
       const size_t qrow = ((size_t)g.b * p.qlen + (active ? jt : 0)) * p.Hq + (size_t)g.kvh * p.g + h;
@@ -422,16 +427,21 @@ __global__ void __launch_bounds__(TcCfg<NB>::kThreads, 1) gqa_tc_kernel(const __
         if (!wait_warp(bbar(blk, B_SF), gi & 1u, abort_flag, p.err)) { ok = false; break; }
         tc_fence_after();
         uint32_t sv[64];
-        __syncwarp();
-        tmem_ld32(tmem + lane_off + col_s, sv);
-        tmem_ld32(tmem + lane_off + col_s + 32, sv + 32);
-        tmem_wait_ld();
+        if (!idle) {
+          __syncwarp();
+          tmem_ld32(tmem + lane_off + col_s, sv);
+          tmem_ld32(tmem + lane_off + col_s + 32, sv + 32);
+          tmem_wait_ld();
+        }
         tc_fence_before();
         bar_arrive(bbar(blk, B_SE));
         // 2. online softmax over the tile's tokens (log2 units), causal per row.
         //    The scale is applied inside the exponent (one FMA per score):
         //    the row max of the scaled scores is sl2 times the raw max.
         float sc[64];
+        float lsum = 0.f, alpha = 1.f;
+        bool rescale = false;
+        if (!idle) {
         float mx;
         if (n_valid == kTile) {
 #pragma unroll
@@ -453,8 +463,7 @@ __global__ void __launch_bounds__(TcCfg<NB>::kThreads, 1) gqa_tc_kernel(const __
             mx = fmaxf(mx, i < n_valid ? sc[i] * sl2 : -INFINITY);
           }
         }
-        float m_new = m_run, alpha = 1.f;
-        bool rescale = false;
+        float m_new = m_run;
         if (m_run == -INFINITY) {
           m_new = mx;
         } else if (mx > m_run + kRescaleThreshold) {
@@ -463,7 +472,6 @@ __global__ void __launch_bounds__(TcCfg<NB>::kThreads, 1) gqa_tc_kernel(const __
           rescale = true;
         }
         const float ref = m_new == -INFINITY ? 0.f : m_new;
-        float lsum;
         {
           float ls[4] = {0.f, 0.f, 0.f, 0.f};
           if (n_valid == kTile) {
@@ -483,12 +491,13 @@ __global__ void __launch_bounds__(TcCfg<NB>::kThreads, 1) gqa_tc_kernel(const __
         }
         l_run = l_run * alpha + lsum;
         m_run = m_new;
+        }  // !idle
         // The residual P_lo matters only where this tile carries more than
         // kLoFraction of some row's weight; the block's four softmax warps vote
         // (its P.V covers all 128 rows, so the residual is formed for all or none).
         bool any_lo;
         {
-          const bool warp_lo = __any_sync(0xffffffffu, lsum > kLoFraction * l_run);
+          const bool warp_lo = __any_sync(0xffffffffu, !idle && lsum > kLoFraction * l_run);
           volatile int* vote = lf + 4 + 4 * (gi & 1u);  // double-buffered by tile parity
           if (lane == 0) {
             vote[wq] = warp_lo ? 1 : 0;
@@ -499,7 +508,7 @@ __global__ void __launch_bounds__(TcCfg<NB>::kThreads, 1) gqa_tc_kernel(const __
         }
         // 3. the P buffer and O are free once the previous tile's P.V has finished
         if (gi >= 1 && !wait_warp(bbar(blk, B_PE), (gi - 1) & 1u, abort_flag, p.err)) { ok = false; break; }
-        {
+        if (!idle) {
           const uint32_t hrow = poff + r * 128;
           const uint32_t lrow = hrow + kPBytes;
 #pragma unroll
@@ -518,8 +527,8 @@ __global__ void __launch_bounds__(TcCfg<NB>::kThreads, 1) gqa_tc_kernel(const __
               st_shared_v4(lrow + (((uint32_t)c ^ (uint32_t)(r & 7)) << 4), lo4[0], lo4[1], lo4[2], lo4[3]);
             }
           }
-          if (lane == 0) lf[wq] = any_lo ? 1 : 0;
         }
+        if (lane == 0) lf[wq] = any_lo ? 1 : 0;
         // 4. value rows past the range's last token may hold anything: zero
         //    them (block 0's warps; a block's P.V waits for its own P only,
         //    so every block's softmax zeroes them: the stores are idempotent)
@@ -653,7 +662,10 @@ bool gqa_tc_eligible(const dcp_attn_desc& d, int qlen) {
   const int g = d.num_q_heads / d.num_kv_heads;
   if (g < 1 || kRows % g != 0) return false;
   if (!(d.block_size % kTile == 0 || kTile % d.block_size == 0)) return false;
-  return qlen * g >= kRows;  // the lanes' 128 rows are (nearly) full
+  // at least half of a lane's 128 rows carry query tokens: the kernel's time
+  // per lane hardly depends on how many rows are filled, and from half full
+  // it beats the mma.sync teams (GQA mid, 4 tokens x 16 heads)
+  return qlen * g >= kRows / 2;
 }
 
 int gqa_tc_rows_tokens(const dcp_attn_desc& d, int qlen) {

@@ -422,7 +422,10 @@ __global__ void __launch_bounds__(TcCfg<NB>::kThreads, 1) gqa_tc_kernel(const __
         const uint32_t gi = gt + j, s = gi % kStages;
         const int tstart = g.lo + kTile * (g.t0 + j);  // global position of the tile's first token
         const int n_tile = min(kTile, g.hi - tstart);  // tokens of the range in the tile
-        const int n_valid = max(0, min(n_tile, hi_r - tstart));
+        // inactive rows (past the last query token) take the full-tile path on
+        // scores nobody reads, so that a warp mixing them with active rows does
+        // not split into two paths; their O rows are never written or read
+        const int n_valid = active ? max(0, min(n_tile, hi_r - tstart)) : kTile;
         // 1. scores of the tile
         if (!wait_warp(bbar(blk, B_SF), gi & 1u, abort_flag, p.err)) { ok = false; break; }
         tc_fence_after();
@@ -497,7 +500,7 @@ __global__ void __launch_bounds__(TcCfg<NB>::kThreads, 1) gqa_tc_kernel(const __
         // (its P.V covers all 128 rows, so the residual is formed for all or none).
         bool any_lo;
         {
-          const bool warp_lo = __any_sync(0xffffffffu, !idle && lsum > kLoFraction * l_run);
+          const bool warp_lo = __any_sync(0xffffffffu, !idle && active && lsum > kLoFraction * l_run);
           volatile int* vote = lf + 4 + 4 * (gi & 1u);  // double-buffered by tile parity
           if (lane == 0) {
             vote[wq] = warp_lo ? 1 : 0;
@@ -662,10 +665,10 @@ bool gqa_tc_eligible(const dcp_attn_desc& d, int qlen) {
   const int g = d.num_q_heads / d.num_kv_heads;
   if (g < 1 || kRows % g != 0) return false;
   if (!(d.block_size % kTile == 0 || kTile % d.block_size == 0)) return false;
-  // at least half of a lane's 128 rows carry query tokens: the kernel's time
-  // per lane hardly depends on how many rows are filled, and from half full
-  // it beats the mma.sync teams (GQA mid, 4 tokens x 16 heads)
-  return qlen * g >= kRows / 2;
+  // at least 3/8 of a lane's 128 rows carry query tokens: the kernel's time
+  // per lane hardly depends on how many rows are filled, and from there it
+  // beats the mma.sync teams (GQA mid: 3 tokens x 16 heads)
+  return qlen * g >= 3 * kRows / 8;
 }
 
 int gqa_tc_rows_tokens(const dcp_attn_desc& d, int qlen) {

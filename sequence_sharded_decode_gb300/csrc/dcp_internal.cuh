@@ -114,7 +114,7 @@ cudaError_t launch_mla(const dcp_attn_desc& d, const void* q, const ShardSet& sh
                        float* o_parts, float* lses, void* ws, const WsLayout& L, int n_ctas,
                        int32_t* err, cudaStream_t st);
 int mla_ctas(const dcp_attn_desc& d, const DeviceInfo& di);
-// Many query rows per KV head (GQA, head dim 128, bf16 cache, q_len * g >= 64):
+// Many query rows per KV head (GQA, head dim 128, bf16 cache, q_len * g >= 48):
 // 128-row lanes of 128/g tokens x g heads on the tcgen05 tensor cores.
 bool gqa_tc_eligible(const dcp_attn_desc& d, int qlen);
 int gqa_tc_rows_tokens(const dcp_attn_desc& d, int qlen);  // query tokens per lane: 128 or 256 rows / g

@@ -296,9 +296,10 @@ def run_ours(args, wl):
 
     bytes_ = st.step_bytes()
     step_bytes = sum(bytes_.values())
+    fused = not args.two_calls
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            st.step(stream)
+            st.step(stream, fused)
     barrier()
     K = args.steps
     ev_p0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -309,12 +310,14 @@ def run_ours(args, wl):
         with torch.cuda.stream(stream):
             start.record(stream)
             for i in range(K):
-                st.append(stream)
+                st.step(stream, fused)
+            end.record(stream)
+            # the dominant kernel's call alone (plan + attention + combine of
+            # split ranges), timed on the same stream for the roofline
+            for i in range(K):
                 ev_p0[i].record(stream)
                 st.partial(stream)
                 ev_p1[i].record(stream)
-                st.merge(stream)
-            end.record(stream)
         stream.synchronize()
     barrier()
     clocks = clk.summary()
@@ -358,7 +361,7 @@ def run_ours(args, wl):
                 stream.wait_event(out_free[b])
             for n in names_in + ["o", "lse"]:
                 setattr(st, n, d[n])
-            st.step(stream)
+            st.step(stream, fused)
             done = torch.cuda.Event()
             done.record(stream)
             in_free[b] = done
@@ -394,7 +397,8 @@ def run_ours(args, wl):
     if rank == 0:
         peak, peak_kind = _peaks()
         value = whole_job_gbs(world, step_bytes, ms)
-        achieved = bytes_["partial"] / (partial_ms * 1e-3) / 1e9
+        call_bytes = bytes_["partial"]
+        achieved = call_bytes / (partial_ms * 1e-3) / 1e9
         kern = "dcp_mla.cu" if wl.kind == 1 else "dcp_gqa.cu"
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
@@ -405,16 +409,18 @@ def run_ours(args, wl):
             "config": _workload_config(wl, st, args.q_len) | {"parallelism": f"replicas x{world}"},
             "hbm_frac_of_peak": round(value / world / peak, 4),
             "tokens_per_s_per_layer": round(world * wl.batch * args.q_len / (ms * 1e-3), 1),
-            "roofline": {"bound": "hbm", "kernel": "dcp_decode_partial_all (plan + attention + combine)",
+            "roofline": {"bound": "hbm", "kernel": "dcp_decode_partial_all (plan + attention + combine), timed alone",
                          "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "traffic": (_traffic_for(kern, wl.name + ("_fp8" if wl.kv_dtype == "fp8" else ""))
                                      if args.q_len == 1 else None),
-                         "algorithmic_bytes_per_launch": bytes_["partial"]},
+                         "algorithmic_bytes_per_launch": call_bytes},
             "step_bytes": bytes_,
+            "step_calls": ("dcp_kv_append, dcp_attention_all (partial attention + one-pass merge)" if fused
+                           else "dcp_kv_append, dcp_decode_partial_all, dcp_merge"),
             "e2e": {"value": round(whole_job_gbs(world, step_bytes, e2e_ms), 2), "unit": "GB/s",
                     "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 5 * K,
+            "gpu_launches": (4 if fused else 5) * K,
             "clocks": clocks,
         }
         if args.q_len > 1:
@@ -451,6 +457,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override the preset's batch (profiling cases)")
     ap.add_argument("--shards", type=int, default=None, help="override the preset's shard count")
+    ap.add_argument("--two-calls", action="store_true",
+                    help="partial attention and merge as two calls (default: one dcp_attention_all call)")
     ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
                     help="KV cache element type (fp8: E4M3 codes with per-tensor scales, GQA only)")
     ap.add_argument("--q-len", type=int, default=1,

@@ -240,6 +240,27 @@ DCP_API int dcp_decode_partial_all_mtp(const dcp_attn_desc* desc, const void* q,
                                        int q_len, float* o_parts, float* lses, void* workspace,
                                        size_t ws_bytes, int32_t* dev_err_flag, void* stream);
 
+/* Steps 2 and 3 in one call: the partial attention of every shard (as
+ * dcp_decode_partial_all_mtp; q_len = 1 for a decode step) followed by one
+ * pass that merges, for every output row, the pieces of all N shards -- the
+ * shard's partial row, or the pieces of a shard range the balanced split cut
+ * across several CTAs -- by the LSE reweighting of dcp_merge. Same result as
+ * dcp_decode_partial_all_mtp + dcp_merge, one kernel launch fewer, and the
+ * split pieces are read once instead of being combined into o_parts first.
+ * (The pages merge the shards' partials after the per-shard attention --
+ * Qiita write-up, section "トークンの区間でGPUに割り振る", third step; this
+ * joins the two on one GPU.)
+ *   o_parts, lses  device fp32 scratch [N, B, q_len, Hq, Dv] / [N, B, q_len, Hq]
+ *                  (partial rows of shards whose range one CTA covered)
+ *   o        device fp32 [B, q_len, num_q_heads, head_dim_v] (out)
+ *   lse_out  device fp32 [B, q_len, num_q_heads] (out) or NULL
+ *   workspace >= dcp_workspace_size_mtp(desc, B, q_len, N) bytes
+ * head_dim_v must be a multiple of 4 and at most 512; o 16-byte aligned. */
+DCP_API int dcp_attention_all(const dcp_attn_desc* desc, const void* q, const dcp_shard* shards, int N,
+                              const int32_t* seq_lens, const int32_t* shard_starts, int B, int q_len,
+                              float* o_parts, float* lses, float* o, float* lse_out, void* workspace,
+                              size_t ws_bytes, int32_t* dev_err_flag, void* stream);
+
 /* Same computation as dcp_decode_partial_all, for callers that cannot
  * allocate device memory at the point of the call: for example a plugin
  * running inside a serving engine that owns every byte of device memory

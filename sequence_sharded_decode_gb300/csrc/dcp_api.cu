@@ -178,9 +178,12 @@ static int layout_for(const dcp_attn_desc& d, int B, int N, const Path& p, WsLay
   return DCP_OK;
 }
 
+// Plan, attention kernel, then either the combine of split lanes into the
+// shards' partial rows, or (o non-NULL) the one-pass merge of every output
+// row across shards and split pieces into o / lse_out.
 static int run_partial(const dcp_attn_desc* desc, const Path& path, const void* q, const ShardSet& sh,
                        const RangeSpec& rs, float* o_parts, float* lses, void* ws, size_t ws_bytes, int32_t* err,
-                       void* stream) {
+                       void* stream, float* o = nullptr, float* lse_out = nullptr) {
   const dcp_attn_desc& d = *desc;
   WsLayout L;
   int n_ctas = 0;
@@ -196,7 +199,11 @@ static int run_partial(const dcp_attn_desc* desc, const Path& path, const void* 
   else e = launch_gqa(d, q, sh, rs, o_parts, lses, ws, L, n_ctas, err, st);
   if (e == cudaErrorNotSupported) return DCP_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return DCP_ERR_CUDA;
-  if (launch_combine(d, g, rs, L.max_lanes, ws, L, o_parts, lses, st) != cudaSuccess) return DCP_ERR_CUDA;
+  if (o) {
+    if (launch_combine_merge(d, g, rs, ws, L, o_parts, lses, o, lse_out, st) != cudaSuccess) return DCP_ERR_CUDA;
+  } else if (launch_combine(d, g, rs, L.max_lanes, ws, L, o_parts, lses, st) != cudaSuccess) {
+    return DCP_ERR_CUDA;
+  }
   return DCP_OK;
 }
 
@@ -241,7 +248,7 @@ const char* dcp_status_string(int status) {
   }
 }
 
-int dcp_version(void) { return 300; }
+int dcp_version(void) { return 400; }
 
 int dcp_shard_plan(const int32_t* ctx_lens, int B, int N, int block_size, int reserve_tokens,
                    int32_t* shard_starts, int32_t* blocks_needed) {
@@ -346,6 +353,28 @@ int dcp_decode_partial_all_mtp(const dcp_attn_desc* desc, const void* q, const d
   if ((long long)B * groups > INT32_MAX) return DCP_ERR_SHAPE;
   RangeSpec rs{seq_lens, shard_starts, nullptr, dev_err_flag, 0, (int)(B * groups), N, q_len, path.tpr};
   return run_partial(desc, path, q, sh, rs, o_parts, lses, workspace, ws_bytes, dev_err_flag, stream);
+}
+
+int dcp_attention_all(const dcp_attn_desc* desc, const void* q, const dcp_shard* shards, int N,
+                      const int32_t* seq_lens, const int32_t* shard_starts, int B, int q_len, float* o_parts,
+                      float* lses, float* o, float* lse_out, void* workspace, size_t ws_bytes,
+                      int32_t* dev_err_flag, void* stream) {
+  int rc = check_desc(desc);
+  if (rc != DCP_OK) return rc;
+  ShardSet sh;
+  rc = check_shards(*desc, shards, N, &sh);
+  if (rc != DCP_OK) return rc;
+  if (B < 0 || q_len < 1 || q_len > DCP_MAX_QUERY_TOKENS) return DCP_ERR_INVALID_ARG;
+  if (B == 0) return DCP_OK;
+  if (!q || !seq_lens || !shard_starts || !o_parts || !lses || !o) return DCP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(o_parts) || !aligned16(o)) return DCP_ERR_INVALID_ARG;
+  if (desc->head_dim_v % 4 || desc->head_dim_v > 512) return DCP_ERR_UNSUPPORTED;
+  if ((long long)B * q_len > INT32_MAX) return DCP_ERR_SHAPE;
+  const Path path = path_for(*desc, q_len);
+  const long long groups = (q_len + path.tpr - 1) / path.tpr;
+  if ((long long)B * groups > INT32_MAX) return DCP_ERR_SHAPE;
+  RangeSpec rs{seq_lens, shard_starts, nullptr, dev_err_flag, 0, (int)(B * groups), N, q_len, path.tpr};
+  return run_partial(desc, path, q, sh, rs, o_parts, lses, workspace, ws_bytes, dev_err_flag, stream, o, lse_out);
 }
 
 int dcp_decode_partial_all_noalloc(const dcp_attn_desc* desc, const void* q, const dcp_shard* shards, int N,

@@ -124,6 +124,11 @@ cudaError_t launch_gqa_tc(const dcp_attn_desc& d, const void* q, const ShardSet&
                           cudaStream_t st);
 cudaError_t launch_combine(const dcp_attn_desc& d, const LaneGeom& lg, const RangeSpec& rs, int n_lanes,
                            const void* ws, const WsLayout& L, float* o_parts, float* lses, cudaStream_t st);
+// Steps 2 and 3 joined: merges every output row's pieces across the shards
+// (direct partial rows and split pieces in the workspace) into o / lse_out.
+cudaError_t launch_combine_merge(const dcp_attn_desc& d, const LaneGeom& lg, const RangeSpec& rs, const void* ws,
+                                 const WsLayout& L, const float* o_parts, const float* lses, float* o,
+                                 float* lse_out, cudaStream_t st);
 cudaError_t launch_merge(const float* o_parts, const float* lses, int N, int rows, int dv, float* o,
                          float* lse_out, cudaStream_t st);
 cudaError_t launch_append(const dcp_attn_desc& d, const ShardSet& sh, int N, const int32_t* starts,

@@ -152,7 +152,126 @@ __global__ void __launch_bounds__(kMergeThreads) combine_kernel(const char* __re
   }
 }
 
+// Steps 2 and 3 joined after the attention kernel: every output row
+// (sequence, query token, head) merges, in one pass, the pieces of all N
+// shards -- a shard's partial row where one item covered its lane, its
+// split pieces in the workspace otherwise (none for an empty lane). One warp
+// per row; the pieces' LSEs are read by every lane (broadcast), the row's
+// float4 columns are spread over the lanes.
+__global__ void __launch_bounds__(kMergeThreads) combine_merge_kernel(const char* __restrict__ ws, WsLayout L,
+                                                                      CombineGeom cg, int N,
+                                                                      const float* __restrict__ o_parts,
+                                                                      const float* __restrict__ lses,
+                                                                      float* __restrict__ o,
+                                                                      float* __restrict__ lse_out) {
+  const int lane = threadIdx.x & 31;
+  const int rpl = L.rows_per_lane, rpt = rpl / cg.tpr, dv4 = cg.dv / 4;
+  const long long rows = (long long)(cg.B / cg.G) * cg.qlen * cg.Hq;  // output rows (= partial rows of a shard)
+  const long long warps = (long long)gridDim.x * (kMergeThreads / 32);
+  const LaneRec* lrec = reinterpret_cast<const LaneRec*>(ws + L.lanes_off);
+  const float* tmp_o = reinterpret_cast<const float*>(ws + L.tmp_o_off);
+  const float* tmp_lse = reinterpret_cast<const float*>(ws + L.tmp_lse_off);
+  for (long long ro = (long long)blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5); ro < rows; ro += warps) {
+    const int h = (int)(ro % cg.Hq);
+    const long long t = ro / cg.Hq;  // b * qlen + jt
+    const int b = (int)(t / cg.qlen), jt = (int)(t - (long long)b * cg.qlen);
+    const int rg = b * cg.G + jt / cg.tpr, js = jt % cg.tpr;
+    int j, hr;  // lane within the unit, head row within the lane
+    if (cg.groups > 0) {
+      const int kvh = h / cg.g, hg = (h - kvh * cg.g) / cg.heads_per_lane;
+      j = kvh * cg.groups + hg;
+      hr = h - (kvh * cg.g + hg * cg.heads_per_lane);
+    } else {
+      j = 0;
+      hr = h;
+    }
+    const int R = js * rpt + hr;
+    float M = -INFINITY;
+    for (int i = 0; i < N; ++i) {
+      const LaneRec ln = lrec[((long long)i * cg.B + rg) * cg.lanes_per_unit + j];
+      if (ln.n_items == 1) {
+        M = fmaxf(M, lses[(long long)i * rows + ro]);
+      } else {
+        for (int k = 0; k < ln.n_items; ++k) M = fmaxf(M, tmp_lse[(long long)(ln.tmp_begin + k) * rpl + R]);
+      }
+    }
+    float4* dst = reinterpret_cast<float4*>(o) + ro * dv4;
+    if (M == -INFINITY) {  // no tokens in any shard
+      for (int c = lane; c < dv4; c += 32) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (lse_out && lane == 0) lse_out[ro] = -INFINITY;
+      continue;
+    }
+    // the columns of this lane (at most 4 float4 per lane: Dv <= 512)
+    float4 acc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+    auto add = [&](const float* row, float li) {
+      if (li == -INFINITY) return;
+      const float w = expf(li - M);
+      wsum += w;
+      const float4* src = reinterpret_cast<const float4*>(row);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int c = lane + 32 * q;
+        if (c < dv4) {
+          const float4 v = src[c];
+          acc[q].x += w * v.x;
+          acc[q].y += w * v.y;
+          acc[q].z += w * v.z;
+          acc[q].w += w * v.w;
+        }
+      }
+    };
+    for (int i = 0; i < N; ++i) {
+      const LaneRec ln = lrec[((long long)i * cg.B + rg) * cg.lanes_per_unit + j];
+      if (ln.n_items == 1) {
+        const long long pr = (long long)i * rows + ro;
+        add(o_parts + pr * cg.dv, lses[pr]);
+      } else {
+        for (int k = 0; k < ln.n_items; ++k) {
+          const long long pr = (long long)(ln.tmp_begin + k) * rpl + R;
+          add(tmp_o + pr * cg.dv, tmp_lse[pr]);
+        }
+      }
+    }
+    const float inv = 1.f / wsum;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int c = lane + 32 * q;
+      if (c < dv4) dst[c] = make_float4(acc[q].x * inv, acc[q].y * inv, acc[q].z * inv, acc[q].w * inv);
+    }
+    if (lse_out && lane == 0) lse_out[ro] = M + logf(wsum);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_combine_merge(const dcp_attn_desc& d, const LaneGeom& lg, const RangeSpec& rs, const void* ws,
+                                 const WsLayout& L, const float* o_parts, const float* lses, float* o,
+                                 float* lse_out, cudaStream_t st) {
+  if (d.head_dim_v % 4 || d.head_dim_v > 512) return cudaErrorInvalidValue;
+  CombineGeom cg;
+  cg.Hq = d.num_q_heads;
+  cg.dv = d.head_dim_v;
+  cg.lanes_per_unit = lg.lanes_per_unit;
+  cg.heads_per_lane = lg.heads_per_lane;
+  cg.groups = d.kind == DCP_KIND_GQA ? lg.groups : 0;
+  cg.g = d.num_q_heads / d.num_kv_heads;
+  cg.tpr = rs.tpr;
+  cg.qlen = rs.qlen;
+  cg.G = (rs.qlen + rs.tpr - 1) / rs.tpr;
+  cg.B = rs.B;
+  DeviceInfo di;
+  if (device_info(&di) != 0) return cudaErrorUnknown;
+  const long long rows = (long long)(rs.B / cg.G) * rs.qlen * d.num_q_heads;
+  if (rows <= 0) return cudaSuccess;
+  const long long want = (rows + kMergeThreads / 32 - 1) / (kMergeThreads / 32);
+  const int grid = (int)(want < di.sm_count * 16LL ? want : di.sm_count * 16LL);
+  combine_merge_kernel<<<grid, kMergeThreads, 0, st>>>(static_cast<const char*>(ws), L, cg, rs.N, o_parts, lses, o,
+                                                       lse_out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_merge(const float* o_parts, const float* lses, int N, int rows, int dv, float* o,
                          float* lse_out, cudaStream_t st) {

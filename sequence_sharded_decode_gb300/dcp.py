@@ -40,6 +40,7 @@ DCP_KV_FP8_E4M3 = 1
 
 EXPORTED = ("dcp_status_string", "dcp_version", "dcp_shard_plan", "dcp_kv_append", "dcp_workspace_size",
             "dcp_workspace_size_mtp", "dcp_decode_partial", "dcp_decode_partial_all", "dcp_decode_partial_all_mtp",
+            "dcp_attention_all",
             "dcp_decode_partial_all_noalloc", "dcp_merge")
 
 
@@ -134,6 +135,8 @@ def load() -> ctypes.CDLL:
     lib.dcp_decode_partial_all.argtypes = [pdesc, vp, pshard, i32, vp, vp, i32, vp, vp, vp, sz, vp, vp]
     lib.dcp_decode_partial_all_mtp.restype = i32
     lib.dcp_decode_partial_all_mtp.argtypes = [pdesc, vp, pshard, i32, vp, vp, i32, i32, vp, vp, vp, sz, vp, vp]
+    lib.dcp_attention_all.restype = i32
+    lib.dcp_attention_all.argtypes = [pdesc, vp, pshard, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp, sz, vp, vp]
     lib.dcp_decode_partial_all_noalloc.restype = i32
     lib.dcp_decode_partial_all_noalloc.argtypes = [pdesc, vp, pshard, i32, vp, vp, i32, vp, vp, vp, vp]
     lib.dcp_merge.restype = i32
@@ -289,6 +292,33 @@ def dcp_decode_partial_all_mtp(desc: AttnDesc, q: torch.Tensor, shards, seq_lens
                                            int(q.shape[1]), o_parts.data_ptr(), lses.data_ptr(),
                                            workspace.data_ptr(), workspace.numel(), _ptr(err), _stream(stream))
     _raise(rc, "dcp_decode_partial_all_mtp")
+
+
+def dcp_attention_all(desc: AttnDesc, q: torch.Tensor, shards, seq_lens: torch.Tensor, shard_starts: torch.Tensor,
+                      o_parts: torch.Tensor, lses: torch.Tensor, o: torch.Tensor, lse_out: torch.Tensor | None,
+                      workspace: torch.Tensor, err: torch.Tensor | None = None, stream=None):
+    """Partial attention of every shard and the merge in one call. q is
+    [B, Hq, Dk] (one-token decode) or [B, q_len, Hq, Dk]; o_parts / lses are
+    scratch of the shards' partial rows; o [B, (q_len,) Hq, Dv], lse_out
+    [B, (q_len,) Hq] or None receive the merged result."""
+    _check(q, torch.bfloat16, "q")
+    _check(seq_lens, torch.int32, "seq_lens")
+    _check(shard_starts, torch.int32, "shard_starts")
+    _check(o_parts, torch.float32, "o_parts")
+    _check(lses, torch.float32, "lses")
+    _check(o, torch.float32, "o")
+    if lse_out is not None:
+        _check(lse_out, torch.float32, "lse_out")
+    _check(workspace, torch.uint8, "workspace")
+    if err is not None:
+        _check(err, torch.int32, "err")
+    q_len = 1 if q.dim() == 3 else int(q.shape[1])
+    arr = _shards(shards)
+    rc = load().dcp_attention_all(ctypes.byref(desc.c()), q.data_ptr(), arr, len(shards), seq_lens.data_ptr(),
+                                  shard_starts.data_ptr(), int(q.shape[0]), q_len, o_parts.data_ptr(),
+                                  lses.data_ptr(), o.data_ptr(), _ptr(lse_out), workspace.data_ptr(),
+                                  workspace.numel(), _ptr(err), _stream(stream))
+    _raise(rc, "dcp_attention_all")
 
 
 def dcp_decode_partial_all_noalloc(desc: AttnDesc, q: torch.Tensor, shards, seq_lens: torch.Tensor,

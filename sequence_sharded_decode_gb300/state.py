@@ -121,13 +121,25 @@ class DecodeState:
             dcp.dcp_decode_partial_all_mtp(self.desc, self.q, self.shards, self.seq_lens, self.starts,
                                            self.o_parts, self.lses, self.workspace, err=self.err, stream=stream)
 
+    def attention(self, stream=None):
+        """Partial attention of every shard and the merge in one call."""
+        dcp.dcp_attention_all(self.desc, self.q, self.shards, self.seq_lens, self.starts, self.o_parts, self.lses,
+                              self.o, self.lse, self.workspace, err=self.err, stream=stream)
+
     def merge(self, stream=None):
         dcp.dcp_merge(self.o_parts, self.lses, self.o, self.lse, stream=stream)
 
-    def step(self, stream=None):
+    def step(self, stream=None, fused: bool = False):
+        """append -> partial attention of every shard -> merge; fused: the last
+        two in one call (dcp_attention_all; the shards' partial rows of split
+        ranges are then not written), else dcp_decode_partial_all(_mtp) then
+        dcp_merge."""
         self.append(stream)
-        self.partial(stream)
-        self.merge(stream)
+        if fused:
+            self.attention(stream)
+        else:
+            self.partial(stream)
+            self.merge(stream)
 
     # -- algorithmic bytes ---------------------------------------------------
     def attended_tokens(self) -> int:

@@ -188,3 +188,22 @@ def test_fp8_cache_validation(lib):
         assert lib.dcp_kv_append(ctypes.byref(d), ctypes.byref(good), 1, 16, 1, None, 16, 16, 16, 1, None,
                                  None) == status, kw
         assert lib.dcp_workspace_size(ctypes.byref(d), 1, 1) == 0
+
+
+def test_attention_all_validation(lib):
+    d = _desc().c()
+    good = dcp._Shard(16, 16, 4, 16, 2)
+    f = lib.dcp_attention_all
+    # NULL merged output, q_len out of range, N out of range: rejected on the host
+    assert f(ctypes.byref(d), 16, ctypes.byref(good), 1, 16, 16, 2, 1, 16, 16, None, None, 256, 1 << 20, None,
+             None) == dcp.DCP_ERR_INVALID_ARG
+    assert f(ctypes.byref(d), 16, ctypes.byref(good), 1, 16, 16, 2, 0, 16, 16, 16, None, 256, 1 << 20, None,
+             None) == dcp.DCP_ERR_INVALID_ARG
+    assert f(ctypes.byref(d), 16, ctypes.byref(good), 33, 16, 16, 2, 1, 16, 16, 16, None, 256, 1 << 20, None,
+             None) == dcp.DCP_ERR_INVALID_ARG
+    # misaligned merged output
+    assert f(ctypes.byref(d), 16, ctypes.byref(good), 1, 16, 16, 2, 1, 16, 16, 18, None, 256, 1 << 20, None,
+             None) == dcp.DCP_ERR_INVALID_ARG
+    # no sequences: nothing to do
+    assert f(ctypes.byref(d), 16, ctypes.byref(good), 1, 16, 16, 0, 1, None, None, None, None, None, 0, None,
+             None) == dcp.DCP_OK

@@ -30,7 +30,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // F8: the cache holds FP8 E4M3 codes (1 byte per element) instead of bf16;
-// a stage is then half as large and a warp's ring twice as deep.
+// a stage is then half as large. With head dim 128 and one warp per team the
+// kernel is held to 168 registers so that three CTAs (12 warps) share an SM,
+// each warp with a 4-stage ring: at twice the bf16 tile rate it is bound by
+// its per-tile instruction chain, and more resident warps hide its latencies.
 __device__ __forceinline__ void mma16816_f16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -48,11 +51,12 @@ __device__ __forceinline__ void split_f16(float x0, float x1, uint32_t& hi, uint
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-// two E4M3 codes (low byte first) -> fp16 pair (exact: every E4M3 value is an fp16 value)
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-  uint32_t r;
-  asm("{\n .reg .b16 t;\n cvt.u16.u32 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}\n" : "=r"(r) : "r"(two_codes));
-  return r;
+// four E4M3 codes (low byte first) -> two fp16 pairs: codes 0, 1 -> lo and
+// 2, 3 -> hi (exact: every E4M3 value is an fp16 value)
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -79,7 +83,7 @@ struct GqaCfg {
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kTile = 16;
   static constexpr int kElem = F8 ? 1 : 2;
-  static constexpr int kStages = (D == 128 ? 3 : 4) * (F8 ? 2 : 1);
+  static constexpr int kStages = F8 ? (D == 128 ? 4 : 8) : (D == 128 ? 3 : 4);
   static constexpr int kRowBytes = D * kElem;
   static constexpr int kChunks = kRowBytes / 16;        // 16-byte chunks per K row
   static constexpr int kTileBytes = kTile * kRowBytes;  // one K or V tile
@@ -165,7 +169,8 @@ __device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uin
 // tokens a lane holds, 4t .. 4t+3, are one 32-bit word of a transposed value
 // row.
 template <int D, int T, bool F8>
-__global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const __grid_constant__ GqaParams p) {
+__global__ void __launch_bounds__(GqaCfg<D>::kThreads, (F8 && D == 128 && T == 1) ? 3 : 1)
+    gqa_partial_kernel(const __grid_constant__ GqaParams p) {
   using C = GqaCfg<D, F8>;
   constexpr int kTeams = C::kWarps / T;
   constexpr int kS = T * C::kStages;  // stages of a team's ring
@@ -354,9 +359,11 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const 
             w[4 * j + 3] = v.w;
           }
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma16816_f16((kk & 1) ? s2[h] : s[h], qa[kk], e4m3x2_to_f16x2(w[kk] & 0xFFFFu),
-                         e4m3x2_to_f16x2(w[kk] >> 16));
+          for (int kk = 0; kk < D / 16; ++kk) {
+            uint32_t b0, b1;
+            e4m3x4_to_f16x4(w[kk], b0, b1);
+            mma16816_f16((kk & 1) ? s2[h] : s[h], qa[kk], b0, b1);
+          }
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h)
@@ -445,7 +452,8 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads) gqa_partial_kernel(const 
 #pragma unroll
         for (int nd = 0; nd < D / 8; ++nd) {
           const uint32_t w = lds32(vb + (nd * 8 + gr) * 16 + t4 * 4);
-          const uint32_t b0 = e4m3x2_to_f16x2(w & 0xFFFFu), b1 = e4m3x2_to_f16x2(w >> 16);
+          uint32_t b0, b1;
+          e4m3x4_to_f16x4(w, b0, b1);
           mma16816_f16(o[nd], pa, b0, b1);
           mma16816_f16(o[nd], pl, b0, b1);
         }

@@ -30,10 +30,12 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // F8: the cache holds FP8 E4M3 codes (1 byte per element) instead of bf16;
-// a stage is then half as large. With head dim 128 and one warp per team the
-// kernel is held to 168 registers so that three CTAs (12 warps) share an SM,
-// each warp with a 4-stage ring: at twice the bf16 tile rate it is bound by
-// its per-tile instruction chain, and more resident warps hide its latencies.
+// a stage is then half as large. kMinCtas: with head dim 128 the 8-bit
+// kernel (any team) and the bf16 kernel with teams of two are held to 168
+// registers so that three CTAs (12 warps) share an SM, with 4 (8-bit) or 2
+// (bf16) stages per warp: those kernels are bound by their per-tile
+// instruction chains, and more resident warps hide its latencies. The bf16
+// one-token kernel streams at the HBM rate with 2 CTAs and 3 stages.
 __device__ __forceinline__ void mma16816_f16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -77,13 +79,14 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-template <int D, bool F8 = false>
+template <int D, bool F8 = false, int T = 1>
 struct GqaCfg {
   static constexpr int kWarps = 4;
   static constexpr int kThreads = kWarps * 32;
+  static constexpr int kMinCtas = (D == 128 && (F8 || T == 2)) ? 3 : 1;
   static constexpr int kTile = 16;
   static constexpr int kElem = F8 ? 1 : 2;
-  static constexpr int kStages = F8 ? (D == 128 ? 4 : 8) : (D == 128 ? 3 : 4);
+  static constexpr int kStages = F8 ? (D == 128 ? 4 : 8) : (D == 128 ? (kMinCtas == 3 ? 2 : 3) : 4);
   static constexpr int kRowBytes = D * kElem;
   static constexpr int kChunks = kRowBytes / 16;        // 16-byte chunks per K row
   static constexpr int kTileBytes = kTile * kRowBytes;  // one K or V tile
@@ -169,9 +172,9 @@ __device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uin
 // tokens a lane holds, 4t .. 4t+3, are one 32-bit word of a transposed value
 // row.
 template <int D, int T, bool F8>
-__global__ void __launch_bounds__(GqaCfg<D>::kThreads, (F8 && D == 128 && T == 1) ? 3 : 1)
+__global__ void __launch_bounds__(GqaCfg<D>::kThreads, (GqaCfg<D, F8, T>::kMinCtas))
     gqa_partial_kernel(const __grid_constant__ GqaParams p) {
-  using C = GqaCfg<D, F8>;
+  using C = GqaCfg<D, F8, T>;
   constexpr int kTeams = C::kWarps / T;
   constexpr int kS = T * C::kStages;  // stages of a team's ring
   extern __shared__ __align__(128) unsigned char smem[];
@@ -555,7 +558,7 @@ int occupancy() {
   std::lock_guard<std::mutex> lock(mu);
   if (dev < 64 && cache[dev] > 0) return cache[dev];
   int occ = 0;
-  using C = GqaCfg<D, F8>;
+  using C = GqaCfg<D, F8, T>;
   if (cudaFuncSetAttribute(gqa_partial_kernel<D, T, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
       cudaSuccess)
     return 0;
@@ -573,13 +576,15 @@ int occupancy_for(int team) {
 
 template <int D, bool F8>
 void launch_t(const GqaParams& p, int team, int n_ctas, cudaStream_t st) {
-  using C = GqaCfg<D, F8>;
+  using C4 = GqaCfg<D, F8, 4>;
+  using C2 = GqaCfg<D, F8, 2>;
+  using C1 = GqaCfg<D, F8, 1>;
   if (team == 4)
-    gqa_partial_kernel<D, 4, F8><<<n_ctas, C::kThreads, C::kSmem, st>>>(p);
+    gqa_partial_kernel<D, 4, F8><<<n_ctas, C4::kThreads, C4::kSmem, st>>>(p);
   else if (team == 2)
-    gqa_partial_kernel<D, 2, F8><<<n_ctas, C::kThreads, C::kSmem, st>>>(p);
+    gqa_partial_kernel<D, 2, F8><<<n_ctas, C2::kThreads, C2::kSmem, st>>>(p);
   else
-    gqa_partial_kernel<D, 1, F8><<<n_ctas, C::kThreads, C::kSmem, st>>>(p);
+    gqa_partial_kernel<D, 1, F8><<<n_ctas, C1::kThreads, C1::kSmem, st>>>(p);
 }
 
 }  // namespace

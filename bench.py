@@ -220,6 +220,43 @@ def oracle_sample(wl, seqs, budget_s: float, q_len: int = 1):
     return nbytes / t_total / 1e9, t_total, desc, _cores()
 
 
+_THREAD_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS")
+
+
+def oracle_leg(args, threads: int):
+    """The oracle sample in a fresh interpreter whose BLAS pool is pinned to
+    `threads` threads (the thread count must be fixed before numpy loads).
+    Returns the leg's JSON dict, or None if it failed."""
+    env = dict(os.environ)
+    for v in _THREAD_VARS:
+        env[v] = str(threads)
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-leg", "--workload", args.workload,
+           "--cpu-seconds", str(args.cpu_seconds), "--q-len", str(args.q_len), "--kv-dtype", args.kv_dtype]
+    if args.batch is not None:
+        cmd += ["--batch", str(args.batch)]
+    if args.shards is not None:
+        cmd += ["--shards", str(args.shards)]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+        for line in reversed(r.stdout.strip().splitlines()):
+            if line.startswith("{"):
+                d = json.loads(line)
+                d["cores"] = threads
+                return d
+    except Exception:
+        pass
+    return None
+
+
+def run_oracle_leg(args, wl):
+    """Child side of oracle_leg: print the sample's throughput as one JSON line."""
+    seqs = [0, min(1, wl.batch - 1)] if wl.batch > 1 else [0]
+    gbs, secs, desc, _ = oracle_sample(wl, seqs, args.cpu_seconds, args.q_len)
+    print(json.dumps({"value": round(gbs, 4), "unit": "GB/s", "kind": "oracle", "sample": desc,
+                      "seconds": round(secs, 2)}), flush=True)
+    return 0
+
+
 def run_reference(args, wl):
     """Reference arm: the float64 CPU oracle, K timed passes over one sampled
     sequence of the workload after W untimed ones (rank 0 only)."""
@@ -435,10 +472,14 @@ def run_ours(args, wl):
                                        "note": "mma.sync / tcgen05 kernels of the decode path; peak = measured "
                                                "cuBLAS bf16, sustained"}
         if world == 1 and not args.no_cpu_baseline:
-            gbs, secs, desc, cores = oracle_sample(wl, [0, min(1, wl.batch - 1)] if wl.batch > 1 else [0],
-                                                   args.cpu_seconds, args.q_len)
-            line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                                    "sample": desc, "seconds": round(secs, 2)}
+            # the oracle on every host core (its BLAS pool pinned to the
+            # affinity count), and once on a single thread
+            allc = oracle_leg(args, _cores())
+            one = oracle_leg(args, 1)
+            if allc is not None:
+                line["cpu_baseline"] = allc
+                if one is not None:
+                    line["cpu_baseline"]["single_thread"] = {k: one[k] for k in ("value", "unit", "cores", "seconds")}
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()
@@ -449,10 +490,11 @@ def run_ours(args, wl):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="gqa_mid")
+    ap.add_argument("--workload", default="mla_high_concurrency")
+    ap.add_argument("--oracle-leg", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override the preset's batch (profiling cases)")
@@ -478,6 +520,8 @@ def main():
         if wl.kind != configs.GQA:
             ap.error("--kv-dtype fp8 is for GQA workloads")
         wl = wl.with_(kv_dtype="fp8")
+    if args.oracle_leg:
+        return run_oracle_leg(args, wl)
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)

@@ -126,6 +126,12 @@ DCP_API const char* dcp_status_string(int status);
 DCP_API int dcp_version(void);
 
 /* Routing plan on the host (step 1 of the method: contiguous token ranges).
+ * Passage: Qiita write-up "vLLMの-dcpが長文脈のKVキャッシュ重複を消して3倍速く
+ * する", section "トークンの区間でGPUに割り振る" (a 200K-token request on 4 GPUs:
+ * each GPU holds one contiguous interval of 50K tokens); "Inference Systems
+ * Infrastructure Notes (7): DCP", section 2 (each GPU keeps only its
+ * [start:end] slice of the sequence). Where the pages are silent (N does not
+ * divide the length; where later tokens go) the reading is the one below.
  * For each sequence b with ctx_lens[b] tokens before decoding, the chunk is
  * C = max(1, ceil(ctx_lens[b] / N)); shard i starts at global position i*C;
  * shard i < N-1 owns [i*C, (i+1)*C) and the last shard is open-ended, so
@@ -143,6 +149,12 @@ DCP_API int dcp_shard_plan(const int32_t* ctx_lens, int B, int N, int block_size
 
 /* Write T tokens' K/V into the owning shards' paged pools (the per-step KV
  * append of decoding; with many tokens it also fills pools from a prefill).
+ * Passage: "Inference Systems Infrastructure Notes (7): DCP", section 1
+ * (decode is token by token: each step adds one token's KV to the cache) and
+ * section 4 (decode shards the KV of every generated token; chunked and
+ * cached prefill write and reuse KV slices); the Qiita write-up, section
+ * "なぜテンソル並列だとKVキャッシュが二重に載るのか" (the cache holds the keys
+ * and values of all past tokens; MLA keeps one latent row per token).
  * Token j belongs to sequence seq_ids[j] (or to sequence j when seq_ids is
  * NULL, which requires T == B) at global position positions[j]. Its owner is
  * the last shard i with shard_starts[b, i] <= position; the local position
@@ -164,11 +176,25 @@ DCP_API int dcp_kv_append(const dcp_attn_desc* desc, const dcp_shard* shards, in
 /* Bytes of workspace dcp_decode_partial / dcp_decode_partial_all need for up
  * to B sequences and N shards with this descriptor (0 on invalid input). The
  * workspace holds the work list and the split-KV temporaries; it is reused
- * by every call (no per-step allocation) and must be 256-byte aligned. */
+ * by every call (no per-step allocation) and must be 256-byte aligned.
+ * Passage: "Inference Systems Infrastructure Notes (7): DCP", section 3 (one
+ * scratch buffer reused for the step's collectives instead of a temporary
+ * allocation and copy per step). The size does not depend on the number of
+ * cached tokens: the work list has one record per (shard, sequence) lane plus
+ * one per work CTA, and the split-range temporaries are bounded by the CTA
+ * count (a lane cut k ways needs k rows and holds k-1 CTA boundaries), so no
+ * maximum token count enters. */
 DCP_API size_t dcp_workspace_size(const dcp_attn_desc* desc, int B, int N);
 
 /* Step 2 of the method for one shard: partial decode attention of every
  * sequence's one-token query against the tokens this shard holds.
+ * Passage: Qiita write-up, section "トークンの区間でGPUに割り振る", second step
+ * (each GPU runs attention of the gathered one-token query over its own KV
+ * interval and keeps the partial output with its log-sum-exp); "Inference
+ * Systems Infrastructure Notes (7): DCP", section 2 (slices processed in
+ * parallel). The pages give no formula; the one below is plain softmax
+ * attention restricted to the shard's tokens, which the merge of step 3
+ * turns back into the exact full-context result.
  * For sequence b and query head h, over global positions t in
  * [shard_range[b,0], min(shard_range[b,1], seq_lens[b])):
  *   s_t = scale * <q[b,h], k_t>,  m = max s_t,  l = sum exp(s_t - m),
@@ -190,6 +216,9 @@ DCP_API int dcp_decode_partial(const dcp_attn_desc* desc, const void* q, const d
 /* Step 2 for all N shards in one pass of launches. Shard i of sequence b
  * covers [shard_starts[b,i], shard_starts[b,i+1]) (the last shard up to
  * seq_lens[b]), clipped to seq_lens[b].
+ * Passage: as dcp_decode_partial (Qiita write-up, section "トークンの区間で
+ * GPUに割り振る", second step); the N shards that run on N GPUs there run here
+ * as one set of launches over N pools in one memory, with the same outputs.
  *   o_parts device fp32 [N, B, num_q_heads, head_dim_v] (out)
  *   lses    device fp32 [N, B, num_q_heads] (out)
  *   workspace >= dcp_workspace_size(desc, B, N) bytes                      */
@@ -205,7 +234,9 @@ DCP_API int dcp_decode_partial_all(const dcp_attn_desc* desc, const void* q, con
 /* Bytes of workspace dcp_decode_partial_all_mtp needs for B sequences with
  * q_len query tokens each and N shards (0 on invalid input or q_len outside
  * [1, DCP_MAX_QUERY_TOKENS]); dcp_workspace_size(desc, B, N) is the q_len = 1
- * case. Same alignment and reuse rules as dcp_workspace_size. */
+ * case. Same alignment and reuse rules as dcp_workspace_size, and the same
+ * passage ("Inference Systems Infrastructure Notes (7): DCP", section 3: one
+ * reused scratch buffer). */
 DCP_API size_t dcp_workspace_size_mtp(const dcp_attn_desc* desc, int B, int q_len, int N);
 
 /* Step 2 for all N shards when each sequence brings q_len new tokens at once
@@ -276,7 +307,10 @@ DCP_API int dcp_attention_all(const dcp_attn_desc* desc, const void* q, const dc
  * allocating library routine.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current) and caches it; make
- *    that first call before any stream capture.
+ *    that first call before any stream capture. The cached address belongs
+ *    to the device's context at that time: after cudaDeviceReset on that
+ *    device it is stale, so do not call this entry point again in a process
+ *    that has reset the device.
  *  - Problems whose workspace (dcp_workspace_size(desc, B, N)) exceeds
  *    DCP_NOALLOC_SCRATCH_BYTES are rejected with DCP_ERR_SCRATCH_LIMIT before
  *    any launch.

@@ -16,12 +16,16 @@ from . import configs, dcp, inputs
 class DecodeState:
     def __init__(self, wl: configs.Workload, device: str = "cuda", fill: bool = True,
                  canary: int | None = None, table_seed: int | None = None, fill_chunk: int = 1 << 18,
-                 q_len: int = 1):
+                 q_len: int = 1, gen_device: str | None = None):
         """q_len > 1: every sequence brings q_len new tokens per step (a
         speculative / multi-token step); query token j sits at position
-        ctx[b] + j and the partial pass is dcp_decode_partial_all_mtp."""
+        ctx[b] + j and the partial pass is dcp_decode_partial_all_mtp.
+        gen_device: where the seeded draws are made before they are copied to
+        `device` (default: on `device`; "cpu" for small cases keeps the
+        device's launch list to the library's own kernels)."""
         self.wl = wl
         self.device = device
+        self.gen = device if gen_device is None else gen_device
         self.q_len = q_len
         self.ctx = wl.ctx_lens().astype(np.int64)
         B, N = wl.batch, wl.shards
@@ -55,10 +59,11 @@ class DecodeState:
         self.starts = torch.from_numpy(starts).to(device)
         qstream = inputs.STREAM_Q_MLA if wl.kind == configs.MLA else inputs.STREAM_Q
         if q_len == 1:
-            self.q = inputs.query(wl.seed, np.arange(B), wl.q_heads, wl.dk, device, stream=qstream)
+            self.q = inputs.query(wl.seed, np.arange(B), wl.q_heads, wl.dk, self.gen, stream=qstream).to(device)
             self.q0 = self.q
         else:
-            self.q = inputs.query_tokens(wl.seed, np.arange(B), q_len, wl.q_heads, wl.dk, device, stream=qstream)
+            self.q = inputs.query_tokens(wl.seed, np.arange(B), q_len, wl.q_heads, wl.dk, self.gen,
+                                         stream=qstream).to(device)
             self.q0 = self.q[:, 0].contiguous()  # planted needles copy query token 0
         self.needles = wl.needle_plan()
         new_b = np.repeat(np.arange(B), q_len)
@@ -82,31 +87,36 @@ class DecodeState:
 
     # -- token rows from the seeded generator -------------------------------
     def token_rows(self, b, t):
+        """K/V (or latent) rows of tokens (b[j], t[j]), drawn on the generation
+        device and returned on the state's device."""
         wl = self.wl
+        g = self.gen
+        b = torch.as_tensor(b).to(g)
+        t = torch.as_tensor(t).to(g)
         if wl.kind == configs.MLA:
-            lat = inputs.kv_tokens(wl.seed, inputs.STREAM_LATENT, b, t, 1, wl.dk, self.device, chunk=1 << 18)
-            lat = inputs.plant_needles(lat.view(-1, wl.dk), b, t, self.q0, self.needles, wl.q_heads)
-            return lat, None
-        k = inputs.kv_tokens(wl.seed, inputs.STREAM_K, b, t, wl.kv_heads, wl.dk, self.device, chunk=1 << 16)
-        k = inputs.plant_needles(k, b, t, self.q0, self.needles, wl.q_heads)
-        v = inputs.kv_tokens(wl.seed, inputs.STREAM_V, b, t, wl.kv_heads, wl.dv, self.device, chunk=1 << 16)
+            lat = inputs.kv_tokens(wl.seed, inputs.STREAM_LATENT, b, t, 1, wl.dk, g, chunk=1 << 18)
+            lat = inputs.plant_needles(lat.view(-1, wl.dk), b, t, self.q0.to(g), self.needles, wl.q_heads)
+            return lat.to(self.device), None
+        k = inputs.kv_tokens(wl.seed, inputs.STREAM_K, b, t, wl.kv_heads, wl.dk, g, chunk=1 << 16)
+        k = inputs.plant_needles(k, b, t, self.q0.to(g), self.needles, wl.q_heads)
+        v = inputs.kv_tokens(wl.seed, inputs.STREAM_V, b, t, wl.kv_heads, wl.dv, g, chunk=1 << 16)
         if self.f8:  # the cache holds the E4M3 codes of the same draws
-            return inputs.e4m3_codes(k), inputs.e4m3_codes(v)
-        return k, v
+            k, v = inputs.e4m3_codes(k), inputs.e4m3_codes(v)
+        return k.to(self.device), v.to(self.device)
 
     def fill_context(self, chunk: int = 1 << 18):
         """Write every context token [0, ctx[b]) of every sequence into the pools."""
-        ctx = torch.from_numpy(self.ctx).to(self.device)
+        ctx = torch.from_numpy(self.ctx).to(self.gen)
         ends = torch.cumsum(ctx, 0)
         begins = ends - ctx
         total = int(ends[-1]) if ctx.numel() else 0
         for s in range(0, total, chunk):
-            idx = torch.arange(s, min(total, s + chunk), dtype=torch.int64, device=self.device)
+            idx = torch.arange(s, min(total, s + chunk), dtype=torch.int64, device=self.gen)
             b = torch.searchsorted(ends, idx, right=True)
             t = idx - begins[b]
             k, v = self.token_rows(b, t)
-            dcp.dcp_kv_append(self.desc, self.shards, self.starts, t.to(torch.int32), k, v,
-                              seq_ids=b.to(torch.int32), err=self.err)
+            dcp.dcp_kv_append(self.desc, self.shards, self.starts, t.to(torch.int32).to(self.device), k, v,
+                              seq_ids=b.to(torch.int32).to(self.device), err=self.err)
 
     # -- the decode step through the C ABI ------------------------------------
     def append(self, stream=None):

@@ -89,12 +89,34 @@ def test_device_flag_bad_block():
     assert np.isfinite(st.o.cpu().numpy()).all()
 
 
+def _check_fused(st, wl, seqs):
+    """The path bench.py times (append, then dcp_attention_all: partial
+    attention and the one-pass merge in one call) on the same state: the
+    merged output of the sampled sequences against the oracle. The append
+    already ran, so only the fused call runs here."""
+    st.o.fill_(float("nan"))
+    st.lse.fill_(float("nan"))
+    st.attention()
+    torch.cuda.synchronize()
+    assert int(st.err.item()) == 0
+    o = st.o.cpu().numpy()
+    lse = st.lse.cpu().numpy()
+    for b in seqs:
+        L = int(st.ctx[b]) + 1
+        ro, rl, _, _ = oracle_sequence(wl, b, L, O.shard_starts([st.ctx[b]], wl.shards)[0])
+        assert_close(o[b], ro, f"fused O[b={b}]")
+        assert_lse_close(lse[b], rl, f"fused LSE[b={b}]")
+
+
 @pytest.mark.parametrize("shards", [8, 16])
 def test_mla_long_sampled(shards):
+    """Full-size long-context workload (8 x 200,001 tokens): the two-call path
+    per shard and merged, then the fused call bench.py times."""
     wl = configs.get("mla_long").with_(shards=shards)
     st = DecodeState(wl)
     st.step()
     _check(st, wl, seqs=[0, 7])
+    _check_fused(st, wl, seqs=[0, 3, 7])
 
 
 def test_mla_decode_full_size_sampled():
@@ -102,14 +124,20 @@ def test_mla_decode_full_size_sampled():
     st = DecodeState(wl)
     st.step()
     ctx = wl.ctx_lens()
-    _check(st, wl, seqs=[int(np.argmin(ctx)), int(np.argmax(ctx)), 17])
+    seqs = [int(np.argmin(ctx)), int(np.argmax(ctx)), 17]
+    _check(st, wl, seqs=seqs)
+    _check_fused(st, wl, seqs=seqs)
 
 
 def test_mla_high_concurrency_full_size_sampled():
     """The 512-sequence workload with fragmented pools, at full size: the
-    shortest and the longest sequence and one in between, every shard."""
+    shortest and the longest sequence and one in between, every shard, on the
+    two-call path and on the fused call bench.py times (append +
+    dcp_attention_all)."""
     wl = configs.get("mla_high_concurrency")
     st = DecodeState(wl)
     st.step()
     ctx = wl.ctx_lens()
-    _check(st, wl, seqs=[int(np.argmin(ctx)), int(np.argmax(ctx)), 255])
+    seqs = [int(np.argmin(ctx)), int(np.argmax(ctx)), 255]
+    _check(st, wl, seqs=seqs)
+    _check_fused(st, wl, seqs=seqs)

@@ -136,3 +136,70 @@ def test_planted_routing_mistakes_fail():
     t_append = L0
     i, _ = O.owner(t_append, starts)
     assert i == N - 1  # open-ended last shard takes the appended token
+
+
+def _mla_scatter_case(scatter):
+    """Scatter latent rows of three sequences into fragmented MLA pools with
+    `scatter` and check every row against the layout [num_blocks, block_size,
+    Dk] written out independently: row j of sequence b at global position t
+    goes to shard i = min(t // C, N - 1) with C = max(1, ceil(ctx / N)), local
+    position p = t - i * C, physical block tables[i][b, p // Bs] and slot
+    p % Bs, i.e. flat row phys * Bs + slot of the pool viewed as [rows, Dk]
+    (the view the kernels' TMA maps use). Canary values stay everywhere else."""
+    rng = np.random.default_rng(11)
+    B, N, Bs, dk = 3, 4, 8, 6
+    ctx = [37, 5, 64]
+    reserve = 3
+    starts = O.shard_starts(ctx, N)
+    counts = O.blocks_needed(ctx, N, Bs, reserve)
+    tables, pools = [], []
+    for i in range(N):
+        need = int(counts[:, i].sum())
+        cap = need + 5                       # holes: a fragmented pool
+        perm = rng.permutation(cap)
+        t = np.full((B, max(1, counts[:, i].max())), -1, dtype=np.int32)
+        off = 0
+        for b in range(B):
+            t[b, :counts[b, i]] = perm[off:off + counts[b, i]]
+            off += counts[b, i]
+        tables.append(t)
+        pools.append(np.full((cap, Bs, dk), 0xBEEF, dtype=np.uint16))
+    seq = [b for b in range(B) for _ in range(ctx[b] + reserve)]
+    pos = [t for b in range(B) for t in range(ctx[b] + reserve)]
+    lat = rng.integers(0, 60000, size=(len(pos), dk)).astype(np.uint16)
+    scatter(pools, starts, tables, Bs, seq, pos, lat)
+    written = [np.zeros(p.shape[0] * Bs, dtype=bool) for p in pools]
+    for j, (b, t) in enumerate(zip(seq, pos)):
+        C = max(1, -(-ctx[b] // N))
+        i = min(t // C, N - 1)
+        p = t - i * C
+        phys = int(tables[i][b, p // Bs])
+        row = phys * Bs + p % Bs
+        flat = pools[i].reshape(-1, dk)
+        if not np.array_equal(flat[row], lat[j]) or written[i][row]:
+            return False
+        written[i][row] = True
+    return all(np.all(pools[i].reshape(-1, dk)[~written[i]] == 0xBEEF) for i in range(N))
+
+
+def test_scatter_mla_layout_roundtrip():
+    assert _mla_scatter_case(O.scatter_mla)
+
+
+def test_scatter_mla_planted_mistakes_fail():
+    # block and slot swapped in the write, or the slot taken from the global
+    # position instead of the shard-local one: each must fail the pin above
+    def swapped(pools, starts, tables, block_size, seq_ids, positions, latent_new):
+        for j in range(len(positions)):
+            b = int(seq_ids[j])
+            i, phys, slot = O.paged_slot(int(positions[j]), starts[b], tables, b, block_size)
+            pools[i][slot % pools[i].shape[0], phys % block_size, :] = latent_new[j]
+
+    def global_slot(pools, starts, tables, block_size, seq_ids, positions, latent_new):
+        for j in range(len(positions)):
+            b, t = int(seq_ids[j]), int(positions[j])
+            i, phys, _ = O.paged_slot(t, starts[b], tables, b, block_size)
+            pools[i][phys, t % block_size, :] = latent_new[j]
+
+    assert not _mla_scatter_case(swapped)
+    assert not _mla_scatter_case(global_slot)

@@ -24,6 +24,11 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("name,over", [
     ("gqa_tiny", {}),
     ("gqa_mid", dict(batch=4, ctx_kind="lognormal", median=3000, sigma=1.0, ctx_lo=0, ctx_hi=20000, shards=3)),
+    # 64 query heads on one KV head: the tcgen05 many-row GQA kernel
+    ("gqa_mid", dict(batch=3, q_heads=64, kv_heads=1, ctx_kind="lognormal", median=2000, sigma=1.0, ctx_lo=0,
+                     ctx_hi=9000, shards=4)),
+    # the MLA pair kernel, with ranges split across CTAs (workspace rows used)
+    ("mla_decode", dict(batch=3, ctx_kind="lognormal", median=20000, sigma=1.0, ctx_lo=0, ctx_hi=60000, shards=8)),
 ])
 def test_noalloc_matches_workspace_entry_point_on_two_calls(name, over):
     wl = configs.get(name).with_(**over)

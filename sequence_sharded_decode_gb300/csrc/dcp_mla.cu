@@ -13,29 +13,45 @@
 // 256 KB, all of one SM's tensor memory, so each work item runs on a 2-CTA
 // cluster and CTA r accumulates output dims [256 r, 256 r + 256). The two
 // CTAs share no data: each computes the full scores S = Q K^T of the tile
-// itself (the score MMA is repeated, 53 % of the flops) because moving the
-// 32 KB of fp32 partial scores per tile between two SMs costs more: the
-// SM-to-SM network measured ~9 B/clk per direction on this part, against
-// ~23 B/clk of HBM bandwidth per SM. Both CTAs stream the same pages, so the
-// second read of each page hits L2. Per 64-token tile (= one paged block):
+// itself (the score MMA is repeated) because moving the 32 KB of fp32 scores
+// per tile between two SMs costs more: the SM-to-SM network measured ~9 B/clk
+// per direction on this part, against ~23 B/clk of HBM bandwidth per SM.
+// (A tcgen05 pair MMA does not avoid the repeat: the pair's two halves of an
+// operand sit at the same shared-memory offsets in both CTAs, so a token half
+// of the page for the score and a value-dim half for P.V cannot share bytes,
+// and 128 heads fill only half of a pair MMA's 256 rows.) Both CTAs stream
+// the same pages; CTA 0 pulls each page into L2 four pages ahead, so the
+// pair's copies find it there. Per 64-token tile (= one paged block):
 //   1. S = Q . K^T (M=128 heads, N=64 tokens, K=576) into TMEM; query dims
 //      0-383 are the MMA's A operand in TMEM, dims 384-575 in shared memory
-//   2. online softmax per head row (thread h owns TMEM lane h), in log2 units,
-//      lazy rescale of O (only when the running max grows by more than 2^8)
-//   3. P is written to shared memory as two bf16 terms, hi = bf16(p) and
-//      lo = bf16(p - hi), so P.V carries ~16 mantissa bits of p
+//   2. online softmax per head row, in log2 units, lazy rescale of O (only
+//      when the running max grows by more than 2^8): eight warps, two per
+//      TMEM lane quadrant; both read all 64 scores of their rows and take the
+//      same maximum, each exponentiates its own 32 tokens and keeps their
+//      row sum; the two sums meet once per item, for the epilogue
+//   3. P as two bf16 terms, hi = bf16(p) and lo = p - hi truncated to bf16
+//      (split with integer operations: conversion instructions share the
+//      SFU's issue slots with ex2), so P.V carries ~15 mantissa bits of p;
+//      P is written into the tile's own stage, over the four boxes of the
+//      other CTA's value dims (read only by the score MMA), so each stage
+//      has its own P buffer
 //   4. O_r += P_hi . V_r (M=128, N=256, K=64) into TMEM, plus P_lo . V_r for
 //      tiles that carry more than 1/32 of some row's running weight (the
 //      first tiles of an item, or a tile with a dominant token); for the
-//      others, dropping the residual changes O by at most 2^-9 x (that
+//      others, dropping the residual changes O by at most 2^-8 x (that
 //      tile's share of the row weight, < 1/32) x max|v|, and the MMA is
 //      skipped.
 // TMA brings each page as nine 64-column, 128-byte-swizzled boxes into a
-// 2-stage ring. One warp schedules the MMAs: it polls its barriers with the
-// non-blocking test_wait (a suspended try_wait reacts hundreds of cycles
-// late) and runs with uniform control flow so that one elect.sync-chosen lane
-// issues each MMA without per-instruction operand shuffling. 4 warps run the
-// softmax (exp2 on the SFU, tree max) and the epilogue. Every barrier's
+// 2-stage ring. Two warps issue MMAs, one for the scores and one for the P.V
+// products, so that a P.V enters the tensor pipe as soon as its P is ready;
+// both poll their barriers with the non-blocking test_wait (a suspended
+// try_wait reacts hundreds of cycles late) and run with uniform control flow
+// so that one elect.sync-chosen lane issues each MMA without per-instruction
+// operand shuffling. Measured on this part (clock64 traces of MLA long), a
+// page spends ~2,000-2,400 cycles in flight, ~1,450 in the score MMA, ~1,500
+// in the softmax and P stores and ~600 in P.V, and a stage holds its page
+// through all of it: with two 72 KB stages per CTA (all the shared memory the
+// query tail leaves) the period is about half that chain. Every barrier's
 // phases are observed in order and never more than one phase late, so parity
 // waits are unambiguous; every wait is bounded: on expiry the kernel raises
 // DCP_DEVERR_TIMEOUT, stops all roles, drains what it issued and frees TMEM.
@@ -61,7 +77,12 @@ constexpr int kKStepsTmem = 24;                  // query dims 0-383: A operand 
 constexpr int kKSteps = 36;                      // 16-column k-steps of the score MMA
 constexpr int kQSmemChunks = 3;                  // query dims 384-575 in shared memory
 constexpr int kStages = 2;                       // K/V tile pipeline depth
-constexpr int kThreads = 192;
+constexpr int kSoftmaxWarps = 8;                 // two per TMEM lane quadrant: token / value-dim halves
+constexpr int kProducerWarp = kSoftmaxWarps;
+constexpr int kMmaWarp = kSoftmaxWarps + 1;   // score MMAs (and the TMEM allocation)
+constexpr int kPvWarp = kSoftmaxWarps + 2;    // P.V MMAs
+constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
+constexpr int kThreads = 32 * (kSoftmaxWarps + 3);
 constexpr int kKvChunkBytes = kTile * 128;       // 64 rows x 64 bf16
 constexpr int kStageBytes = kChunks * kKvChunkBytes;
 constexpr int kQChunkBytes = kHeads * 128;       // 128 rows x 64 bf16
@@ -69,21 +90,39 @@ constexpr int kPBytes = kHeads * 128;            // 128 heads x 64 tokens bf16 (
 
 constexpr int kOffKv = 0;
 constexpr int kOffQ = kOffKv + kStages * kStageBytes;
-constexpr int kOffP = kOffQ + kQSmemChunks * kQChunkBytes;  // hi at kOffP, lo at kOffP + kPBytes
-constexpr int kOffBar = kOffP + 2 * kPBytes;
-constexpr int kNumBars = 16;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag
-constexpr int kSmemUsed = kOffMisc + 32;
+// P of a tile (hi, then lo: 2 x 16 KB) lives in its own stage, in the four boxes
+// of the other CTA's value dims (dims 256 (1-r) .. 256 (1-r) + 255), which this
+// CTA reads only in the score MMA: one P buffer per stage, so writing P never
+// waits for the previous tile's P.V.
+constexpr int kOffBar = kOffQ + kQSmemChunks * kQChunkBytes;
+constexpr int kNumBars = 18;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag, residual votes (per stage)
+constexpr int kOffLx = kOffMisc + 128;            // row-sum halves exchanged at the end of an item
+constexpr int kSmemUsed = kOffLx + 2 * kHeads * 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;      // slack to align the base to 1024
 
 // barrier slots
-constexpr int BQ_FULL = 0, BQ_EMPTY = 1, BS_FULL = 2, BS_EMPTY = 3, BP_FULL = 4, BP_EMPTY = 5, BDRAIN = 6,
-              BKV_FULL = 7, BKV_EMPTY = 7 + kStages;
+// BP_EMPTY + s: the P.V of the stage's latest tile finished (one per stage: the
+// softmax waits on it only now and then, and a stage's barrier can never run
+// more than one phase ahead of such a wait -- the tile after next in the same
+// stage needs this tile's P.V to have finished before its page may land).
+constexpr int BQ_FULL = 0, BQ_EMPTY = 1, BS_FULL = 2, BS_EMPTY = 3, BP_EMPTY = 4, BDRAIN = 6,
+              BKV_FULL = 7, BKV_EMPTY = 7 + kStages, BXCH = 7 + 2 * kStages,  // BXCH: one per lane quadrant
+              BDRAIN2 = BXCH + 4, BP_FULL = 16;  // BP_FULL + stage: the tile's P is in its stage
+static_assert(BDRAIN2 + 1 <= BP_FULL && BP_FULL + kStages <= kNumBars, "barrier slots");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;       // 256 columns: O_r, fp32
 constexpr uint32_t kColS = 256;     // 64 columns: S, fp32
 constexpr uint32_t kColQ = 320;     // 192 columns: query dims 0-383, bf16 pairs
+
+// Pages pulled into L2 ahead of the ring by CTA 0 of the pair (0: none); the
+// ring's copies then find their page in L2 instead of waiting for HBM.
+#ifndef DCP_MLA_PREFETCH_PAGES
+#define DCP_MLA_PREFETCH_PAGES 4
+#endif
+constexpr int kPrefetch = DCP_MLA_PREFETCH_PAGES;
+static_assert(kPrefetch >= 0 && kPrefetch <= 32, "prefetch distance within the table window");
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -132,6 +171,26 @@ __device__ __forceinline__ int tile_block(const MlaParams& p, const ItemGeom& g,
   return (phys < 0 || phys >= p.sh.nblk[g.shard]) ? -1 : phys;
 }
 
+// One chunk (6 of the 36 16-column k-steps) of the score MMA S = Q . K^T:
+// k-steps 0-23 take the query from TMEM, 24-35 from shared memory. kd is the
+// stage's key descriptor; descriptors advance by (byte offset >> 4).
+constexpr int kScoreChunks = 6;
+constexpr int kStepsPerChunk = kKSteps / kScoreChunks;
+template <int C>
+__device__ __forceinline__ void score_chunk(uint32_t tmem, uint64_t kd, uint64_t qdesc0, uint32_t id_s) {
+#pragma unroll
+  for (int i = 0; i < kStepsPerChunk; ++i) {
+    const int kk = C * kStepsPerChunk + i;
+    const uint64_t bdesc = kd + (uint64_t)((((kk >> 2) * kKvChunkBytes) + 32 * (kk & 3)) >> 4);
+    if (kk < kKStepsTmem) {
+      mma_ts(tmem + kColS, tmem + kColQ + 8 * kk, bdesc, id_s, kk > 0);
+    } else {
+      const int qk = kk - kKStepsTmem;
+      mma_ss(tmem + kColS, qdesc0 + (uint64_t)((((qk >> 2) * kQChunkBytes) + 32 * (qk & 3)) >> 4), bdesc, id_s, 1);
+    }
+  }
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_partial_kernel(const __grid_constant__ MlaParams p) {
   extern __shared__ unsigned char smem_raw[];
@@ -144,24 +203,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return sbase + kOffBar + 8u * i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 8);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  volatile int* lo_flags = reinterpret_cast<volatile int*>(smem + kOffMisc + 16);  // one per softmax warp
+  volatile int* lo_flags = reinterpret_cast<volatile int*>(smem + kOffMisc + 16);  // [stage][softmax warp]
 
   if (threadIdx.x == 0) {
-    bar_init(bar(BQ_FULL), 1 + kHeads);  // producer's copy of Q[:, 384:576] + softmax threads' Q[:, 0:384]
+    // producer's copy of Q[:, 384:576] + every softmax thread's share of Q[:, 0:384]
+    bar_init(bar(BQ_FULL), 1 + kSoftmaxThreads);
     bar_init(bar(BQ_EMPTY), 1);
     bar_init(bar(BS_FULL), 1);
-    bar_init(bar(BS_EMPTY), kHeads);
-    bar_init(bar(BP_FULL), kHeads);
-    bar_init(bar(BP_EMPTY), 1);
+    bar_init(bar(BS_EMPTY), kSoftmaxThreads);
+    for (int s = 0; s < kStages; ++s) bar_init(bar(BP_FULL + s), kSoftmaxThreads);
+    for (int s = 0; s < kStages; ++s) bar_init(bar(BP_EMPTY + s), 1);
     bar_init(bar(BDRAIN), 1);
+    bar_init(bar(BDRAIN2), 1);
     for (int s = 0; s < kStages; ++s) {
       bar_init(bar(BKV_FULL + s), 1);
       bar_init(bar(BKV_EMPTY + s), 1);
     }
+    for (int q4 = 0; q4 < 4; ++q4) bar_init(bar(BXCH + q4), 64);  // the two warps of a lane quadrant
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(saddr(tmem_slot)),
                  "r"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
@@ -174,7 +236,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int* cta_begin = reinterpret_cast<const int*>(p.ws + p.L.cta_off);
   const int k_begin = cta_begin[cluster], k_end = cta_begin[cluster + 1];
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     // The whole warp reads block-table entries 32 tiles at a time (lane i
     // holds tile base + i); lane 0 issues the copies.
@@ -203,6 +265,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           nxt = j + 32 + lane < nt ? tile_block(p, g, g.t0 + j + 32 + lane) : -1;
         }
         const int phys = __shfl_sync(0xffffffffu, cur, j & 31);
+        int phys_pf = -1;
+        if (kPrefetch > 0) {  // tile j + kPrefetch sits in this window of 32 table entries or the next
+          const int jp = j + kPrefetch;
+          const int a = __shfl_sync(0xffffffffu, cur, jp & 31), b2 = __shfl_sync(0xffffffffu, nxt, jp & 31);
+          phys_pf = jp < nt ? ((jp >> 5) == (j >> 5) ? a : b2) : -1;
+        }
         if (lane == 0) {
           const uint32_t s = fills % kStages, use = fills / kStages;
           if (use > 0 && !wait_bar(bar(BKV_EMPTY + s), (use - 1) & 1u, abort_flag, p.err, false)) {
@@ -214,6 +282,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int c = 0; c < kChunks; ++c)
               tma_load(sbase + kOffKv + s * kStageBytes + c * kKvChunkBytes, &p.tm_kv[g.shard], 64 * c, row,
                        bar(BKV_FULL + s));
+            if (kPrefetch > 0 && rank == 0 && phys_pf >= 0)
+              l2_prefetch(static_cast<const char*>(p.sh.k[g.shard]) + (size_t)phys_pf * kStageBytes, kStageBytes);
           }
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) { stop = true; break; }
@@ -226,85 +296,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t f0 = fills > (uint32_t)kStages ? fills - kStages : 0;
       for (uint32_t f = f0; f < fills; ++f) drain_bar(bar(BKV_FULL + f % kStages), (f / kStages) & 1u);
     }
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer
-    {  // the whole warp runs the loop (uniform control flow); one elected lane issues
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ score MMA issuer
+    // The whole warp runs the loop (uniform control flow); one elected lane
+    // issues. The P.V products come from a warp of their own (below), so a
+    // ready P.V enters the tensor pipe while a score is being issued instead
+    // of waiting for all its 36 MMAs.
+    {
       const uint32_t id_s = idesc(128, 64, 0);
-      const uint32_t id_pv = idesc(128, 256, 1);
       const uint64_t kdesc0 = sdesc(sbase + kOffKv, 0);
       const uint64_t qdesc0 = sdesc(sbase + kOffQ, 0);
-      const uint64_t pdesc0 = sdesc(sbase + kOffP, 0);
-      const uint64_t vdesc0 = sdesc(sbase + kOffKv + 4 * rank * kKvChunkBytes, kKvChunkBytes);
-      // Event-driven issue: the score MMA of the next tile and the P.V of the
-      // oldest tile whose P is ready go out as soon as their inputs are, so
-      // a late page copy never holds back the P.V that frees a stage.
       auto n_tiles = [&](int k) {
         const ItemRec it = reinterpret_cast<const ItemRec*>(p.ws + p.L.items_off)[k];
         return it.t1 - it.t0;
       };
       int ks = k_begin, js = 0, nts = ks < k_end ? n_tiles(ks) : 0;  // next score tile
-      int kp = k_begin, jp = 0, ntp = nts;                            // next P.V tile
-      uint32_t g_s = 0, g_p = 0, q_loads = 0;
+      uint32_t g_s = 0, q_loads = 0;
       bool q_ready = false;
       uint32_t idle = 0;
-      while (kp < k_end) {
+      while (ks < k_end) {
         bool progressed = false;
-        if (ks < k_end) {
-          if (!q_ready && bar_test_warp(bar(BQ_FULL), q_loads & 1u)) {
-            q_ready = true;
-            tc_fence_after();
-          }
-          const uint32_t s = g_s % kStages;
-          if (q_ready && bar_test_warp(bar(BKV_FULL + s), (g_s / kStages) & 1u) &&
-              (g_s == 0 || bar_test_warp(bar(BS_EMPTY), (g_s - 1) & 1u))) {
-            tc_fence_after();
-            // descriptors advance by (byte offset >> 4) in their address field
-            const uint64_t kd = kdesc0 + (uint64_t)((s * kStageBytes) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < kKSteps; ++kk) {
-              const uint64_t bdesc = kd + (uint64_t)((((kk >> 2) * kKvChunkBytes) + 32 * (kk & 3)) >> 4);
-              if (kk < kKStepsTmem) {
-                mma_ts(tmem + kColS, tmem + kColQ + 8 * kk, bdesc, id_s, kk > 0);
-              } else {
-                const int qk = kk - kKStepsTmem;
-                mma_ss(tmem + kColS, qdesc0 + (uint64_t)((((qk >> 2) * kQChunkBytes) + 32 * (qk & 3)) >> 4), bdesc,
-                    id_s, 1);
-              }
-            }
-            mma_commit(bar(BS_FULL));
-            if (++js == nts) {  // last score tile of the item: its queries may be replaced
-              mma_commit(bar(BQ_EMPTY));
-              ++ks;
-              js = 0;
-              nts = ks < k_end ? n_tiles(ks) : 0;
-              ++q_loads;
-              q_ready = false;
-            }
-            ++g_s;
-            progressed = true;
-          }
-        }
-        if (g_p < g_s && bar_test_warp(bar(BP_FULL), g_p & 1u)) {
+        if (!q_ready && bar_test_warp(bar(BQ_FULL), q_loads & 1u)) {
+          q_ready = true;
           tc_fence_after();
-          const uint32_t s = g_p % kStages;
-          const uint64_t vd = vdesc0 + (uint64_t)((s * kStageBytes) >> 4);  // V dims of this CTA
-          const int terms = (lo_flags[0] | lo_flags[1] | lo_flags[2] | lo_flags[3]) ? 2 : 1;
+        }
+        const uint32_t s = g_s % kStages;
+        if (q_ready && bar_test_warp(bar(BKV_FULL + s), (g_s / kStages) & 1u) &&
+            (g_s == 0 || bar_test_warp(bar(BS_EMPTY), (g_s - 1) & 1u))) {
+          tc_fence_after();
+          // descriptors advance by (byte offset >> 4) in their address field
+          const uint64_t kd = kdesc0 + (uint64_t)((s * kStageBytes) >> 4);
 #pragma unroll
-          for (int term = 0; term < 2; ++term) {
-            if (term >= terms) break;
-#pragma unroll
-            for (int kt = 0; kt < kTile / 16; ++kt)
-              mma_ss(tmem + kColO, pdesc0 + (uint64_t)((term * kPBytes + 32 * kt) >> 4),
-                  vd + (uint64_t)((2048 * kt) >> 4), id_pv, (jp == 0 && term == 0 && kt == 0) ? 0 : 1);
+          for (int kk = 0; kk < kKSteps; ++kk) {
+            const uint64_t bdesc = kd + (uint64_t)((((kk >> 2) * kKvChunkBytes) + 32 * (kk & 3)) >> 4);
+            if (kk < kKStepsTmem) {
+              mma_ts(tmem + kColS, tmem + kColQ + 8 * kk, bdesc, id_s, kk > 0);
+            } else {
+              const int qk = kk - kKStepsTmem;
+              mma_ss(tmem + kColS, qdesc0 + (uint64_t)((((qk >> 2) * kQChunkBytes) + 32 * (qk & 3)) >> 4), bdesc,
+                  id_s, 1);
+            }
           }
-          mma_commit(bar(BKV_EMPTY + s));
-          mma_commit(bar(BP_EMPTY));  // also tells softmax that this P.V finished
-          if (++jp == ntp) {
-            ++kp;
-            jp = 0;
-            ntp = kp < k_end ? n_tiles(kp) : 0;
+          mma_commit(bar(BS_FULL));
+          if (++js == nts) {  // last score tile of the item: its queries may be replaced
+            mma_commit(bar(BQ_EMPTY));
+            ++ks;
+            js = 0;
+            nts = ks < k_end ? n_tiles(ks) : 0;
+            ++q_loads;
+            q_ready = false;
           }
-          ++g_p;
+          ++g_s;
           progressed = true;
         }
         if (progressed) {
@@ -317,29 +359,94 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
       }
-      mma_commit(bar(BDRAIN));  // all issued MMAs complete before TMEM may be freed
+      mma_commit(bar(BDRAIN));  // this warp's MMAs complete before TMEM may be freed
       drain_bar(bar(BDRAIN), 0);
+    }
+  } else if (warp == kPvWarp) {
+    // ------------------------------------------------------------ P.V MMA issuer
+    // Waits for each tile's P in order. BP_FULL + s's phase for tile g (stage
+    // s = g % kStages) completes only after the stage was refilled, i.e. after
+    // the P.V of tile g - kStages, so this warp is never more than one phase
+    // behind on either barrier and its parity waits are unambiguous.
+    {
+      const uint32_t id_pv = idesc(128, 256, 1);
+      const uint64_t pdesc0 = sdesc(sbase + kOffKv + 4 * (1 - rank) * kKvChunkBytes, 0);
+      const uint64_t vdesc0 = sdesc(sbase + kOffKv + 4 * rank * kKvChunkBytes, kKvChunkBytes);
+      auto n_tiles = [&](int k) {
+        const ItemRec it = reinterpret_cast<const ItemRec*>(p.ws + p.L.items_off)[k];
+        return it.t1 - it.t0;
+      };
+      int kp = k_begin, jp = 0, ntp = kp < k_end ? n_tiles(kp) : 0;  // next P.V tile
+      uint32_t g_p = 0;
+      uint32_t idle = 0;
+      while (kp < k_end) {
+        const uint32_t s = g_p % kStages;
+        if (bar_test_warp(bar(BP_FULL + s), (g_p / kStages) & 1u)) {
+          tc_fence_after();
+          const uint64_t vd = vdesc0 + (uint64_t)((s * kStageBytes) >> 4);  // V dims of this CTA
+          const uint64_t pd = pdesc0 + (uint64_t)((s * kStageBytes) >> 4);  // P of this tile
+          int any_lo = 0;
+#pragma unroll
+          for (int w = 0; w < kSoftmaxWarps; ++w) any_lo |= lo_flags[kSoftmaxWarps * s + w];
+          const int terms = any_lo ? 2 : 1;
+#pragma unroll
+          for (int term = 0; term < 2; ++term) {
+            if (term >= terms) break;
+#pragma unroll
+            for (int kt = 0; kt < kTile / 16; ++kt)
+              mma_ss(tmem + kColO, pd + (uint64_t)((term * kPBytes + 32 * kt) >> 4),
+                  vd + (uint64_t)((2048 * kt) >> 4), id_pv, (jp == 0 && term == 0 && kt == 0) ? 0 : 1);
+          }
+          mma_commit(bar(BKV_EMPTY + s));
+          mma_commit(bar(BP_EMPTY + s));  // also tells softmax that this P.V finished
+          if (++jp == ntp) {
+            ++kp;
+            jp = 0;
+            ntp = kp < k_end ? n_tiles(kp) : 0;
+          }
+          ++g_p;
+          idle = 0;
+        } else if (++idle >= kSpinLimit) {
+          *abort_flag = 1;
+          raise_flag(p.err, DCP_DEVERR_TIMEOUT);
+          break;
+        } else if ((idle & 63u) == 0 && __any_sync(0xffffffffu, *abort_flag != 0)) {
+          break;
+        }
+      }
+      mma_commit(bar(BDRAIN2));  // this warp's MMAs complete before TMEM may be freed
+      drain_bar(bar(BDRAIN2), 0);
     }
   } else {
     // ------------------------------------------------------------ softmax / epilogue
-    const int h = threadIdx.x;  // query head = TMEM lane
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    // Warp w owns TMEM lane quadrant qd = w % 4 (query heads 32 qd .. 32 qd + 31,
+    // one per lane) and half e = w / 4: the tile's tokens 32 e .. 32 e + 31 for
+    // the exponentials and P, and this CTA's value dims 128 e .. 128 e + 127 of
+    // O. Both warps of a quadrant read all 64 scores of their rows and take
+    // the same maximum, so they hold the same running max without talking to
+    // each other; each keeps the row sum of its own tokens, and the two sums
+    // are added once per item, through shared memory, for the epilogue.
+    const int qd = warp & 3, e = warp >> 2;
+    const int h = 32 * qd + lane;  // query head = TMEM lane
+    const uint32_t lane_off = (uint32_t)(32 * qd) << 16;
     const int vlo = 4 * (int)rank;  // first V box of this CTA
+    const bool pos_scale = p.sl2 >= 0.f;
+    float* lx = reinterpret_cast<float*>(smem + kOffLx);  // [2][kHeads] row-sum halves
     uint32_t gt = 0;
     int n_items = 0;
     bool ok = true;
     for (int k = k_begin; k < k_end && ok; ++k) {
       const ItemGeom g = item_geom(p, k);
       const int nt = g.t1 - g.t0;
-      // query dims 0-383 of this item into TMEM (after the previous item's score MMAs)
+      // query dims 192 e .. 192 e + 191 of this item into TMEM (after the previous item's score MMAs)
       if (n_items > 0 && !wait_warp(bar(BQ_EMPTY), (n_items - 1) & 1, abort_flag, p.err, false)) break;
       tc_fence_after();
       {
-        const uint4* qr = reinterpret_cast<const uint4*>(p.q + ((size_t)g.b * kHeads + h) * kDk);
+        const uint4* qr = reinterpret_cast<const uint4*>(p.q + ((size_t)g.b * kHeads + h) * kDk + 192 * e);
         uint32_t qv[16];
         __syncwarp();
 #pragma unroll 1
-        for (int c = 0; c < 12; ++c) {
+        for (int c = 0; c < 6; ++c) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const uint4 v = qr[4 * c + i];
@@ -348,48 +455,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             qv[4 * i + 2] = v.z;
             qv[4 * i + 3] = v.w;
           }
-          tmem_st16(tmem + lane_off + kColQ + 16 * c, qv);
+          tmem_st16(tmem + lane_off + kColQ + 96 * e + 16 * c, qv);
         }
         tmem_wait_st();
       }
       tc_fence_before();
       bar_arrive(bar(BQ_FULL));
-      float m_run = -INFINITY, l_run = 0.f;
+      float m_run = -INFINITY, l_half = 0.f;
       for (int j = 0; j < nt; ++j) {
         const uint32_t gi = gt + j, s = gi % kStages;
         const int t = g.t0 + j;
         const int phys = tile_block(p, g, t);  // its latency hides behind the score wait
-        // 1. scores of the tile
+        // 1. scores of the tile: all 64 for the maximum, this warp's 32 for P
         if (!wait_warp(bar(BS_FULL), gi & 1u, abort_flag, p.err, false)) { ok = false; break; }
         tc_fence_after();
+        // sv[0..31]: this warp's tokens 32 e .., sv[32..63]: the other half's
         uint32_t sv[64];
         __syncwarp();
-        tmem_ld32(tmem + lane_off + kColS, sv);
-        tmem_ld32(tmem + lane_off + kColS + 32, sv + 32);
+        tmem_ld32(tmem + lane_off + kColS + 32 * e, sv);
+        tmem_ld32(tmem + lane_off + kColS + 32 * (1 - e), sv + 32);
         tmem_wait_ld();
         tc_fence_before();
         bar_arrive(bar(BS_EMPTY));
-        // 2. online softmax over the 64 tokens (log2 units)
+        // 2. online softmax (log2 units). The maximum of scale * s is taken as
+        // scale * max(s) (or * min(s) for a negative scale): one multiply.
         const int n_valid = phys < 0 ? 0 : min(kTile, g.hi - (g.lo + kTile * t));
-        float sc[64];
-        float mx;
-        if (n_valid == kTile) {  // common case: no masking; the max as a tree for ILP
-#pragma unroll
-          for (int i = 0; i < 64; ++i) sc[i] = __uint_as_float(sv[i]) * p.sl2;
+        float raw_ext;
+        if (n_valid == kTile) {  // common case: no masking; a tree for ILP
           float m8[8];
+          if (pos_scale) {
 #pragma unroll
-          for (int j8 = 0; j8 < 8; ++j8)
-            m8[j8] = fmaxf(fmaxf(fmaxf(sc[8 * j8], sc[8 * j8 + 1]), fmaxf(sc[8 * j8 + 2], sc[8 * j8 + 3])),
-                           fmaxf(fmaxf(sc[8 * j8 + 4], sc[8 * j8 + 5]), fmaxf(sc[8 * j8 + 6], sc[8 * j8 + 7])));
-          mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            for (int j8 = 0; j8 < 8; ++j8) {
+              const float* x = reinterpret_cast<const float*>(sv + 8 * j8);
+              m8[j8] = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])), fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
+            }
+            raw_ext = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+          } else {
+#pragma unroll
+            for (int j8 = 0; j8 < 8; ++j8) {
+              const float* x = reinterpret_cast<const float*>(sv + 8 * j8);
+              m8[j8] = fminf(fminf(fminf(x[0], x[1]), fminf(x[2], x[3])), fminf(fminf(x[4], x[5]), fminf(x[6], x[7])));
+            }
+            raw_ext = fminf(fminf(fminf(m8[0], m8[1]), fminf(m8[2], m8[3])), fminf(fminf(m8[4], m8[5]), fminf(m8[6], m8[7])));
+          }
         } else {
-          mx = -INFINITY;
+          raw_ext = pos_scale ? -INFINITY : INFINITY;
 #pragma unroll
           for (int i = 0; i < 64; ++i) {
-            sc[i] = i < n_valid ? __uint_as_float(sv[i]) * p.sl2 : -INFINITY;
-            mx = fmaxf(mx, sc[i]);
+            const float x = __uint_as_float(sv[i]);
+            const int tok = i < 32 ? 32 * e + i : 32 * (1 - e) + (i - 32);
+            if (tok < n_valid) raw_ext = pos_scale ? fmaxf(raw_ext, x) : fminf(raw_ext, x);
           }
         }
+        // an empty tile leaves raw_ext infinite; its scaled max is -inf
+        const float mx = n_valid > 0 ? raw_ext * p.sl2 : -INFINITY;
         float m_new = m_run, alpha = 1.f;
         bool rescale = false;
         if (m_run == -INFINITY) {
@@ -400,79 +519,91 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           rescale = true;
         }
         const float ref = m_new == -INFINITY ? 0.f : m_new;
+        float sc[32];
         float lsum;
         {
+          const int t0 = 32 * e;
           float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            sc[i] = ex2_ftz(sc[i] - ref);  // masked entries: 2^-inf = 0
+          for (int i = 0; i < 32; ++i) {
+            const float x = fmaf(__uint_as_float(sv[i]), p.sl2, -ref);
+            sc[i] = (t0 + i < n_valid) ? ex2_ftz(x) : 0.f;
             ls[i & 3] += sc[i];
           }
           lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
         }
-        l_run = l_run * alpha + lsum;
+        l_half = l_half * alpha + lsum;
         m_run = m_new;
         // The residual term matters only where this tile carries a noticeable
         // share of the row's weight (the first tiles of an item, or a tile
-        // with a dominant token); elsewhere its P.V is skipped. The residual
+        // with a dominant token); elsewhere its P.V is skipped. Each warp
+        // judges its own tokens against its own running sum (a share of a
+        // part of the row bounds the share of the whole row). The residual
         // itself is stored for every row on every tile: the P.V covers all
         // 128 rows, so when any warp asks for it, every row must be current.
-        const bool any_lo = __any_sync(0xffffffffu, lsum > kLoFraction * l_run);
-        // 3. the P buffer and O are free once the previous tile's P.V has finished
-        if (gi >= 1 && !wait_warp(bar(BP_EMPTY), (gi - 1) & 1u, abort_flag, p.err, false)) { ok = false; break; }
+        const bool any_lo = __any_sync(0xffffffffu, lsum > kLoFraction * l_half);
+        // 3. P into its stage (the score MMA that read those boxes has finished)
         {
-          const uint32_t hrow = sbase + kOffP + h * 128;
+          const uint32_t hrow = sbase + kOffKv + s * kStageBytes + 4 * (1 - rank) * kKvChunkBytes + h * 128;
           const uint32_t lrow = hrow + kPBytes;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint32_t hi[4];
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t chunk = (uint32_t)(4 * e + c);
+            uint32_t hi[4], lo[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) hi[e] = pack_bf16(sc[8 * c + 2 * e], sc[8 * c + 2 * e + 1]);
-            st_shared_v4(hrow + (((uint32_t)c ^ (uint32_t)(h & 7)) << 4), hi[0], hi[1], hi[2], hi[3]);
+            for (int k2 = 0; k2 < 4; ++k2) split_p_bf16(sc[8 * c + 2 * k2], sc[8 * c + 2 * k2 + 1], hi[k2], lo[k2]);
+            st_shared_v4(hrow + ((chunk ^ (uint32_t)(h & 7)) << 4), hi[0], hi[1], hi[2], hi[3]);
+            st_shared_v4(lrow + ((chunk ^ (uint32_t)(h & 7)) << 4), lo[0], lo[1], lo[2], lo[3]);
           }
-          {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              uint32_t lo[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) lo[e] = residual_bf16(sc[8 * c + 2 * e], sc[8 * c + 2 * e + 1]);
-              st_shared_v4(lrow + (((uint32_t)c ^ (uint32_t)(h & 7)) << 4), lo[0], lo[1], lo[2], lo[3]);
-            }
-          }
-          if (lane == 0) lo_flags[warp] = any_lo ? 1 : 0;
+          if (lane == 0) lo_flags[kSoftmaxWarps * s + warp] = any_lo ? 1 : 0;
         }
         // 4. V rows past the end of a partial tile may hold anything: zero them
         if (n_valid < kTile) {
           const int rows = kTile - n_valid;
-          for (int e = h; e < rows * 4 * 8; e += kHeads) {
-            const int r = n_valid + e / 32, c = vlo + ((e >> 3) & 3), piece = e & 7;
+          const int tid = threadIdx.x;  // 0 .. kSoftmaxThreads-1
+          for (int x = tid; x < rows * 4 * 8; x += kSoftmaxThreads) {
+            const int r = n_valid + x / 32, c = vlo + ((x >> 3) & 3), piece = x & 7;
             st_shared_v4(sbase + kOffKv + s * kStageBytes + c * kKvChunkBytes + r * 128 + piece * 16, 0u, 0u, 0u, 0u);
           }
         }
-        // 5. lazy rescale of O (warp-wide: TMEM access is per warp; the others multiply by 1)
+        // 5. lazy rescale of this warp's half of O (warp-wide: TMEM access is per
+        // warp; rows that did not grow multiply by 1), once the previous
+        // tile's P.V has finished accumulating into it.
         if (__any_sync(0xffffffffu, rescale)) {
+          if (gi >= 1 && !wait_warp(bar(BP_EMPTY + (gi - 1) % kStages), ((gi - 1) / kStages) & 1u, abort_flag, p.err,
+                                    false)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           uint32_t ov[32];
           __syncwarp();
 #pragma unroll 1
-          for (int c = 0; c < 8; ++c) {
-            tmem_ld32(tmem + lane_off + kColO + 32 * c, ov);
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t col = kColO + 128 * e + 32 * c;
+            tmem_ld32(tmem + lane_off + col, ov);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-            tmem_st32(tmem + lane_off + kColO + 32 * c, ov);
+            tmem_st32(tmem + lane_off + col, ov);
           }
           tmem_wait_st();
         }
         // 6. publish P to the MMA issuer
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
         tc_fence_before();
-        bar_arrive(bar(BP_FULL));
+        bar_arrive(bar(BP_FULL + s));
       }
       if (!ok) break;
-      // epilogue: wait for the last P.V, then write O_r / l and the LSE
+      // epilogue: the row sum of the two halves, then wait for the last P.V
+      // and write this warp's dims of O_r / l and the LSE
+      lx[e * kHeads + h] = l_half;
+      bar_arrive(bar(BXCH + qd));  // release: the partner reads lx after its wait
+      if (!wait_warp(bar(BXCH + qd), (uint32_t)n_items & 1u, abort_flag, p.err, false)) break;
+      const float l_run = l_half + lx[(1 - e) * kHeads + h];
       const uint32_t glast = gt + nt - 1;
-      if (!wait_warp(bar(BP_EMPTY), glast & 1u, abort_flag, p.err, false)) break;
+      // (P.V products finish in issue order: the last one implies the others)
+      if (!wait_warp(bar(BP_EMPTY + glast % kStages), (glast / kStages) & 1u, abort_flag, p.err, false)) break;
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       float* out;
@@ -485,12 +616,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         out = p.o_parts + ((size_t)g.u * kHeads + h) * kDv;
         out_lse = p.lses + (size_t)g.u * kHeads + h;
       }
-      out += 256 * rank;
+      out += 256 * rank + 128 * e;
       uint32_t ov[32];
       __syncwarp();
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
-        tmem_ld32(tmem + lane_off + kColO + 32 * c, ov);
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(tmem + lane_off + kColO + 128 * e + 32 * c, ov);
         tmem_wait_ld();
         float4* o4 = reinterpret_cast<float4*>(out + 32 * c);
 #pragma unroll
@@ -498,7 +629,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           o4[i] = make_float4(__uint_as_float(ov[4 * i]) * inv, __uint_as_float(ov[4 * i + 1]) * inv,
                               __uint_as_float(ov[4 * i + 2]) * inv, __uint_as_float(ov[4 * i + 3]) * inv);
       }
-      if (rank == 0) *out_lse = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+      if (rank == 0 && e == 0) *out_lse = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
       tc_fence_before();
       gt += nt;
       ++n_items;
@@ -507,7 +638,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols));
   }

@@ -96,6 +96,11 @@ __device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, i
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar) : "memory");
 }
 
+// Pull `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
+__device__ __forceinline__ void l2_prefetch(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Shared-memory matrix descriptor: 128-byte swizzle, 8-row groups 1024 B apart.
 // lbo is the byte stride between 64-element atoms along M/N for MN-major
 // operands (unused for K-major ones).
@@ -164,6 +169,19 @@ __device__ __forceinline__ float ex2_ftz(float x) {
 __device__ __forceinline__ uint32_t pack_bf16(float x0, float x1) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
   return *reinterpret_cast<const uint32_t*>(&h);
+}
+// P as two bf16 terms without conversion instructions (they share the SFU's
+// issue rate with ex2): hi = x rounded to bf16 (half-way cases up, which for
+// x >= 0 moves hi by at most half an ulp: |x - hi| <= 2^-8 |x|), taken as the
+// top 16 bits of x + 2^15 (as bits) with a byte permute; lo = the remainder
+// x - hi (exact in fp32) truncated to bf16, so |x - hi - lo| < 2^-15 |x|.
+// Pairs: x0 in the low half of each word. For finite x >= 0 below 2^127.
+__device__ __forceinline__ void split_p_bf16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const uint32_t u0 = __float_as_uint(x0) + 0x8000u, u1 = __float_as_uint(x1) + 0x8000u;
+  hi = __byte_perm(u0, u1, 0x7632);
+  const float r0 = x0 - __uint_as_float(u0 & 0xFFFF0000u);
+  const float r1 = x1 - __uint_as_float(u1 & 0xFFFF0000u);
+  lo = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
 }
 // bf16 pair of the rounding residuals x - bf16(x)
 __device__ __forceinline__ uint32_t residual_bf16(float x0, float x1) {

@@ -95,7 +95,7 @@ constexpr int kOffQ = kOffKv + kStages * kStageBytes;
 // CTA reads only in the score MMA: one P buffer per stage, so writing P never
 // waits for the previous tile's P.V.
 constexpr int kOffBar = kOffQ + kQSmemChunks * kQChunkBytes;
-constexpr int kNumBars = 18;
+constexpr int kNumBars = 19;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag, residual votes (per stage)
 constexpr int kOffLx = kOffMisc + 128;            // row-sum halves exchanged at the end of an item
 constexpr int kSmemUsed = kOffLx + 2 * kHeads * 4;
@@ -108,8 +108,9 @@ constexpr int kSmemBytes = kSmemUsed + 1024;      // slack to align the base to 
 // stage needs this tile's P.V to have finished before its page may land).
 constexpr int BQ_FULL = 0, BQ_EMPTY = 1, BS_FULL = 2, BS_EMPTY = 3, BP_EMPTY = 4, BDRAIN = 6,
               BKV_FULL = 7, BKV_EMPTY = 7 + kStages, BXCH = 7 + 2 * kStages,  // BXCH: one per lane quadrant
-              BDRAIN2 = BXCH + 4, BP_FULL = 16;  // BP_FULL + stage: the tile's P is in its stage
-static_assert(BDRAIN2 + 1 <= BP_FULL && BP_FULL + kStages <= kNumBars, "barrier slots");
+              BDRAIN2 = BXCH + 4, BP_FULL = 16,  // BP_FULL + stage: the tile's P is in its stage
+              BQT = BP_FULL + kStages;           // the copy of the query tail landed
+static_assert(BDRAIN2 + 1 <= BP_FULL && BQT + 1 <= kNumBars, "barrier slots");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;       // 256 columns: O_r, fp32
@@ -171,26 +172,6 @@ __device__ __forceinline__ int tile_block(const MlaParams& p, const ItemGeom& g,
   return (phys < 0 || phys >= p.sh.nblk[g.shard]) ? -1 : phys;
 }
 
-// One chunk (6 of the 36 16-column k-steps) of the score MMA S = Q . K^T:
-// k-steps 0-23 take the query from TMEM, 24-35 from shared memory. kd is the
-// stage's key descriptor; descriptors advance by (byte offset >> 4).
-constexpr int kScoreChunks = 6;
-constexpr int kStepsPerChunk = kKSteps / kScoreChunks;
-template <int C>
-__device__ __forceinline__ void score_chunk(uint32_t tmem, uint64_t kd, uint64_t qdesc0, uint32_t id_s) {
-#pragma unroll
-  for (int i = 0; i < kStepsPerChunk; ++i) {
-    const int kk = C * kStepsPerChunk + i;
-    const uint64_t bdesc = kd + (uint64_t)((((kk >> 2) * kKvChunkBytes) + 32 * (kk & 3)) >> 4);
-    if (kk < kKStepsTmem) {
-      mma_ts(tmem + kColS, tmem + kColQ + 8 * kk, bdesc, id_s, kk > 0);
-    } else {
-      const int qk = kk - kKStepsTmem;
-      mma_ss(tmem + kColS, qdesc0 + (uint64_t)((((qk >> 2) * kQChunkBytes) + 32 * (qk & 3)) >> 4), bdesc, id_s, 1);
-    }
-  }
-}
-
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_partial_kernel(const __grid_constant__ MlaParams p) {
   extern __shared__ unsigned char smem_raw[];
@@ -206,8 +187,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   volatile int* lo_flags = reinterpret_cast<volatile int*>(smem + kOffMisc + 16);  // [stage][softmax warp]
 
   if (threadIdx.x == 0) {
-    // producer's copy of Q[:, 384:576] + every softmax thread's share of Q[:, 0:384]
-    bar_init(bar(BQ_FULL), 1 + kSoftmaxThreads);
+    bar_init(bar(BQ_FULL), kSoftmaxThreads);  // every softmax thread's share of Q[:, 0:384] in TMEM
+    bar_init(bar(BQT), 1);                    // the producer's copy of Q[:, 384:576]
     bar_init(bar(BQ_EMPTY), 1);
     bar_init(bar(BS_FULL), 1);
     bar_init(bar(BS_EMPTY), kSoftmaxThreads);
@@ -253,9 +234,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (n_items > 0 && !wait_bar(bar(BQ_EMPTY), (n_items - 1) & 1, abort_flag, p.err, false)) {
           ok = false;
         } else {
-          bar_arrive_tx(bar(BQ_FULL), kQSmemChunks * kQChunkBytes);
+          bar_arrive_tx(bar(BQT), kQSmemChunks * kQChunkBytes);
           for (int c = 0; c < kQSmemChunks; ++c)
-            tma_load(sbase + kOffQ + c * kQChunkBytes, &p.tm_q, 384 + 64 * c, g.b * kHeads, bar(BQ_FULL));
+            tma_load(sbase + kOffQ + c * kQChunkBytes, &p.tm_q, 384 + 64 * c, g.b * kHeads, bar(BQT));
         }
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) { stop = true; break; }
@@ -292,7 +273,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ++n_items;
     }
     if (lane == 0 && *abort_flag) {  // copies in flight must land before the CTA may exit
-      if (n_items > 0) drain_bar(bar(BQ_FULL), (n_items - 1) & 1u);
+      if (n_items > 0) drain_bar(bar(BQT), (n_items - 1) & 1u);
       const uint32_t f0 = fills > (uint32_t)kStages ? fills - kStages : 0;
       for (uint32_t f = f0; f < fills; ++f) drain_bar(bar(BKV_FULL + f % kStages), (f / kStages) & 1u);
     }
@@ -316,7 +297,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t idle = 0;
       while (ks < k_end) {
         bool progressed = false;
-        if (!q_ready && bar_test_warp(bar(BQ_FULL), q_loads & 1u)) {
+        if (!q_ready && bar_test_warp(bar(BQ_FULL), q_loads & 1u) && bar_test_warp(bar(BQT), q_loads & 1u)) {
           q_ready = true;
           tc_fence_after();
         }

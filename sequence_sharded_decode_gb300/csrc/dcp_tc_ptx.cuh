@@ -17,7 +17,13 @@
 namespace dcp {
 namespace {
 
-constexpr uint32_t kSpinLimit = 1u << 24;  // polls before a wait gives up
+// Polls before a wait gives up. A build may lower it (-DDCP_SPIN_LIMIT=n) to
+// exercise the expiry path: every kernel then aborts at its first wait that
+// is not already satisfied, raises DCP_DEVERR_TIMEOUT and returns.
+#ifndef DCP_SPIN_LIMIT
+#define DCP_SPIN_LIMIT (1u << 24)
+#endif
+constexpr uint32_t kSpinLimit = DCP_SPIN_LIMIT;
 
 __device__ __forceinline__ uint32_t saddr(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
@@ -84,10 +90,11 @@ __device__ __forceinline__ bool wait_warp(uint32_t b, uint32_t parity, volatile 
   const bool ok = wait_bar(b, parity, abort_flag, err, cluster_scope);
   return __all_sync(0xffffffffu, ok);
 }
-// Bounded wait that ignores the abort flag (teardown drains).
+// Bounded wait that ignores the abort flag (teardown drains: copies and MMAs
+// already issued always complete). Polled, so the bound is a poll count.
 __device__ __forceinline__ void drain_bar(uint32_t b, uint32_t parity) {
   for (uint32_t i = 0; i < (1u << 22); ++i)
-    if (bar_try(b, parity)) return;
+    if (bar_test(b, parity)) return;
 }
 
 __device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {

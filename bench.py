@@ -167,7 +167,10 @@ def oracle_prepare(wl, seqs, q_len: int = 1):
             q = inputs.bf16_bits(inputs.query(wl.seed, [b], wl.q_heads, wl.dk, stream=qs))[0]
         else:
             q = inputs.bf16_bits(inputs.query_tokens(wl.seed, [b], q_len, wl.q_heads, wl.dk, stream=qs))[0]
-        if wl.kind == configs.MLA:
+        if wl.kind == configs.MLA and wl.kv_dtype == "fp8":  # one row of E4M3 codes per token
+            kb = inputs.e4m3_codes(inputs.sequence_kv(wl.seed, inputs.STREAM_LATENT, b, 0, L, 1, wl.dk)).numpy()
+            vb = kb[:, :, :wl.dv]
+        elif wl.kind == configs.MLA:
             kb = inputs.bf16_bits(inputs.sequence_kv(wl.seed, inputs.STREAM_LATENT, b, 0, L, 1, wl.dk))
             vb = None
         elif wl.kv_dtype == "fp8":  # E4M3 codes (uint8) of the same draws
@@ -502,7 +505,7 @@ def main():
     ap.add_argument("--two-calls", action="store_true",
                     help="partial attention and merge as two calls (default: one dcp_attention_all call)")
     ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
-                    help="KV cache element type (fp8: E4M3 codes with per-tensor scales, GQA only)")
+                    help="KV cache element type (fp8: E4M3 codes with per-tensor scales)")
     ap.add_argument("--q-len", type=int, default=1,
                     help="query tokens per sequence per step (speculative step, or a prefill chunk)")
     args = ap.parse_args()
@@ -517,8 +520,6 @@ def main():
     if args.shards is not None:
         wl = wl.with_(shards=args.shards)
     if args.kv_dtype == "fp8":
-        if wl.kind != configs.GQA:
-            ap.error("--kv-dtype fp8 is for GQA workloads")
         wl = wl.with_(kv_dtype="fp8")
     if args.oracle_leg:
         return run_oracle_leg(args, wl)

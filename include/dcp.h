@@ -30,8 +30,8 @@
  *    is non-NULL) and skips that access; the caller reads the flag after the
  *    stream is synchronised and clears it itself.
  *  - Data types: queries are bf16 (raw 16-bit patterns); the KV cache and
- *    appended tokens are bf16, or for GQA optionally FP8 E4M3 codes with one
- *    scale for all keys and one for all values (dcp_attn_desc.kv_dtype);
+ *    appended tokens are bf16, or optionally FP8 E4M3 codes with one scale
+ *    for all keys and one for all values (dcp_attn_desc.kv_dtype);
  *    outputs and partials are fp32; LSE is the natural logarithm.
  */
 #ifndef DCP_H_
@@ -83,11 +83,13 @@ typedef enum { DCP_KV_BF16 = 0, DCP_KV_FP8_E4M3 = 1 } dcp_kv_dtype;
  *       head_dim_k == head_dim_v in {64, 128}; block_size a multiple of 16.
  *  MLA (absorbed): num_kv_heads == 1; the cached row is the latent of width
  *       head_dim_k (576); the key is the whole row and the value is its first
- *       head_dim_v (512) entries; block_size == 64; kv_dtype bf16 only.
+ *       head_dim_v (512) entries; block_size == 64. With the 8-bit cache the
+ *       row is stored once as codes: key = k_scale * decode(row), value =
+ *       v_scale * decode(row[:head_dim_v]).
  *  scale multiplies q.k before the softmax (e.g. 1/sqrt(head_dim_k)).
- *  kv_dtype DCP_KV_FP8_E4M3 (GQA only): k_scale and v_scale must be finite
- *  and > 0; the kernels widen the codes to fp16 exactly and convert q to
- *  fp16 (|q| must stay below 65504). For bf16 the scales are ignored. */
+ *  kv_dtype DCP_KV_FP8_E4M3: k_scale and v_scale must be finite and > 0; the
+ *  kernels widen the codes to fp16 exactly and convert q to fp16 (|q| must
+ *  stay below 65504). For bf16 the scales are ignored. */
 typedef struct {
   int kind;          /* dcp_kind */
   int num_q_heads;
@@ -107,7 +109,8 @@ typedef struct {
  *       FP8 cache: k_pool [num_blocks, num_kv_heads, block_size, head_dim_k]
  *       and v_pool [num_blocks, num_kv_heads, head_dim_v, block_size] E4M3
  *       codes (the values of a block stored transposed, dims by tokens).
- *  MLA: k_pool [num_blocks, block_size, head_dim_k] bf16, v_pool NULL.
+ *  MLA: k_pool [num_blocks, block_size, head_dim_k] bf16 (or E4M3 codes),
+ *       v_pool NULL.
  *  block_table: int32 [B, max_blocks_per_seq]; row b maps the shard-local
  *  logical block index (local position / block_size) of sequence b to a
  *  physical block of this pool. Pools must be 16-byte aligned. */

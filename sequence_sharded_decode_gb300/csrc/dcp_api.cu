@@ -126,7 +126,6 @@ static int check_desc(const dcp_attn_desc* d) {
   if (d->kv_dtype == DCP_KV_FP8_E4M3) {
     if (!std::isfinite(d->k_scale) || !std::isfinite(d->v_scale) || !(d->k_scale > 0.f) || !(d->v_scale > 0.f))
       return DCP_ERR_INVALID_ARG;
-    if (d->kind != DCP_KIND_GQA) return DCP_ERR_UNSUPPORTED;
   }
   if (d->kind == DCP_KIND_GQA) {
     if (d->head_dim_k != d->head_dim_v) return DCP_ERR_UNSUPPORTED;

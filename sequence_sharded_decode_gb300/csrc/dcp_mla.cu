@@ -64,6 +64,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <cmath>
 #include <mutex>
@@ -95,17 +96,26 @@ constexpr int kQChunkBytes = kHeads * 128;       // 128 rows x 64 bf16
 constexpr int kPBytes = kHeads * 128;            // 128 heads x 64 tokens bf16 (one term)
 
 constexpr int kOffKv = 0;
-constexpr int kOffQ = kOffKv + kStages * kStageBytes;
+constexpr int kCodesPage = kTile * kDk;          // 8-bit cache: one page of E4M3 codes (36 KB)
 // P of a tile (hi, then lo: 2 x 16 KB) lives in its own stage, in the four boxes
 // of the other CTA's value dims (dims 256 (1-r) .. 256 (1-r) + 255), which this
 // CTA reads only in the score MMA: one P buffer per stage, so writing P never
 // waits for the previous tile's P.V.
-constexpr int kOffBar = kOffQ + kQSmemChunks * kQChunkBytes;
-constexpr int kNumBars = 19;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag, residual votes (per stage)
-constexpr int kOffLx = kOffMisc + 128;            // row-sum halves exchanged at the end of an item
-constexpr int kSmemUsed = kOffLx + 2 * kHeads * 4;
-constexpr int kSmemBytes = kSmemUsed + 1024;      // slack to align the base to 1024
+// The 8-bit cache (F8) rings pages of E4M3 codes instead (36 KB per stage,
+// one bulk copy each, no multicast), and the softmax warps widen each page,
+// exactly, into one fp16 page laid out like the bf16 boxes (kOffF16), which
+// the fp16 MMAs read; its P then lives in that page's dead boxes.
+constexpr int kNumBars = 21;
+template <bool F8>
+struct MlaLayout {
+  static constexpr int kStage = F8 ? kCodesPage : kStageBytes;  // one ring stage
+  static constexpr int kOffF16 = kOffKv + kStages * kStage;      // F8: the widened page
+  static constexpr int kOffQ = F8 ? kOffF16 + kStageBytes : kOffF16;
+  static constexpr int kOffBar = kOffQ + kQSmemChunks * kQChunkBytes;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag, residual votes (per stage)
+  static constexpr int kOffLx = kOffMisc + 128;            // row-sum halves exchanged at the end of an item
+  static constexpr int kSmemBytes = kOffLx + 2 * kHeads * 4 + 1024;  // slack to align the base to 1024
+};
 
 // barrier slots
 // BP_EMPTY + s: the P.V of the stage's latest tile finished (one per stage: the
@@ -115,8 +125,10 @@ constexpr int kSmemBytes = kSmemUsed + 1024;      // slack to align the base to 
 constexpr int BQ_FULL = 0, BQ_EMPTY = 1, BS_FULL = 2, BS_EMPTY = 3, BP_EMPTY = 4, BDRAIN = 6,
               BKV_FULL = 7, BKV_EMPTY = 7 + kStages, BXCH = 7 + 2 * kStages,  // BXCH: one per lane quadrant
               BDRAIN2 = BXCH + 4, BP_FULL = 16,  // BP_FULL + stage: the tile's P is in its stage
-              BQT = BP_FULL + kStages;           // the copy of the query tail landed
-static_assert(BDRAIN2 + 1 <= BP_FULL && BQT + 1 <= kNumBars, "barrier slots");
+              BQT = BP_FULL + kStages,           // the copy of the query tail landed
+              BF_FULL = BQT + 1,                 // F8: the widened page is in place
+              BF_EMPTY = BQT + 2;                // F8: the widened page's P.V finished
+static_assert(BDRAIN2 + 1 <= BP_FULL && BF_EMPTY + 1 <= kNumBars, "barrier slots");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;       // 256 columns: O_r, fp32
@@ -148,7 +160,8 @@ struct MlaParams {
   int32_t* err;
   int B;     // query rows: sequences x qlen
   int qlen;  // query tokens per sequence (block-table row = query row / qlen)
-  float sl2;
+  float sl2;      // scale * log2(e) (x k_scale for the 8-bit cache)
+  float v_scale;  // 8-bit cache: a value is v_scale * decode(code); 1 otherwise
 };
 
 // Shared geometry of one work item, derived identically by every role.
@@ -178,8 +191,41 @@ __device__ __forceinline__ int tile_block(const MlaParams& p, const ItemGeom& g,
   return (phys < 0 || phys >= p.sh.nblk[g.shard]) ? -1 : phys;
 }
 
+// hi = fp16(x), lo = fp16(x - hi) for a pair (x0 in the low half): P of the
+// 8-bit cache's fp16 MMAs carries ~22 mantissa bits; x >= 0, below 2^15.
+__device__ __forceinline__ void split_p_f16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(x0, x1);
+  const float2 hf = __half22float2(h);
+  const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+// bf16 pair -> fp16 pair (round to nearest; the query of the 8-bit cache's
+// fp16 MMAs, |q| below 65504)
+__device__ __forceinline__ uint32_t bf16x2_as_f16x2(uint32_t v) {
+  const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+  const __half2 h = __floats2half2_rn(f.x, f.y);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ uint4 lds128_u32(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+// four E4M3 codes (low byte first) -> two fp16 pairs, exactly: codes 0, 1 ->
+// lo, codes 2, 3 -> hi
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+template <bool F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_partial_kernel(const __grid_constant__ MlaParams p) {
+  using Lay = MlaLayout<F8>;
+  constexpr int kOffQ = Lay::kOffQ, kOffBar = Lay::kOffBar, kOffMisc = Lay::kOffMisc, kOffLx = Lay::kOffLx;
+  constexpr int kStage = Lay::kStage, kOffF16 = Lay::kOffF16;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = saddr(smem_raw);
   unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -204,9 +250,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bar_init(bar(BDRAIN2), 1);
     for (int s = 0; s < kStages; ++s) {
       bar_init(bar(BKV_FULL + s), 1);
-      bar_init(bar(BKV_EMPTY + s), 2);  // the P.V of both CTAs (the page lands in both)
+      // bf16: the P.V of both CTAs (the page lands in both); F8: the widening of the codes
+      bar_init(bar(BKV_EMPTY + s), F8 ? kSoftmaxThreads : 2);
     }
     for (int q4 = 0; q4 < 4; ++q4) bar_init(bar(BXCH + q4), 64);  // the two warps of a lane quadrant
+    bar_init(bar(BF_FULL), kSoftmaxThreads);
+    bar_init(bar(BF_EMPTY), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
@@ -238,7 +287,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int nxt = 32 + lane < nt ? tile_block(p, g, g.t0 + 32 + lane) : -1;
       bool ok = true;
       if (lane == 0) {
-        if (n_items > 0 && !wait_bar(bar(BQ_EMPTY), (n_items - 1) & 1, abort_flag, p.err, false)) {
+        if (F8) {
+          // the softmax warps write the fp16 query tail themselves
+        } else if (n_items > 0 && !wait_bar(bar(BQ_EMPTY), (n_items - 1) & 1, abort_flag, p.err, false)) {
           ok = false;
         } else {
           bar_arrive_tx(bar(BQT), kQSmemChunks * kQChunkBytes);
@@ -265,16 +316,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ok = false;
           } else {
             if (phys < 0 && rank == 0) raise_flag(p.err, DCP_DEVERR_BLOCK_RANGE);
-            const int row = phys < 0 ? -kTile : phys * kTile;  // out of range: the copy reads zeros
-            // the pair copies each page once: each CTA fetches alternate boxes
-            // into both CTAs (one L2 read per box); every CTA's barrier
-            // expects the whole page
-            bar_arrive_tx(bar(BKV_FULL + s), kChunks * kKvChunkBytes);
-            for (int c = (int)rank; c < kChunks; c += 2)
-              tma_load_mc(sbase + kOffKv + s * kStageBytes + c * kKvChunkBytes, &p.tm_kv[g.shard], 64 * c, row,
-                          bar(BKV_FULL + s), 0x3);
+            if constexpr (F8) {
+              // one bulk copy of the page's codes (an unusable table entry
+              // copies nothing: the widening writes zeros for it)
+              if (phys < 0) {
+                bar_arrive(bar(BKV_FULL + s));
+              } else {
+                bar_arrive_tx(bar(BKV_FULL + s), kCodesPage);
+                bulk_load(sbase + kOffKv + s * kStage,
+                          static_cast<const unsigned char*>(p.sh.k[g.shard]) + (size_t)phys * kCodesPage, kCodesPage,
+                          bar(BKV_FULL + s));
+              }
+            } else {
+              const int row = phys < 0 ? -kTile : phys * kTile;  // out of range: the copy reads zeros
+              // the pair copies each page once: each CTA fetches alternate boxes
+              // into both CTAs (one L2 read per box); every CTA's barrier
+              // expects the whole page
+              bar_arrive_tx(bar(BKV_FULL + s), kChunks * kKvChunkBytes);
+              for (int c = (int)rank; c < kChunks; c += 2)
+                tma_load_mc(sbase + kOffKv + s * kStageBytes + c * kKvChunkBytes, &p.tm_kv[g.shard], 64 * c, row,
+                            bar(BKV_FULL + s), 0x3);
+            }
             if (kPrefetch > 0 && rank == 0 && phys_pf >= 0)
-              l2_prefetch(static_cast<const char*>(p.sh.k[g.shard]) + (size_t)phys_pf * kStageBytes, kStageBytes);
+              l2_prefetch(static_cast<const char*>(p.sh.k[g.shard]) + (size_t)phys_pf * kStage, kStage);
           }
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) { stop = true; break; }
@@ -283,7 +347,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ++n_items;
     }
     if (lane == 0 && *abort_flag) {  // copies in flight must land before the CTA may exit
-      if (n_items > 0) drain_bar(bar(BQT), (n_items - 1) & 1u);
+      if (!F8 && n_items > 0) drain_bar(bar(BQT), (n_items - 1) & 1u);
       // (the other CTA's copies into this one land on the same barriers; it
       // can be at most one page ahead, which may never complete here: the
       // poll bound ends that wait)
@@ -297,8 +361,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ready P.V enters the tensor pipe while a score is being issued instead
     // of waiting for all its 36 MMAs.
     {
-      const uint32_t id_s = idesc(128, 64, 0);
-      const uint64_t kdesc0 = sdesc(sbase + kOffKv, 0);
+      const uint32_t id_s = idesc(128, 64, 0, F8);
+      const uint64_t kdesc0 = sdesc(sbase + (F8 ? kOffF16 : kOffKv), 0);
       const uint64_t qdesc0 = sdesc(sbase + kOffQ, 0);
       auto n_tiles = [&](int k) {
         const ItemRec it = reinterpret_cast<const ItemRec*>(p.ws + p.L.items_off)[k];
@@ -310,16 +374,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t idle = 0;
       while (ks < k_end) {
         bool progressed = false;
-        if (!q_ready && bar_test_warp(bar(BQ_FULL), q_loads & 1u) && bar_test_warp(bar(BQT), q_loads & 1u)) {
+        if (!q_ready && bar_test_warp(bar(BQ_FULL), q_loads & 1u) && (F8 || bar_test_warp(bar(BQT), q_loads & 1u))) {
           q_ready = true;
           tc_fence_after();
         }
         const uint32_t s = g_s % kStages;
-        if (q_ready && bar_test_warp(bar(BKV_FULL + s), (g_s / kStages) & 1u) &&
-            (g_s == 0 || bar_test_warp(bar(BS_EMPTY), (g_s - 1) & 1u))) {
+        const bool page_in = F8 ? bar_test_warp(bar(BF_FULL), g_s & 1u)  // the widened page
+                                : bar_test_warp(bar(BKV_FULL + s), (g_s / kStages) & 1u);
+        if (q_ready && page_in && (g_s == 0 || bar_test_warp(bar(BS_EMPTY), (g_s - 1) & 1u))) {
           tc_fence_after();
           // descriptors advance by (byte offset >> 4) in their address field
-          const uint64_t kd = kdesc0 + (uint64_t)((s * kStageBytes) >> 4);
+          const uint64_t kd = kdesc0 + (F8 ? 0ull : (uint64_t)((s * kStageBytes) >> 4));
 #pragma unroll
           for (int kk = 0; kk < kKSteps; ++kk) {
             const uint64_t bdesc = kd + (uint64_t)((((kk >> 2) * kKvChunkBytes) + 32 * (kk & 3)) >> 4);
@@ -363,9 +428,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // the P.V of tile g - kStages, so this warp is never more than one phase
     // behind on either barrier and its parity waits are unambiguous.
     {
-      const uint32_t id_pv = idesc(128, 256, 1);
-      const uint64_t pdesc0 = sdesc(sbase + kOffKv + 4 * (1 - rank) * kKvChunkBytes, 0);
-      const uint64_t vdesc0 = sdesc(sbase + kOffKv + 4 * rank * kKvChunkBytes, kKvChunkBytes);
+      const uint32_t id_pv = idesc(128, 256, 1, F8);
+      const uint32_t pbase = sbase + (F8 ? kOffF16 : kOffKv);  // the page the MMAs read
+      const uint64_t pdesc0 = sdesc(pbase + 4 * (1 - rank) * kKvChunkBytes, 0);
+      const uint64_t vdesc0 = sdesc(pbase + 4 * rank * kKvChunkBytes, kKvChunkBytes);
       auto n_tiles = [&](int k) {
         const ItemRec it = reinterpret_cast<const ItemRec*>(p.ws + p.L.items_off)[k];
         return it.t1 - it.t0;
@@ -377,8 +443,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t s = g_p % kStages;
         if (bar_test_warp(bar(BP_FULL + s), (g_p / kStages) & 1u)) {
           tc_fence_after();
-          const uint64_t vd = vdesc0 + (uint64_t)((s * kStageBytes) >> 4);  // V dims of this CTA
-          const uint64_t pd = pdesc0 + (uint64_t)((s * kStageBytes) >> 4);  // P of this tile
+          const uint64_t soff = F8 ? 0ull : (uint64_t)((s * kStageBytes) >> 4);
+          const uint64_t vd = vdesc0 + soff;  // V dims of this CTA
+          const uint64_t pd = pdesc0 + soff;  // P of this tile
           int any_lo = 0;
 #pragma unroll
           for (int w = 0; w < kSoftmaxWarps; ++w) any_lo |= lo_flags[kSoftmaxWarps * s + w];
@@ -391,7 +458,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               mma_ss(tmem + kColO, pd + (uint64_t)((term * kPBytes + 32 * kt) >> 4),
                   vd + (uint64_t)((2048 * kt) >> 4), id_pv, (jp == 0 && term == 0 && kt == 0) ? 0 : 1);
           }
-          mma_commit_mc(bar(BKV_EMPTY + s), 0x3);  // the stage is free in both CTAs once both P.V finished
+          if (F8)
+            mma_commit(bar(BF_EMPTY));  // the widened page may be overwritten
+          else
+            mma_commit_mc(bar(BKV_EMPTY + s), 0x3);  // the stage is free in both CTAs once both P.V finished
           mma_commit(bar(BP_EMPTY + s));  // also tells softmax that this P.V finished
           if (++jp == ntp) {
             ++kp;
@@ -444,14 +514,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const uint4 v = qr[4 * c + i];
-            qv[4 * i] = v.x;
-            qv[4 * i + 1] = v.y;
-            qv[4 * i + 2] = v.z;
-            qv[4 * i + 3] = v.w;
+            qv[4 * i] = F8 ? bf16x2_as_f16x2(v.x) : v.x;
+            qv[4 * i + 1] = F8 ? bf16x2_as_f16x2(v.y) : v.y;
+            qv[4 * i + 2] = F8 ? bf16x2_as_f16x2(v.z) : v.z;
+            qv[4 * i + 3] = F8 ? bf16x2_as_f16x2(v.w) : v.w;
           }
           tmem_st16(tmem + lane_off + kColQ + 96 * e + 16 * c, qv);
         }
         tmem_wait_st();
+        if constexpr (F8) {
+          // query dims 384 + 96 e .. + 95 in fp16 into the shared-memory tail
+          // (128-byte swizzled rows of 64 dims, as the copy would lay them out)
+          const uint4* qt = reinterpret_cast<const uint4*>(p.q + ((size_t)g.b * kHeads + h) * kDk + 384 + 96 * e);
+#pragma unroll 4
+          for (int c = 0; c < 12; ++c) {
+            const uint4 v = qt[c];
+            const int d = 96 * e + 8 * c;  // dim - 384
+            const uint32_t a = sbase + kOffQ + (d >> 6) * kQChunkBytes + h * 128 +
+                               (((uint32_t)((d & 63) >> 3) ^ (uint32_t)(h & 7)) << 4);
+            st_shared_v4(a, bf16x2_as_f16x2(v.x), bf16x2_as_f16x2(v.y), bf16x2_as_f16x2(v.z), bf16x2_as_f16x2(v.w));
+          }
+          asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        }
       }
       tc_fence_before();
       bar_arrive(bar(BQ_FULL));
@@ -460,6 +544,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t gi = gt + j, s = gi % kStages;
         const int t = g.t0 + j;
         const int phys = tile_block(p, g, t);  // its latency hides behind the score wait
+        if constexpr (F8) {
+          // 0. widen the page's codes to fp16, exactly (E4M3 is a subset of
+          // fp16), into the page the MMAs read, once the previous page's P.V
+          // has finished with it; rows past the range (or of an unusable
+          // table entry) become zeros, so that no value can carry NaN bits
+          const int n_rows = phys < 0 ? 0 : min(kTile, g.hi - (g.lo + kTile * t));
+          if (gi >= 1 && !wait_warp(bar(BF_EMPTY), (gi - 1) & 1u, abort_flag, p.err, false)) { ok = false; break; }
+          if (!wait_warp(bar(BKV_FULL + s), (gi / kStages) & 1u, abort_flag, p.err, false)) { ok = false; break; }
+          // four threads per row (thread = row 4r + q), 16 codes per load:
+          // codes 16 g .. 16 g + 15 -> box g / 4, 16-byte chunks 2 (g % 4), +1
+          {
+            const int r = threadIdx.x >> 2, q4 = threadIdx.x & 3;
+            const uint32_t src = sbase + kOffKv + s * kStage + r * kDk;
+            const uint32_t dst = sbase + kOffF16 + r * 128;
+            const uint32_t sw = (uint32_t)(r & 7);
+            const bool live = r < n_rows;
+#pragma unroll 3
+            for (int i = 0; i < kDk / 64; ++i) {
+              const int g16 = q4 + 4 * i;  // 0 .. 35
+              uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+              if (live) {
+                const uint4 c = lds128_u32(src + 16 * g16);
+                e4m3x4_to_f16x4(c.x, w[0], w[1]);
+                e4m3x4_to_f16x4(c.y, w[2], w[3]);
+                e4m3x4_to_f16x4(c.z, w[4], w[5]);
+                e4m3x4_to_f16x4(c.w, w[6], w[7]);
+              }
+              const uint32_t box = dst + (g16 >> 2) * kKvChunkBytes;
+              const uint32_t ch = 2u * (uint32_t)(g16 & 3);
+              st_shared_v4(box + ((ch ^ sw) << 4), w[0], w[1], w[2], w[3]);
+              st_shared_v4(box + (((ch + 1) ^ sw) << 4), w[4], w[5], w[6], w[7]);
+            }
+          }
+          asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+          bar_arrive(bar(BF_FULL));
+          bar_arrive(bar(BKV_EMPTY + s));  // the codes' stage may be refilled
+        }
         // 1. scores of the tile: all 64 for the maximum, this warp's 32 for P
         if (!wait_warp(bar(BS_FULL), gi & 1u, abort_flag, p.err, false)) { ok = false; break; }
         tc_fence_after();
@@ -536,23 +657,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // itself is stored for every row on every tile: the P.V covers all
         // 128 rows, so when any warp asks for it, every row must be current.
         const bool any_lo = __any_sync(0xffffffffu, lsum > kLoFraction * l_half);
-        // 3. P into its stage (the score MMA that read those boxes has finished)
+        // 3. P into its stage (the score MMA that read those boxes has finished;
+        // F8: into the widened page, as fp16 terms)
         {
-          const uint32_t hrow = sbase + kOffKv + s * kStageBytes + 4 * (1 - rank) * kKvChunkBytes + h * 128;
+          const uint32_t hrow = (F8 ? sbase + kOffF16 : sbase + kOffKv + s * kStageBytes) +
+                                4 * (1 - rank) * kKvChunkBytes + h * 128;
           const uint32_t lrow = hrow + kPBytes;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const uint32_t chunk = (uint32_t)(4 * e + c);
             uint32_t hi[4], lo[4];
 #pragma unroll
-            for (int k2 = 0; k2 < 4; ++k2) split_p_bf16(sc[8 * c + 2 * k2], sc[8 * c + 2 * k2 + 1], hi[k2], lo[k2]);
+            for (int k2 = 0; k2 < 4; ++k2) {
+              if constexpr (F8)
+                split_p_f16(sc[8 * c + 2 * k2], sc[8 * c + 2 * k2 + 1], hi[k2], lo[k2]);
+              else
+                split_p_bf16(sc[8 * c + 2 * k2], sc[8 * c + 2 * k2 + 1], hi[k2], lo[k2]);
+            }
             st_shared_v4(hrow + ((chunk ^ (uint32_t)(h & 7)) << 4), hi[0], hi[1], hi[2], hi[3]);
             st_shared_v4(lrow + ((chunk ^ (uint32_t)(h & 7)) << 4), lo[0], lo[1], lo[2], lo[3]);
           }
           if (lane == 0) lo_flags[kSoftmaxWarps * s + warp] = any_lo ? 1 : 0;
         }
         // 4. V rows past the end of a partial tile may hold anything: zero them
-        if (n_valid < kTile) {
+        // (F8: the widening already wrote zeros there)
+        if (!F8 && n_valid < kTile) {
           const int rows = kTile - n_valid;
           const int tid = threadIdx.x;  // 0 .. kSoftmaxThreads-1
           for (int x = tid; x < rows * 4 * 8; x += kSoftmaxThreads) {
@@ -599,7 +728,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // (P.V products finish in issue order: the last one implies the others)
       if (!wait_warp(bar(BP_EMPTY + glast % kStages), (glast / kStages) & 1u, abort_flag, p.err, false)) break;
       tc_fence_after();
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const float inv = l_run > 0.f ? p.v_scale / l_run : 0.f;
       float* out;
       float* out_lse;
       if (g.out_row >= 0) {
@@ -656,7 +785,9 @@ bool latent_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_ro
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Co-resident clusters on the current device (0 on failure), cached.
+// Co-resident clusters on the current device for the bf16 (F8 = false) or
+// the 8-bit kernel (0 on failure), cached.
+template <bool F8>
 int mla_clusters() {
   static std::mutex mu;
   static int cache[64] = {};
@@ -664,7 +795,8 @@ int mla_clusters() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
   if (cache[dev] > 0) return cache[dev];
-  if (cudaFuncSetAttribute(mla_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+  constexpr int kSmem = MlaLayout<F8>::kSmemBytes;
+  if (cudaFuncSetAttribute(mla_partial_kernel<F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
       cudaSuccess)
     return 0;
   int sms = 0;
@@ -672,7 +804,7 @@ int mla_clusters() {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = kSmem;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
   attr.val.clusterDim.x = 2;
@@ -681,7 +813,7 @@ int mla_clusters() {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, mla_partial_kernel, &cfg) != cudaSuccess || n <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&n, mla_partial_kernel<F8>, &cfg) != cudaSuccess || n <= 0) {
     cudaGetLastError();
     n = sms / 2;
   }
@@ -691,17 +823,22 @@ int mla_clusters() {
 
 }  // namespace
 
-int mla_ctas(const dcp_attn_desc&, const DeviceInfo&) { return mla_clusters(); }
+int mla_ctas(const dcp_attn_desc& d, const DeviceInfo&) {
+  return d.kv_dtype == DCP_KV_FP8_E4M3 ? mla_clusters<true>() : mla_clusters<false>();
+}
 
 cudaError_t launch_mla(const dcp_attn_desc& d, const void* q, const ShardSet& sh, const RangeSpec& rs,
                        float* o_parts, float* lses, void* ws, const WsLayout& L, int n_ctas, int32_t* err,
                        cudaStream_t st) {
-  if (n_ctas <= 0 || mla_clusters() <= 0) return cudaErrorNotSupported;
+  const bool f8 = d.kv_dtype == DCP_KV_FP8_E4M3;
+  if (n_ctas <= 0 || (f8 ? mla_clusters<true>() : mla_clusters<false>()) <= 0) return cudaErrorNotSupported;
   MlaParams p;
   memset(&p, 0, sizeof(p));
-  if (!latent_map(&p.tm_q, q, (uint64_t)rs.B * kHeads, kHeads)) return cudaErrorNotSupported;
-  for (int i = 0; i < rs.N; ++i)
-    if (!latent_map(&p.tm_kv[i], sh.k[i], (uint64_t)sh.nblk[i] * kTile, kTile)) return cudaErrorNotSupported;
+  if (!f8) {  // the 8-bit kernel copies its pages with plain bulk copies and loads its query itself
+    if (!latent_map(&p.tm_q, q, (uint64_t)rs.B * kHeads, kHeads)) return cudaErrorNotSupported;
+    for (int i = 0; i < rs.N; ++i)
+      if (!latent_map(&p.tm_kv[i], sh.k[i], (uint64_t)sh.nblk[i] * kTile, kTile)) return cudaErrorNotSupported;
+  }
   p.sh = sh;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.ws = static_cast<const char*>(ws);
@@ -711,8 +848,12 @@ cudaError_t launch_mla(const dcp_attn_desc& d, const void* q, const ShardSet& sh
   p.err = err;
   p.B = rs.B;
   p.qlen = rs.qlen;
-  p.sl2 = d.scale * kLog2e;
-  mla_partial_kernel<<<2 * n_ctas, kThreads, kSmemBytes, st>>>(p);
+  p.sl2 = d.scale * kLog2e * (f8 ? d.k_scale : 1.f);
+  p.v_scale = f8 ? d.v_scale : 1.f;
+  if (f8)
+    mla_partial_kernel<true><<<2 * n_ctas, kThreads, MlaLayout<true>::kSmemBytes, st>>>(p);
+  else
+    mla_partial_kernel<false><<<2 * n_ctas, kThreads, MlaLayout<false>::kSmemBytes, st>>>(p);
   return cudaGetLastError();
 }
 

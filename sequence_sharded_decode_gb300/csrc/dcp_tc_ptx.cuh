@@ -118,6 +118,13 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
+// Plain bulk copy of `bytes` contiguous bytes (a multiple of 16, both
+// addresses 16-byte aligned) into this CTA's shared memory.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
 // Pull `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
 __device__ __forceinline__ void l2_prefetch(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
@@ -134,10 +141,10 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo) {
   d |= 2ull << 61;   // 128-byte swizzle
   return d;
 }
-// Instruction descriptor, kind::f16: bf16 A/B, fp32 accumulate.
-__host__ __device__ constexpr uint32_t idesc(int M, int N, int b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn_major << 16) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor, kind::f16: bf16 A/B (fp16 with f16 set), fp32 accumulate.
+__host__ __device__ constexpr uint32_t idesc(int M, int N, int b_mn_major, bool f16 = false) {
+  return (1u << 4) | (f16 ? 0u : (1u << 7) | (1u << 10)) | ((uint32_t)b_mn_major << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 // D (+)= A . B with A and B in shared memory; the whole warp calls, one elected lane issues
 __device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id, int accumulate) {

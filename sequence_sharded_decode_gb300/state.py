@@ -38,8 +38,9 @@ class DecodeState:
         self.tables_host = inputs.block_tables(seed_t, blocks, wl.capacity_factor)
         self.shards = []
         for cap, tab in self.tables_host:
-            if wl.kind == configs.MLA:
-                k = torch.empty((cap, wl.block_size, wl.dk), dtype=torch.bfloat16, device=device)
+            if wl.kind == configs.MLA:  # one latent row per token (E4M3 codes for the 8-bit cache)
+                k = torch.empty((cap, wl.block_size, wl.dk), dtype=torch.uint8 if self.f8 else torch.bfloat16,
+                                device=device)
                 v = None
             elif self.f8:  # E4M3 codes; the values of a block stored transposed (dims x tokens)
                 k = torch.empty((cap, wl.kv_heads, wl.block_size, wl.dk), dtype=torch.uint8, device=device)
@@ -50,7 +51,8 @@ class DecodeState:
             if canary is not None:
                 if self.f8:
                     k.fill_(canary & 0xFF)
-                    v.fill_(canary & 0xFF)
+                    if v is not None:
+                        v.fill_(canary & 0xFF)
                 else:
                     k.view(torch.int16).fill_(canary)
                     if v is not None:
@@ -96,6 +98,8 @@ class DecodeState:
         if wl.kind == configs.MLA:
             lat = inputs.kv_tokens(wl.seed, inputs.STREAM_LATENT, b, t, 1, wl.dk, g, chunk=1 << 18)
             lat = inputs.plant_needles(lat.view(-1, wl.dk), b, t, self.q0.to(g), self.needles, wl.q_heads)
+            if self.f8:  # the cache holds the E4M3 codes of the same draws
+                lat = inputs.e4m3_codes(lat)
             return lat.to(self.device), None
         k = inputs.kv_tokens(wl.seed, inputs.STREAM_K, b, t, wl.kv_heads, wl.dk, g, chunk=1 << 16)
         k = inputs.plant_needles(k, b, t, self.q0.to(g), self.needles, wl.q_heads)

@@ -42,6 +42,9 @@ def oracle_kv(wl: configs.Workload, b: int, L: int):
         if plan_b:
             q = inputs.query(wl.seed, np.arange(b + 1), wl.q_heads, wl.dk, stream=inputs.STREAM_Q_MLA)
             lat = inputs.plant_needles(lat.view(L, wl.dk), bids, pos, q, plan_b, wl.q_heads).view(L, 1, wl.dk)
+        if wl.kv_dtype == "fp8":  # one row of codes: key = k_scale * decode, value = v_scale * decode[:dv]
+            codes = inputs.e4m3_codes(lat).numpy()
+            return O.fp8_kv(codes, codes[:, :, :wl.dv], wl.k_scale, wl.v_scale)
         lat = f64(lat)
         return lat, lat[:, :, :wl.dv]
     k = inputs.sequence_kv(wl.seed, inputs.STREAM_K, b, 0, L, wl.kv_heads, wl.dk)

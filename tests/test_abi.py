@@ -182,12 +182,18 @@ def test_fp8_cache_validation(lib):
         (dict(kv_dtype=dcp.DCP_KV_FP8_E4M3, k_scale=float("inf")), dcp.DCP_ERR_INVALID_ARG),
         (dict(kv_dtype=dcp.DCP_KV_FP8_E4M3, v_scale=float("nan")), dcp.DCP_ERR_INVALID_ARG),
         (dict(kind=dcp.DCP_KIND_MLA, num_q_heads=128, num_kv_heads=1, head_dim_k=576, head_dim_v=512,
-              block_size=64, kv_dtype=dcp.DCP_KV_FP8_E4M3), dcp.DCP_ERR_UNSUPPORTED),
+              block_size=64, kv_dtype=dcp.DCP_KV_FP8_E4M3, k_scale=0.0), dcp.DCP_ERR_INVALID_ARG),
     ]:
         d = _desc(**kw).c()
         assert lib.dcp_kv_append(ctypes.byref(d), ctypes.byref(good), 1, 16, 1, None, 16, 16, 16, 1, None,
                                  None) == status, kw
         assert lib.dcp_workspace_size(ctypes.byref(d), 1, 1) == 0
+    # the MLA latent cache takes 8-bit codes too (one row per token, no value pool)
+    mla = _desc(kind=dcp.DCP_KIND_MLA, num_q_heads=128, num_kv_heads=1, head_dim_k=576, head_dim_v=512,
+                block_size=64, kv_dtype=dcp.DCP_KV_FP8_E4M3, k_scale=0.5, v_scale=2.0).c()
+    mla_shard = dcp._Shard(16, None, 4, 16, 2)
+    assert lib.dcp_kv_append(ctypes.byref(mla), ctypes.byref(mla_shard), 1, 16, 2, 16, 16, 16, None, 0, None,
+                             None) == dcp.DCP_OK
 
 
 def test_attention_all_validation(lib):

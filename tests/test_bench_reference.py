@@ -42,9 +42,7 @@ def test_reference_arm_prints_one_contract_line(args):
         assert d["config"]["kv_cache"].startswith("fp8")
 
 
-def test_fp8_is_for_gqa_only():
-    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
-    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
-                          "mla_decode", "--kv-dtype", "fp8"], capture_output=True, text=True, env=env, timeout=120,
-                         cwd=ROOT)
-    assert out.returncode != 0 and "GQA" in out.stderr
+def test_fp8_mla_reference_arm():
+    # the 8-bit latent cache: one row of codes per token, key and value decoded from it
+    d = _run("--workload", "mla_decode", "--batch", "1", "--kv-dtype", "fp8")
+    assert d["impl"] == "reference" and d["value"] > 0 and d["config"]["kv_cache"].startswith("fp8")

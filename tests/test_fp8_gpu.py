@@ -94,3 +94,59 @@ def test_fp8_full_size_gqa_mid_sampled():
     st = DecodeState(wl)
     st.step()
     _check(st, wl, seqs=[0, 13, 31])
+
+
+# The MLA latent cache over 8-bit codes: one row of 576 codes per token; the
+# key is k_scale x the decoded row, the value v_scale x its first 512 entries.
+MLA_RAGGED = dict(ctx_kind="lognormal", median=900, sigma=1.0, ctx_lo=0, ctx_hi=5000)
+MLA_CASES = [
+    ("mla_decode", dict(batch=2, ctx_kind="fixed", ctx_fixed=300, shards=4, **F8)),
+    ("mla_decode", dict(batch=1, ctx_kind="fixed", ctx_fixed=63, shards=1, **F8)),      # exactly one page
+    ("mla_decode", dict(batch=1, ctx_kind="fixed", ctx_fixed=0, shards=2, **F8)),       # one token
+    ("mla_decode", dict(batch=5, shards=8, **MLA_RAGGED, **F8)),                        # ragged, empty shards
+    ("mla_high_concurrency", dict(batch=6, shards=8, **MLA_RAGGED, **F8)),              # fragmented pools
+    ("mla_decode", dict(batch=3, ctx_kind="fixed", ctx_fixed=3000, shards=4, needles=3, **F8)),
+    ("mla_decode", dict(batch=2, ctx_kind="fixed", ctx_fixed=5000, shards=3, scale=1.0, **F8)),  # peaky
+    ("mla_decode", dict(batch=2, ctx_kind="fixed", ctx_fixed=1200, shards=3, k_scale=0.5, v_scale=2.0, **F8)),
+    ("mla_decode", dict(batch=2, ctx_kind="fixed", ctx_fixed=900, shards=2, scale=-0.0417, k_scale=0.25,
+                        v_scale=0.125, **F8)),
+]
+
+
+@pytest.mark.parametrize("name,over", MLA_CASES)
+def test_fp8_mla_step_matches_oracle(name, over):
+    wl = configs.get(name).with_(**over)
+    st = DecodeState(wl)
+    st.step()
+    _check(st, wl)
+    # the fused call on the same state
+    st.o.fill_(float("nan"))
+    st.attention()
+    torch.cuda.synchronize()
+    o = st.o.cpu().numpy()
+    lse = st.lse.cpu().numpy()
+    for b in range(wl.batch):
+        ro, rl, _, _ = oracle_sequence(wl, b, int(st.ctx[b]) + 1, O.shard_starts([st.ctx[b]], wl.shards)[0])
+        assert_close(o[b], ro, f"fused O[b={b}]")
+        assert_lse_close(lse[b], rl, f"fused LSE[b={b}]")
+
+
+def test_fp8_mla_codes_land_bit_exactly():
+    wl = configs.get("mla_decode").with_(batch=2, ctx_kind="fixed", ctx_fixed=300, shards=3, **F8)
+    st = DecodeState(wl, canary=0x55)
+    st.append()
+    torch.cuda.synchronize()
+    for b in range(wl.batch):
+        L = int(st.ctx[b]) + 1
+        lat = inputs.e4m3_codes(inputs.sequence_kv(wl.seed, inputs.STREAM_LATENT, b, 0, L, 1, wl.dk)).numpy()
+        for t in (0, 1, L // 2, L - 2, L - 1):
+            i, phys, slot = O.paged_slot(int(t), st.starts_host[b], [tab for _, tab in st.tables_host], b,
+                                         wl.block_size)
+            assert np.array_equal(st.shards[i].k_pool[phys, slot, :].cpu().numpy(), lat[t, 0]), (b, t)
+
+
+def test_fp8_mla_long_sampled():
+    wl = configs.get("mla_long").with_(**F8)
+    st = DecodeState(wl)
+    st.step()
+    _check(st, wl, seqs=[0, 7])

@@ -334,9 +334,16 @@ def run_ours(args, wl):
             dist.barrier()
         torch.cuda.synchronize()
 
-    bytes_ = st.step_bytes()
-    step_bytes = sum(bytes_.values())
     fused = not args.two_calls
+    bytes_ = st.step_bytes(fused)
+    step_bytes = sum(bytes_.values())
+    # the dominant kernel's call, timed alone for the roofline: MLA's one call
+    # (plan + attention with the shards merged on chip) where the step uses it,
+    # else the partial call (plan + attention + combine of split ranges)
+    one_call_mla = fused and wl.kind == 1
+    call_bytes = bytes_["attention"] if one_call_mla else st.step_bytes(False)["partial"]
+    call_name = ("dcp_attention_all (plan + attention, shards merged in the kernel), timed alone" if one_call_mla
+                 else "dcp_decode_partial_all (plan + attention + combine), timed alone")
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             st.step(stream, fused)
@@ -352,11 +359,13 @@ def run_ours(args, wl):
             for i in range(K):
                 st.step(stream, fused)
             end.record(stream)
-            # the dominant kernel's call alone (plan + attention + combine of
-            # split ranges), timed on the same stream for the roofline
+            # the dominant kernel's call alone, on the same stream
             for i in range(K):
                 ev_p0[i].record(stream)
-                st.partial(stream)
+                if one_call_mla:
+                    st.attention(stream)
+                else:
+                    st.partial(stream)
                 ev_p1[i].record(stream)
         stream.synchronize()
     barrier()
@@ -437,7 +446,6 @@ def run_ours(args, wl):
     if rank == 0:
         peak, peak_kind = _peaks()
         value = whole_job_gbs(world, step_bytes, ms)
-        call_bytes = bytes_["partial"]
         achieved = call_bytes / (partial_ms * 1e-3) / 1e9
         kern = "dcp_mla.cu" if wl.kind == 1 else "dcp_gqa.cu"
         line = {
@@ -449,18 +457,20 @@ def run_ours(args, wl):
             "config": _workload_config(wl, st, args.q_len) | {"parallelism": f"replicas x{world}"},
             "hbm_frac_of_peak": round(value / world / peak, 4),
             "tokens_per_s_per_layer": round(world * wl.batch * args.q_len / (ms * 1e-3), 1),
-            "roofline": {"bound": "hbm", "kernel": "dcp_decode_partial_all (plan + attention + combine), timed alone",
+            "roofline": {"bound": "hbm", "kernel": call_name,
                          "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "traffic": (_traffic_for(kern, wl.name + ("_fp8" if wl.kv_dtype == "fp8" else ""))
                                      if args.q_len == 1 else None),
                          "algorithmic_bytes_per_launch": call_bytes},
             "step_bytes": bytes_,
-            "step_calls": ("dcp_kv_append, dcp_attention_all (partial attention + one-pass merge)" if fused
+            "step_calls": ("dcp_kv_append, dcp_attention_all (partial attention, shards merged in the kernel)"
+                           if one_call_mla else
+                           "dcp_kv_append, dcp_attention_all (partial attention + one-pass merge)" if fused
                            else "dcp_kv_append, dcp_decode_partial_all, dcp_merge"),
             "e2e": {"value": round(whole_job_gbs(world, step_bytes, e2e_ms), 2), "unit": "GB/s",
                     "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": (4 if fused else 5) * K,
+            "gpu_launches": (3 if one_call_mla else 4 if fused else 5) * K,
             "clocks": clocks,
         }
         if args.q_len > 1:

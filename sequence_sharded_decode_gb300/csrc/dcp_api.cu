@@ -10,13 +10,14 @@ namespace dcp {
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-WsLayout ws_layout(int n_lanes, int max_ctas, int rows_per_lane, int dv) {
+WsLayout ws_layout(int n_lanes, int max_ctas, int rows_per_lane, int dv, int n_groups) {
   WsLayout L;
   L.max_lanes = n_lanes;
   L.max_ctas = max_ctas;
   L.max_items = n_lanes + max_ctas;
   L.max_tmp = 2 * max_ctas;  // a lane cut k ways holds k-1 CTA boundaries, k <= 2(k-1)
   L.rows_per_lane = rows_per_lane;
+  L.max_groups = n_groups;
   size_t off = sizeof(WsHeader);
   L.lanes_off = off;
   off = align256(off + sizeof(LaneRec) * (size_t)n_lanes);
@@ -24,6 +25,8 @@ WsLayout ws_layout(int n_lanes, int max_ctas, int rows_per_lane, int dv) {
   off = align256(off + sizeof(ItemRec) * (size_t)L.max_items);
   L.cta_off = off;
   off = align256(off + sizeof(int) * (size_t)(max_ctas + 1));
+  L.grp_off = off;
+  off = align256(off + sizeof(GroupRec) * (size_t)n_groups);
   L.tmp_o_off = off;
   off = align256(off + sizeof(float) * (size_t)L.max_tmp * rows_per_lane * dv);
   L.tmp_lse_off = off;
@@ -172,7 +175,7 @@ static int layout_for(const dcp_attn_desc& d, int B, int N, const Path& p, WsLay
   if (c <= 0) return DCP_ERR_CUDA;
   const long long lanes = (long long)B * N * p.lg.lanes_per_unit;
   if (lanes > (1 << 26)) return DCP_ERR_SHAPE;
-  *L = ws_layout((int)lanes, c, p.rows_per_lane, d.head_dim_v);
+  *L = ws_layout((int)lanes, c, p.rows_per_lane, d.head_dim_v, d.kind == DCP_KIND_MLA ? B : 0);
   *n_ctas = c;
   return DCP_OK;
 }
@@ -191,14 +194,20 @@ static int run_partial(const dcp_attn_desc* desc, const Path& path, const void* 
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < L.total) return DCP_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const LaneGeom& g = path.lg;
-  if (launch_plan(rs, g.lanes_per_unit, g.tile, n_ctas, ws, L, st) != cudaSuccess) return DCP_ERR_CUDA;
+  // MLA with o: the attention kernel merges the shards itself
+  const bool mla_merge = d.kind == DCP_KIND_MLA && o != nullptr;
+  if (launch_plan(rs, g.lanes_per_unit, g.tile, n_ctas, ws, L, d.kind == DCP_KIND_MLA, st) != cudaSuccess)
+    return DCP_ERR_CUDA;
   cudaError_t e;
-  if (d.kind == DCP_KIND_MLA) e = launch_mla(d, q, sh, rs, o_parts, lses, ws, L, n_ctas, err, st);
+  if (d.kind == DCP_KIND_MLA)
+    e = launch_mla(d, q, sh, rs, o_parts, lses, ws, L, n_ctas, err, st, mla_merge ? o : nullptr, lse_out);
   else if (path.tc) e = launch_gqa_tc(d, q, sh, rs, o_parts, lses, ws, L, n_ctas, err, st);
   else e = launch_gqa(d, q, sh, rs, o_parts, lses, ws, L, n_ctas, err, st);
   if (e == cudaErrorNotSupported) return DCP_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return DCP_ERR_CUDA;
-  if (o) {
+  if (mla_merge) {
+    // nothing left: the rows are merged
+  } else if (o) {
     if (launch_combine_merge(d, g, rs, ws, L, o_parts, lses, o, lse_out, st) != cudaSuccess) return DCP_ERR_CUDA;
   } else if (launch_combine(d, g, rs, L.max_lanes, ws, L, o_parts, lses, st) != cudaSuccess) {
     return DCP_ERR_CUDA;

@@ -10,6 +10,15 @@
 // one item is written straight to the shard's partial output; a lane split
 // over several items is written as per-item partials to the workspace and
 // merged by the combine kernel (same LSE merge as across shards).
+//
+// MLA lays the lanes out row group by row group instead -- the N shard lanes
+// of a query row next to each other -- so consecutive items of a CTA pair
+// share their query. Its one-call path (partial attention and merge together)
+// then carries one online softmax through the consecutive shards of a row
+// group, so the shards are merged on chip: a row group whose tiles one CTA run
+// covers is written straight to the output; one that a CTA boundary cuts
+// leaves one *piece* per run in the workspace, and the CTA that writes the
+// last piece merges them.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -68,6 +77,15 @@ struct ItemRec {     // 16 bytes
   int out_row;       // >= 0: workspace partial row; -1: write the lane's output directly
 };
 
+struct GroupRec {    // 32 bytes: one query row group of the one-call MLA path
+  int pieces;        // CTA runs its tiles span (0: no tokens in any shard)
+  int tmp_begin;     // first workspace partial row if pieces > 1
+  int first_cta;     // CTA run of piece 0
+  int pad;
+  int cnt[2];        // pieces written, per CTA of the pair (zeroed by the plan)
+  int pad2[2];
+};
+
 struct WsHeader {
   int n_items;
   int n_lanes;
@@ -77,13 +95,14 @@ struct WsHeader {
 };
 
 struct WsLayout {
-  size_t lanes_off, items_off, cta_off, tmp_o_off, tmp_lse_off, total;
-  int max_lanes, max_items, max_ctas, max_tmp, rows_per_lane;
+  size_t lanes_off, items_off, cta_off, grp_off, tmp_o_off, tmp_lse_off, total;
+  int max_lanes, max_items, max_ctas, max_tmp, rows_per_lane, max_groups;
 };
 
 // Workspace layout for n_lanes lanes, up to max_ctas work CTAs, rows_per_lane
-// query heads per lane and dv-wide outputs.
-WsLayout ws_layout(int n_lanes, int max_ctas, int rows_per_lane, int dv);
+// query heads per lane, dv-wide outputs and n_groups group records (the row
+// groups of the one-call MLA path; 0 where unused).
+WsLayout ws_layout(int n_lanes, int max_ctas, int rows_per_lane, int dv, int n_groups);
 
 // Per-device launch facts (cached).
 struct DeviceInfo {
@@ -102,17 +121,21 @@ struct LaneGeom {
 LaneGeom lane_geom(const dcp_attn_desc& d);
 
 // Kernel launchers (return the launch's cudaError_t).
+// group_order: lay the lanes out row group by row group and fill the group
+// records (MLA); otherwise shard by shard.
 cudaError_t launch_plan(const RangeSpec& rs, int lanes_per_unit, int tile, int n_ctas,
-                        void* ws, const WsLayout& L, cudaStream_t st);
+                        void* ws, const WsLayout& L, bool group_order, cudaStream_t st);
 cudaError_t launch_gqa(const dcp_attn_desc& d, const void* q, const ShardSet& sh, const RangeSpec& rs,
                        float* o_parts, float* lses, void* ws, const WsLayout& L, int n_ctas,
                        int32_t* err, cudaStream_t st);
 // Query tokens that share each K/V tile in the GQA kernel (1, 2 or 4).
 int gqa_team(int qlen);
 int gqa_ctas(const dcp_attn_desc& d, const DeviceInfo& di, int team);
+// o non-NULL: the one-call path (plan laid out with group_order): the
+// merged rows go to o / lse_out (NULL allowed) and o_parts / lses are unused.
 cudaError_t launch_mla(const dcp_attn_desc& d, const void* q, const ShardSet& sh, const RangeSpec& rs,
                        float* o_parts, float* lses, void* ws, const WsLayout& L, int n_ctas,
-                       int32_t* err, cudaStream_t st);
+                       int32_t* err, cudaStream_t st, float* o = nullptr, float* lse_out = nullptr);
 int mla_ctas(const dcp_attn_desc& d, const DeviceInfo& di);
 // Many query rows per KV head (GQA, head dim 128, bf16 cache, q_len * g >= 48):
 // 128-row lanes of 128/g tokens x g heads on the tcgen05 tensor cores.

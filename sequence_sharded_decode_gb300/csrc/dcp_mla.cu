@@ -61,6 +61,19 @@
 // phases are observed in order and never more than one phase late, so parity
 // waits are unambiguous; every wait is bounded: on expiry the kernel raises
 // DCP_DEVERR_TIMEOUT, stops all roles, drains what it issued and frees TMEM.
+//
+// One-call path (o non-NULL; step 3 joined to step 2, "Inference Systems
+// Infrastructure Notes (7): DCP", section 3: intermediate results stay in
+// reused buffers -- here, on chip): the plan lays each query row group's N
+// shard lanes next to each other, and a CTA pair whose run holds several
+// shards of a row group carries one online softmax through them -- the
+// running maximum, row sums and O simply continue from one shard's tiles to
+// the next, which is the LSE reweighting of the merge done as it goes, and the
+// query stays in place. A row group whose tiles lie in one CTA run is written
+// to o directly; one cut by a run boundary leaves one normalised piece (and
+// its LSE) per run in the workspace, each CTA then counts its piece with an
+// atomic, and the CTA whose count completes the group merges the pieces of
+// its value dims (the same reweighting) into o. No CTA ever waits for another.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -105,7 +118,7 @@ constexpr int kCodesPage = kTile * kDk;          // 8-bit cache: one page of E4M
 // one bulk copy each, no multicast), and the softmax warps widen each page,
 // exactly, into one fp16 page laid out like the bf16 boxes (kOffF16), which
 // the fp16 MMAs read; its P then lives in that page's dead boxes.
-constexpr int kNumBars = 21;
+constexpr int kNumBars = 23;
 template <bool F8>
 struct MlaLayout {
   static constexpr int kStage = F8 ? kCodesPage : kStageBytes;  // one ring stage
@@ -114,7 +127,8 @@ struct MlaLayout {
   static constexpr int kOffBar = kOffQ + kQSmemChunks * kQChunkBytes;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag, residual votes (per stage)
   static constexpr int kOffLx = kOffMisc + 128;            // row-sum halves exchanged at the end of an item
-  static constexpr int kSmemBytes = kOffLx + 2 * kHeads * 4 + 1024;  // slack to align the base to 1024
+  static constexpr int kOffMw = kOffLx + 2 * kHeads * 4;   // one-call path: merge weights [8 warps][16][32]
+  static constexpr int kSmemBytes = kOffMw + kSoftmaxWarps * 16 * 32 * 4 + 1024;  // slack to align the base to 1024
 };
 
 // barrier slots
@@ -127,8 +141,10 @@ constexpr int BQ_FULL = 0, BQ_EMPTY = 1, BS_FULL = 2, BS_EMPTY = 3, BP_EMPTY = 4
               BDRAIN2 = BXCH + 4, BP_FULL = 16,  // BP_FULL + stage: the tile's P is in its stage
               BQT = BP_FULL + kStages,           // the copy of the query tail landed
               BF_FULL = BQT + 1,                 // F8: the widened page is in place
-              BF_EMPTY = BQT + 2;                // F8: the widened page's P.V finished
-static_assert(BDRAIN2 + 1 <= BP_FULL && BF_EMPTY + 1 <= kNumBars, "barrier slots");
+              BF_EMPTY = BQT + 2,                // F8: the widened page's P.V finished
+              BPC = BQT + 3,                     // one-call path: every softmax thread's piece rows are out
+              BGO = BQT + 4;                     // one-call path: the piece is counted (merge or not)
+static_assert(BDRAIN2 + 1 <= BP_FULL && BGO + 1 <= kNumBars, "barrier slots");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;       // 256 columns: O_r, fp32
@@ -157,6 +173,8 @@ struct MlaParams {
   WsLayout L;
   float* o_parts;
   float* lses;
+  float* o;        // one-call path: merged rows [B][128][512] (NULL otherwise)
+  float* lse_out;  // one-call path: merged LSEs (may be NULL)
   int32_t* err;
   int B;     // query rows: sequences x qlen
   int qlen;  // query tokens per sequence (block-table row = query row / qlen)
@@ -183,6 +201,177 @@ __device__ __forceinline__ ItemGeom item_geom(const MlaParams& p, int k) {
   g.start = ln.start;
   return g;
 }
+// Item k has the query rows of item k - 1 (the same row group, next shard:
+// the plan lays a row group's shard lanes next to each other), so the query
+// already in place serves it.
+__device__ __forceinline__ bool same_rows(const MlaParams& p, int k, int k_begin) {
+  if (k <= k_begin) return false;
+  const ItemRec* items = reinterpret_cast<const ItemRec*>(p.ws + p.L.items_off);
+  return items[k].lane % p.B == items[k - 1].lane % p.B;
+}
+// One-call path: item k also carries on the online softmax of item k - 1
+// instead of starting afresh.
+__device__ __forceinline__ bool continues(const MlaParams& p, int k, int k_begin) {
+  return p.o != nullptr && same_rows(p, k, k_begin);
+}
+
+// One-call path: the CTA that completed row group rg's piece count merges the
+// pieces' value dims [256 rank, 256 rank + 256) into o (the LSE reweighting:
+// M = max LSE_i, w_i = e^(LSE_i - M), O = sum w_i O_i / sum w_i, LSE = M +
+// ln sum w_i). The 256 softmax threads: warp w takes heads 16 w .. 16 w + 15,
+// lane l columns 4l .. 4l + 3 and 128 + 4l ..; loads bypass L1 (the pieces
+// were written by other SMs). The merge sits at the end of the CTAs' runs,
+// where its dependent L2 round trips are the cost: the weights of all 16 heads
+// come from one round of loads (lane k: piece k's LSEs) and wait in shared
+// memory, and each head's pieces (or four heads' few pieces) are loaded in one
+// batch.
+constexpr int kMergeFast = 32;  // pieces whose weights fit the shared-memory table
+constexpr int kMergeBatch = 12; // pieces (x heads) loaded per round trip
+
+template <int HB>  // heads per batch: pieces per head <= kMergeBatch / HB
+__device__ __forceinline__ void merge_rows(const MlaParams& p, const float* tmp_o, int rg, int tmp_begin, int n,
+                                           uint32_t rank, int h0, int lane, const float* wt) {
+  constexpr int KB = kMergeBatch / HB;
+#pragma unroll 1
+  for (int i0 = 0; i0 < 16; i0 += HB) {
+    float4 a0[HB], a1[HB];
+#pragma unroll
+    for (int hb = 0; hb < HB; ++hb) a0[hb] = a1[hb] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+    for (int k0 = 0; k0 < n; k0 += KB) {
+      float4 v0[HB][KB], v1[HB][KB];
+#pragma unroll
+      for (int hb = 0; hb < HB; ++hb)
+#pragma unroll
+        for (int u = 0; u < KB; ++u) {
+          const int k = k0 + u;
+          v0[hb][u] = v1[hb][u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (k < n) {
+            const float4* src = reinterpret_cast<const float4*>(
+                tmp_o + ((size_t)(tmp_begin + k) * kHeads + h0 + i0 + hb) * kDv + 256 * rank);
+            v0[hb][u] = __ldcg(src + lane);
+            v1[hb][u] = __ldcg(src + 32 + lane);
+          }
+        }
+#pragma unroll
+      for (int hb = 0; hb < HB; ++hb)
+#pragma unroll
+        for (int u = 0; u < KB; ++u) {
+          const int k = k0 + u;
+          const float w = k < n ? wt[(i0 + hb) * kMergeFast + k] : 0.f;
+          a0[hb].x = fmaf(w, v0[hb][u].x, a0[hb].x);
+          a0[hb].y = fmaf(w, v0[hb][u].y, a0[hb].y);
+          a0[hb].z = fmaf(w, v0[hb][u].z, a0[hb].z);
+          a0[hb].w = fmaf(w, v0[hb][u].w, a0[hb].w);
+          a1[hb].x = fmaf(w, v1[hb][u].x, a1[hb].x);
+          a1[hb].y = fmaf(w, v1[hb][u].y, a1[hb].y);
+          a1[hb].z = fmaf(w, v1[hb][u].z, a1[hb].z);
+          a1[hb].w = fmaf(w, v1[hb][u].w, a1[hb].w);
+        }
+    }
+#pragma unroll
+    for (int hb = 0; hb < HB; ++hb) {
+      float4* dst = reinterpret_cast<float4*>(p.o + ((size_t)rg * kHeads + h0 + i0 + hb) * kDv + 256 * rank);
+      dst[lane] = a0[hb];
+      dst[32 + lane] = a1[hb];
+    }
+  }
+}
+
+__device__ __noinline__ void merge_pieces(const MlaParams& p, int rg, int tmp_begin, int n, uint32_t rank, int warp,
+                                          int lane, float* mw) {
+  const float* tmp_o = reinterpret_cast<const float*>(p.ws + p.L.tmp_o_off);
+  const float* tmp_lse = reinterpret_cast<const float*>(p.ws + p.L.tmp_lse_off);
+  const int h0 = 16 * warp;
+  if (n <= kMergeFast) {
+    // lane k: piece k's LSEs of the warp's 16 heads (one round of loads)
+    float lv[16];
+    if (lane < n) {
+      const float4* src = reinterpret_cast<const float4*>(tmp_lse + (size_t)(tmp_begin + lane) * kHeads + h0);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float4 v = __ldcg(src + c);
+        lv[4 * c] = v.x;
+        lv[4 * c + 1] = v.y;
+        lv[4 * c + 2] = v.z;
+        lv[4 * c + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) lv[i] = -INFINITY;
+    }
+    float* wt = mw + warp * 16 * kMergeFast;  // [head][piece]: normalised weights
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float M = lv[i];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      const float w = (M == -INFINITY || lv[i] == -INFINITY) ? 0.f : expf(lv[i] - M);
+      float ws = w;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+      wt[i * kMergeFast + lane] = ws > 0.f ? w / ws : 0.f;
+      if (rank == 0 && lane == 0 && p.lse_out)
+        p.lse_out[(size_t)rg * kHeads + h0 + i] = ws > 0.f ? M + logf(ws) : -INFINITY;
+    }
+    __syncwarp();
+    if (n * 4 <= kMergeBatch)
+      merge_rows<4>(p, tmp_o, rg, tmp_begin, n, rank, h0, lane, wt);
+    else
+      merge_rows<1>(p, tmp_o, rg, tmp_begin, n, rank, h0, lane, wt);
+    __syncwarp();
+    return;
+  }
+  // many pieces (a few very long row groups over few CTA runs): head by head
+#pragma unroll 1
+  for (int h = h0; h < h0 + 16; ++h) {
+    float M = -INFINITY;
+    for (int k = lane; k < n; k += 32) M = fmaxf(M, __ldcg(tmp_lse + (size_t)(tmp_begin + k) * kHeads + h));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float wsum = 0.f;
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+    if (M != -INFINITY) {
+#pragma unroll 1
+      for (int k0 = 0; k0 < n; k0 += 8) {
+        float4 v0[8], v1[8];
+        float w[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int k = k0 + u;
+          w[u] = 0.f;
+          v0[u] = v1[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (k < n) {
+            const size_t row = (size_t)(tmp_begin + k) * kHeads + h;
+            const float li = __ldcg(tmp_lse + row);
+            w[u] = li == -INFINITY ? 0.f : expf(li - M);
+            const float4* src = reinterpret_cast<const float4*>(tmp_o + row * kDv + 256 * rank);
+            v0[u] = __ldcg(src + lane);
+            v1[u] = __ldcg(src + 32 + lane);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          wsum += w[u];
+          a0.x = fmaf(w[u], v0[u].x, a0.x);
+          a0.y = fmaf(w[u], v0[u].y, a0.y);
+          a0.z = fmaf(w[u], v0[u].z, a0.z);
+          a0.w = fmaf(w[u], v0[u].w, a0.w);
+          a1.x = fmaf(w[u], v1[u].x, a1.x);
+          a1.y = fmaf(w[u], v1[u].y, a1.y);
+          a1.z = fmaf(w[u], v1[u].z, a1.z);
+          a1.w = fmaf(w[u], v1[u].w, a1.w);
+        }
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    float4* dst = reinterpret_cast<float4*>(p.o + ((size_t)rg * kHeads + h) * kDv + 256 * rank);
+    dst[lane] = make_float4(a0.x * inv, a0.y * inv, a0.z * inv, a0.w * inv);
+    dst[32 + lane] = make_float4(a1.x * inv, a1.y * inv, a1.z * inv, a1.w * inv);
+    if (rank == 0 && lane == 0 && p.lse_out) p.lse_out[(size_t)rg * kHeads + h] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+  }
+}
+
 // Physical block of tile t of the item, or -1 if the table entry is unusable.
 __device__ __forceinline__ int tile_block(const MlaParams& p, const ItemGeom& g, int t) {
   const int lb = (g.lo - g.start) / kTile + t;
@@ -256,6 +445,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int q4 = 0; q4 < 4; ++q4) bar_init(bar(BXCH + q4), 64);  // the two warps of a lane quadrant
     bar_init(bar(BF_FULL), kSoftmaxThreads);
     bar_init(bar(BF_EMPTY), 1);
+    bar_init(bar(BPC), kSoftmaxThreads);
+    bar_init(bar(BGO), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
@@ -278,18 +469,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // The whole warp reads block-table entries 32 tiles at a time (lane i
     // holds tile base + i); lane 0 issues the copies.
     uint32_t fills = 0;  // K/V tiles issued (global across items)
-    int n_items = 0;
+    int q_done = 0;      // query tails copied
     bool stop = false;
     for (int k = k_begin; k < k_end && !stop; ++k) {
       const ItemGeom g = item_geom(p, k);
       const int nt = g.t1 - g.t0;
+      const bool same_q = same_rows(p, k, k_begin);  // the query in place serves this item too
+      // the next row group's query into L2 while this item runs (its load is
+      // a few dependent round trips at the next item boundary otherwise)
+      if (lane == 0 && rank == 0 && k + 1 < k_end && !same_rows(p, k + 1, k_begin)) {
+        const int nb = reinterpret_cast<const ItemRec*>(p.ws + p.L.items_off)[k + 1].lane % p.B;
+        l2_prefetch(p.q + (size_t)nb * kHeads * kDk, kHeads * kDk * 2);
+      }
       int cur = lane < nt ? tile_block(p, g, g.t0 + lane) : -1;
       int nxt = 32 + lane < nt ? tile_block(p, g, g.t0 + 32 + lane) : -1;
       bool ok = true;
       if (lane == 0) {
-        if (F8) {
-          // the softmax warps write the fp16 query tail themselves
-        } else if (n_items > 0 && !wait_bar(bar(BQ_EMPTY), (n_items - 1) & 1, abort_flag, p.err, false)) {
+        if (F8 || same_q) {
+          // (F8: the softmax warps write the fp16 query tail themselves)
+        } else if (q_done > 0 && !wait_bar(bar(BQ_EMPTY), (q_done - 1) & 1, abort_flag, p.err, false)) {
           ok = false;
         } else {
           bar_arrive_tx(bar(BQT), kQSmemChunks * kQChunkBytes);
@@ -298,6 +496,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) { stop = true; break; }
+      if (!F8 && !same_q) ++q_done;
       for (int j = 0; j < nt; ++j) {
         if ((j & 31) == 0 && j > 0) {
           cur = nxt;
@@ -344,10 +543,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!__shfl_sync(0xffffffffu, ok, 0)) { stop = true; break; }
         ++fills;
       }
-      ++n_items;
     }
     if (lane == 0 && *abort_flag) {  // copies in flight must land before the CTA may exit
-      if (!F8 && n_items > 0) drain_bar(bar(BQT), (n_items - 1) & 1u);
+      if (!F8 && q_done > 0) drain_bar(bar(BQT), (q_done - 1) & 1u);
       // (the other CTA's copies into this one land on the same barriers; it
       // can be at most one page ahead, which may never complete here: the
       // poll bound ends that wait)
@@ -397,13 +595,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
           }
           mma_commit(bar(BS_FULL));
-          if (++js == nts) {  // last score tile of the item: its queries may be replaced
-            mma_commit(bar(BQ_EMPTY));
+          if (++js == nts) {  // last score tile of the item
+            if (!(ks + 1 < k_end && same_rows(p, ks + 1, k_begin))) {  // its queries may be replaced
+              mma_commit(bar(BQ_EMPTY));
+              ++q_loads;
+              q_ready = false;
+            }
             ++ks;
             js = 0;
             nts = ks < k_end ? n_tiles(ks) : 0;
-            ++q_loads;
-            q_ready = false;
           }
           ++g_s;
           progressed = true;
@@ -437,6 +637,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         return it.t1 - it.t0;
       };
       int kp = k_begin, jp = 0, ntp = kp < k_end ? n_tiles(kp) : 0;  // next P.V tile
+      bool acc_in = false;  // the item's first P.V adds to O (it carries on the previous item)
       uint32_t g_p = 0;
       uint32_t idle = 0;
       while (kp < k_end) {
@@ -456,7 +657,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kt = 0; kt < kTile / 16; ++kt)
               mma_ss(tmem + kColO, pd + (uint64_t)((term * kPBytes + 32 * kt) >> 4),
-                  vd + (uint64_t)((2048 * kt) >> 4), id_pv, (jp == 0 && term == 0 && kt == 0) ? 0 : 1);
+                  vd + (uint64_t)((2048 * kt) >> 4), id_pv, (jp == 0 && !acc_in && term == 0 && kt == 0) ? 0 : 1);
           }
           if (F8)
             mma_commit(bar(BF_EMPTY));  // the widened page may be overwritten
@@ -467,6 +668,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ++kp;
             jp = 0;
             ntp = kp < k_end ? n_tiles(kp) : 0;
+            acc_in = kp < k_end && continues(p, kp, k_begin);
           }
           ++g_p;
           idle = 0;
@@ -497,49 +699,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const bool pos_scale = p.sl2 >= 0.f;
     float* lx = reinterpret_cast<float*>(smem + kOffLx);  // [2][kHeads] row-sum halves
     uint32_t gt = 0;
-    int n_items = 0;
+    int n_q = 0, n_epi = 0;  // query loads, epilogues
+    uint32_t n_pc = 0;       // pieces counted (one-call path)
+    float m_run = -INFINITY, l_half = 0.f;
+    volatile int* merge_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 96);
     bool ok = true;
     for (int k = k_begin; k < k_end && ok; ++k) {
       const ItemGeom g = item_geom(p, k);
       const int nt = g.t1 - g.t0;
-      // query dims 192 e .. 192 e + 191 of this item into TMEM (after the previous item's score MMAs)
-      if (n_items > 0 && !wait_warp(bar(BQ_EMPTY), (n_items - 1) & 1, abort_flag, p.err, false)) break;
-      tc_fence_after();
-      {
-        const uint4* qr = reinterpret_cast<const uint4*>(p.q + ((size_t)g.b * kHeads + h) * kDk + 192 * e);
-        uint32_t qv[16];
-        __syncwarp();
+      if (!same_rows(p, k, k_begin)) {  // a new query row group: its query
+        // query dims 192 e .. 192 e + 191 of this item into TMEM (after the previous item's score MMAs)
+        if (n_q > 0 && !wait_warp(bar(BQ_EMPTY), (n_q - 1) & 1, abort_flag, p.err, false)) break;
+        tc_fence_after();
+        {
+          const uint4* qr = reinterpret_cast<const uint4*>(p.q + ((size_t)g.b * kHeads + h) * kDk + 192 * e);
+          uint32_t qv[16];
+          __syncwarp();
 #pragma unroll 1
-        for (int c = 0; c < 6; ++c) {
+          for (int c = 0; c < 6; ++c) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint4 v = qr[4 * c + i];
-            qv[4 * i] = F8 ? bf16x2_as_f16x2(v.x) : v.x;
-            qv[4 * i + 1] = F8 ? bf16x2_as_f16x2(v.y) : v.y;
-            qv[4 * i + 2] = F8 ? bf16x2_as_f16x2(v.z) : v.z;
-            qv[4 * i + 3] = F8 ? bf16x2_as_f16x2(v.w) : v.w;
+            for (int i = 0; i < 4; ++i) {
+              const uint4 v = qr[4 * c + i];
+              qv[4 * i] = F8 ? bf16x2_as_f16x2(v.x) : v.x;
+              qv[4 * i + 1] = F8 ? bf16x2_as_f16x2(v.y) : v.y;
+              qv[4 * i + 2] = F8 ? bf16x2_as_f16x2(v.z) : v.z;
+              qv[4 * i + 3] = F8 ? bf16x2_as_f16x2(v.w) : v.w;
+            }
+            tmem_st16(tmem + lane_off + kColQ + 96 * e + 16 * c, qv);
           }
-          tmem_st16(tmem + lane_off + kColQ + 96 * e + 16 * c, qv);
-        }
-        tmem_wait_st();
-        if constexpr (F8) {
-          // query dims 384 + 96 e .. + 95 in fp16 into the shared-memory tail
-          // (128-byte swizzled rows of 64 dims, as the copy would lay them out)
-          const uint4* qt = reinterpret_cast<const uint4*>(p.q + ((size_t)g.b * kHeads + h) * kDk + 384 + 96 * e);
+          tmem_wait_st();
+          if constexpr (F8) {
+            // query dims 384 + 96 e .. + 95 in fp16 into the shared-memory tail
+            // (128-byte swizzled rows of 64 dims, as the copy would lay them out)
+            const uint4* qt = reinterpret_cast<const uint4*>(p.q + ((size_t)g.b * kHeads + h) * kDk + 384 + 96 * e);
 #pragma unroll 4
-          for (int c = 0; c < 12; ++c) {
-            const uint4 v = qt[c];
-            const int d = 96 * e + 8 * c;  // dim - 384
-            const uint32_t a = sbase + kOffQ + (d >> 6) * kQChunkBytes + h * 128 +
-                               (((uint32_t)((d & 63) >> 3) ^ (uint32_t)(h & 7)) << 4);
-            st_shared_v4(a, bf16x2_as_f16x2(v.x), bf16x2_as_f16x2(v.y), bf16x2_as_f16x2(v.z), bf16x2_as_f16x2(v.w));
+            for (int c = 0; c < 12; ++c) {
+              const uint4 v = qt[c];
+              const int d = 96 * e + 8 * c;  // dim - 384
+              const uint32_t a = sbase + kOffQ + (d >> 6) * kQChunkBytes + h * 128 +
+                                 (((uint32_t)((d & 63) >> 3) ^ (uint32_t)(h & 7)) << 4);
+              st_shared_v4(a, bf16x2_as_f16x2(v.x), bf16x2_as_f16x2(v.y), bf16x2_as_f16x2(v.z), bf16x2_as_f16x2(v.w));
+            }
+            asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
           }
-          asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
         }
+        tc_fence_before();
+        bar_arrive(bar(BQ_FULL));
+        ++n_q;
       }
-      tc_fence_before();
-      bar_arrive(bar(BQ_FULL));
-      float m_run = -INFINITY, l_half = 0.f;
+      if (!continues(p, k, k_begin)) {  // a fresh softmax
+        m_run = -INFINITY;
+        l_half = 0.f;
+      }
       for (int j = 0; j < nt; ++j) {
         const uint32_t gi = gt + j, s = gi % kStages;
         const int t = g.t0 + j;
@@ -718,11 +929,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bar_arrive(bar(BP_FULL + s));
       }
       if (!ok) break;
+      if (k + 1 < k_end && continues(p, k + 1, k_begin)) {  // the next shard carries on this softmax
+        gt += nt;
+        continue;
+      }
       // epilogue: the row sum of the two halves, then wait for the last P.V
       // and write this warp's dims of O_r / l and the LSE
       lx[e * kHeads + h] = l_half;
       bar_arrive(bar(BXCH + qd));  // release: the partner reads lx after its wait
-      if (!wait_warp(bar(BXCH + qd), (uint32_t)n_items & 1u, abort_flag, p.err, false)) break;
+      if (!wait_warp(bar(BXCH + qd), (uint32_t)n_epi & 1u, abort_flag, p.err, false)) break;
       const float l_run = l_half + lx[(1 - e) * kHeads + h];
       const uint32_t glast = gt + nt - 1;
       // (P.V products finish in issue order: the last one implies the others)
@@ -731,7 +946,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const float inv = l_run > 0.f ? p.v_scale / l_run : 0.f;
       float* out;
       float* out_lse;
-      if (g.out_row >= 0) {
+      GroupRec gr;
+      bool piece = false;  // one-call path, row group cut by a CTA run boundary
+      if (p.o) {
+        gr = reinterpret_cast<const GroupRec*>(p.ws + p.L.grp_off)[g.b];
+        piece = gr.pieces > 1;
+        if (piece) {
+          const size_t row = (size_t)(gr.tmp_begin + cluster - gr.first_cta);
+          out = reinterpret_cast<float*>(const_cast<char*>(p.ws) + p.L.tmp_o_off) + (row * kHeads + h) * kDv;
+          out_lse = reinterpret_cast<float*>(const_cast<char*>(p.ws) + p.L.tmp_lse_off) + row * kHeads + h;
+        } else {
+          out = p.o + ((size_t)g.b * kHeads + h) * kDv;
+          out_lse = p.lse_out ? p.lse_out + (size_t)g.b * kHeads + h : nullptr;
+        }
+      } else if (g.out_row >= 0) {
         out = reinterpret_cast<float*>(const_cast<char*>(p.ws) + p.L.tmp_o_off) +
               ((size_t)g.out_row * kHeads + h) * kDv;
         out_lse = reinterpret_cast<float*>(const_cast<char*>(p.ws) + p.L.tmp_lse_off) + (size_t)g.out_row * kHeads + h;
@@ -752,10 +980,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           o4[i] = make_float4(__uint_as_float(ov[4 * i]) * inv, __uint_as_float(ov[4 * i + 1]) * inv,
                               __uint_as_float(ov[4 * i + 2]) * inv, __uint_as_float(ov[4 * i + 3]) * inv);
       }
-      if (rank == 0 && e == 0) *out_lse = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+      // A piece's LSE is written by both CTAs of the pair (the same value:
+      // both computed the same scores and sums), so that each CTA's own count
+      // below covers every LSE its merge reads.
+      if (e == 0 && out_lse && (rank == 0 || piece))
+        *out_lse = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
       tc_fence_before();
       gt += nt;
-      ++n_items;
+      ++n_epi;
+      if (piece) {
+        // count this CTA's piece once all its rows are out (every thread's
+        // stores, then a fence, then its arrival); the count that completes
+        // the group merges it. Bounded waits on mbarriers, not bar.sync, so
+        // that an abort cannot leave threads waiting for one that left.
+        __threadfence();
+        bar_arrive(bar(BPC));
+        if (threadIdx.x == 0) {
+          int last = 0;
+          if (wait_bar(bar(BPC), n_pc & 1u, abort_flag, p.err, false)) {
+            __threadfence();
+            GroupRec* grw = reinterpret_cast<GroupRec*>(const_cast<char*>(p.ws) + p.L.grp_off);
+            last = atomicAdd(&grw[g.b].cnt[rank], 1) == gr.pieces - 1 ? 1 : 0;
+            __threadfence();
+          }
+          *merge_flag = last;
+          bar_arrive(bar(BGO));
+        }
+        if (!wait_warp(bar(BGO), n_pc & 1u, abort_flag, p.err, false)) break;
+        ++n_pc;
+        if (*merge_flag) {
+          __threadfence();
+          merge_pieces(p, g.b, gr.tmp_begin, gr.pieces, rank, warp, lane,
+                       reinterpret_cast<float*>(smem + Lay::kOffMw));
+        }
+      }
+    }
+    if (p.o) {
+      // row groups without a token in any shard (no CTA visits them): o = 0, LSE = -inf
+      const GroupRec* grp = reinterpret_cast<const GroupRec*>(p.ws + p.L.grp_off);
+      for (int rg = cluster; rg < p.B; rg += (int)(gridDim.x >> 1)) {
+        if (grp[rg].pieces != 0) continue;
+        for (int hh = warp; hh < kHeads; hh += kSoftmaxWarps) {
+          float4* dst = reinterpret_cast<float4*>(p.o + ((size_t)rg * kHeads + hh) * kDv + 256 * rank);
+          dst[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+          dst[32 + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (rank == 0 && lane == 0 && p.lse_out) p.lse_out[(size_t)rg * kHeads + hh] = -INFINITY;
+        }
+      }
     }
   }
 
@@ -829,7 +1100,7 @@ int mla_ctas(const dcp_attn_desc& d, const DeviceInfo&) {
 
 cudaError_t launch_mla(const dcp_attn_desc& d, const void* q, const ShardSet& sh, const RangeSpec& rs,
                        float* o_parts, float* lses, void* ws, const WsLayout& L, int n_ctas, int32_t* err,
-                       cudaStream_t st) {
+                       cudaStream_t st, float* o, float* lse_out) {
   const bool f8 = d.kv_dtype == DCP_KV_FP8_E4M3;
   if (n_ctas <= 0 || (f8 ? mla_clusters<true>() : mla_clusters<false>()) <= 0) return cudaErrorNotSupported;
   MlaParams p;
@@ -845,6 +1116,8 @@ cudaError_t launch_mla(const dcp_attn_desc& d, const void* q, const ShardSet& sh
   p.L = L;
   p.o_parts = o_parts;
   p.lses = lses;
+  p.o = o;
+  p.lse_out = lse_out;
   p.err = err;
   p.B = rs.B;
   p.qlen = rs.qlen;

@@ -4,8 +4,10 @@
 // (device memory, so the host never synchronises), and writes into the
 // workspace:
 //   lanes[l]   token range, tile count, and the items covering the lane
-//   items[k]   (lane, tile range, output row) in lane order
+//   items[k]   (lane, tile range, output row) in layout order
 //   cta_begin  CTA c processes items [cta_begin[c], cta_begin[c+1])
+//   groups[r]  (group order only) the CTA runs row group r spans, its
+//              workspace rows, and zeroed piece counters
 // CTA c's tiles are [c*T/S, (c+1)*T/S) of the T tiles laid end to end, so the
 // CTAs' loads differ by at most one tile.
 #include <climits>
@@ -93,20 +95,31 @@ __device__ __forceinline__ long long cta_start(long long c, long long T, long lo
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(RangeSpec rs, int lanes_per_unit, int tile,
-                                                            int n_ctas, char* ws, WsLayout L) {
+                                                            int n_ctas, char* ws, WsLayout L, int group_order) {
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   LaneRec* lanes = reinterpret_cast<LaneRec*>(ws + L.lanes_off);
   ItemRec* items = reinterpret_cast<ItemRec*>(ws + L.items_off);
   int* cta_begin = reinterpret_cast<int*>(ws + L.cta_off);
+  GroupRec* groups = reinterpret_cast<GroupRec*>(ws + L.grp_off);
 
   const int n_lanes = rs.B * rs.N * lanes_per_unit;
+  const int group_lanes = rs.N * lanes_per_unit;  // lanes of one row group
+  // the lane at layout position x: shard by shard (x itself), or row group by
+  // row group (x = (r * N + shard) * lanes_per_unit + j)
+  auto lane_at = [&](int x) {
+    if (!group_order) return x;
+    const int r = x / group_lanes, rem = x - r * group_lanes;
+    const int i = rem / lanes_per_unit, j = rem - i * lanes_per_unit;
+    return (i * rs.B + r) * lanes_per_unit + j;
+  };
   const int per = (n_lanes + kPlanThreads - 1) / kPlanThreads;
-  const int l0 = threadIdx.x * per;
-  const int l1 = min(n_lanes, l0 + per);
+  const int x0 = threadIdx.x * per;
+  const int x1 = min(n_lanes, x0 + per);
 
   // pass 1: ranges and tile counts
   long long my_tiles = 0;
-  for (int l = l0; l < l1; ++l) {
+  for (int x = x0; x < x1; ++x) {
+    const int l = lane_at(x);
     int lo, hi, start;
     unit_range(rs, l / lanes_per_unit, &lo, &hi, &start);
     LaneRec r;
@@ -130,12 +143,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(RangeSpec rs, int la
 
   // pass 2: items per lane (number of CTA runs the lane overlaps)
   long long p = pre.a, my_items = 0, my_split = 0;
-  for (int l = l0; l < l1; ++l) {
+  for (int x = x0; x < x1; ++x) {
+    const int l = lane_at(x);
     const int t = lanes[l].tiles;
     int n = 0;
     if (t > 0) n = cta_of(p + t - 1, T, S) - cta_of(p, T, S) + 1;
     lanes[l].n_items = n;
-    lanes[l].pad = (int)p;  // tile prefix, used in pass 3
+    lanes[l].pad = (int)p;  // tile prefix, used below and in pass 3
     my_items += n;
     if (n > 1) my_split += n;
     p += t;
@@ -143,9 +157,45 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(RangeSpec rs, int la
   Scan2 tot2;
   Scan2 pre2 = block_exclusive_scan2(Scan2{my_items, my_split}, &tot2);
 
+  if (group_order) {
+    // row groups: the CTA runs their tiles span, and workspace rows for the
+    // pieces of those that span several (the scans' barriers order these
+    // reads of the tile prefixes after pass 2 and before pass 3)
+    const int n_groups = rs.B;
+    const int gper = (n_groups + kPlanThreads - 1) / kPlanThreads;
+    const int g0 = threadIdx.x * gper, g1 = min(n_groups, g0 + gper);
+    auto span = [&](int r, int* first) {
+      const long long a = lanes[lane_at(r * group_lanes)].pad;
+      const long long e = r + 1 < n_groups ? (long long)lanes[lane_at((r + 1) * group_lanes)].pad : T;
+      *first = e > a ? cta_of(a, T, S) : 0;
+      return e > a ? cta_of(e - 1, T, S) - *first + 1 : 0;
+    };
+    long long my_rows = 0;
+    for (int r = g0; r < g1; ++r) {
+      int first;
+      const int n = span(r, &first);
+      if (n > 1) my_rows += n;
+    }
+    Scan2 tot3;
+    Scan2 pre3 = block_exclusive_scan2(Scan2{my_rows, 0}, &tot3);
+    long long row = pre3.a;
+    for (int r = g0; r < g1; ++r) {
+      GroupRec gr;
+      gr.pieces = span(r, &gr.first_cta);
+      gr.tmp_begin = gr.pieces > 1 ? (int)row : 0;
+      gr.pad = 0;
+      gr.cnt[0] = gr.cnt[1] = 0;
+      gr.pad2[0] = gr.pad2[1] = 0;
+      groups[r] = gr;
+      if (gr.pieces > 1) row += gr.pieces;
+    }
+    __syncthreads();
+  }
+
   // pass 3: items
   long long ib = pre2.a, tb = pre2.b;
-  for (int l = l0; l < l1; ++l) {
+  for (int x = x0; x < x1; ++x) {
+    const int l = lane_at(x);
     LaneRec r = lanes[l];
     const long long P = r.pad;
     r.item_begin = (int)ib;
@@ -186,8 +236,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(RangeSpec rs, int la
 }  // namespace
 
 cudaError_t launch_plan(const RangeSpec& rs, int lanes_per_unit, int tile, int n_ctas, void* ws,
-                        const WsLayout& L, cudaStream_t st) {
-  plan_kernel<<<1, kPlanThreads, 0, st>>>(rs, lanes_per_unit, tile, n_ctas, static_cast<char*>(ws), L);
+                        const WsLayout& L, bool group_order, cudaStream_t st) {
+  plan_kernel<<<1, kPlanThreads, 0, st>>>(rs, lanes_per_unit, tile, n_ctas, static_cast<char*>(ws), L,
+                                          group_order ? 1 : 0);
   return cudaGetLastError();
 }
 

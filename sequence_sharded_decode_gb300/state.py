@@ -146,8 +146,8 @@ class DecodeState:
     def step(self, stream=None, fused: bool = False):
         """append -> partial attention of every shard -> merge; fused: the last
         two in one call (dcp_attention_all; the shards' partial rows of split
-        ranges are then not written), else dcp_decode_partial_all(_mtp) then
-        dcp_merge."""
+        ranges -- for MLA, all of them -- are then not written), else
+        dcp_decode_partial_all(_mtp) then dcp_merge."""
         self.append(stream)
         if fused:
             self.attention(stream)
@@ -172,14 +172,24 @@ class DecodeState:
         """KV bytes the partial-attention pass must read (each attended token once)."""
         return self.attended_tokens() * self.wl.kv_bytes_per_token
 
-    def step_bytes(self) -> dict:
-        """Algorithmic HBM bytes of one step, by kernel."""
+    def step_bytes(self, fused: bool = False) -> dict:
+        """Algorithmic HBM bytes of one step, by call. Two calls (and GQA's
+        one call): the shards' partial rows are written and read back. MLA's
+        one call merges the shards on chip: KV, queries and the merged rows
+        only (the pieces of the few row groups a CTA boundary cuts are left
+        out: at most two per CTA pair)."""
         wl = self.wl
         B, N, Hq, dv, dk = wl.batch * self.q_len, wl.shards, wl.q_heads, wl.dv, wl.dk
         part = N * B * Hq * (dv + 1) * 4
+        out = B * Hq * (dv + 1) * 4
         new_tok = B * (wl.kv_bytes_per_token if wl.kind == configs.GQA else dk * 2)
+        if fused and wl.kind == configs.MLA:
+            return {
+                "append": 2 * new_tok,                  # read the new rows, write them
+                "attention": self.kv_bytes() + B * Hq * dk * 2 + out,
+            }
         return {
-            "append": 2 * new_tok,                      # read the new rows, write them
+            "append": 2 * new_tok,
             "partial": self.kv_bytes() + B * Hq * dk * 2 + part,
-            "merge": part + B * Hq * (dv + 1) * 4,
+            "merge": part + out,
         }

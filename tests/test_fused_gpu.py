@@ -1,7 +1,8 @@
-"""Steps 2 and 3 in one call (dcp_attention_all: per-shard partial attention,
-then one pass merging every output row's pieces across shards and split
-ranges) against the float64 oracle, and against the two-call path
-(partial + dcp_merge) on the same device state."""
+"""Steps 2 and 3 in one call (dcp_attention_all: GQA: per-shard partial
+attention, then one pass merging every output row's pieces across shards and
+split ranges; MLA: the attention kernel merges the shards itself) against the
+float64 oracle, and against the two-call path (partial + dcp_merge) on the
+same device state."""
 import numpy as np
 import pytest
 import torch
@@ -43,11 +44,17 @@ def test_attention_all_matches_oracle_and_two_calls(name, q_len, over):
     torch.cuda.synchronize()
     assert int(st.err.item()) == 0
     o, lse = st.o.cpu().numpy(), st.lse.cpu().numpy()
-    # the two paths differ only in the order of the fp32 merge
-    assert np.allclose(o, o2.cpu().numpy(), atol=2e-6, rtol=1e-5)
     np.testing.assert_array_equal(np.isneginf(lse), np.isneginf(l2.cpu().numpy()))
     fin = np.isfinite(lse)
-    assert np.allclose(lse[fin], l2.cpu().numpy()[fin], atol=1e-5)
+    if wl.kind == configs.MLA:
+        # the MLA kernel merges the shards inside its online softmax (its own
+        # rounding): the two paths agree to the parity bar
+        assert_close(o, o2.cpu().numpy(), "one call vs two calls")
+        assert_lse_close(lse, l2.cpu().numpy(), "one call vs two calls")
+    else:
+        # the two paths differ only in the order of the fp32 merge
+        assert np.allclose(o, o2.cpu().numpy(), atol=2e-6, rtol=1e-5)
+        assert np.allclose(lse[fin], l2.cpu().numpy()[fin], atol=1e-5)
     for b in range(wl.batch):
         ctx_b = int(st.ctx[b])
         starts_b = O.shard_starts([ctx_b], wl.shards)[0]

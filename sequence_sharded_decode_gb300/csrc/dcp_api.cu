@@ -27,6 +27,8 @@ WsLayout ws_layout(int n_lanes, int max_ctas, int rows_per_lane, int dv, int n_g
   off = align256(off + sizeof(int) * (size_t)(max_ctas + 1));
   L.grp_off = off;
   off = align256(off + sizeof(GroupRec) * (size_t)n_groups);
+  L.fin_off = off;
+  off = align256(off + sizeof(int) * (size_t)n_groups);
   L.tmp_o_off = off;
   off = align256(off + sizeof(float) * (size_t)L.max_tmp * rows_per_lane * dv);
   L.tmp_lse_off = off;

@@ -17,8 +17,11 @@
 // then carries one online softmax through the consecutive shards of a row
 // group, so the shards are merged on chip: a row group whose tiles one CTA run
 // covers is written straight to the output; one that a CTA boundary cuts
-// leaves one *piece* per run in the workspace, and the CTA that writes the
-// last piece merges them.
+// leaves one *piece* per run in the workspace. Up to kMlaMergeInKernel pieces
+// the CTA that writes the last piece merges them; a group cut into more (a
+// few long sequences over many CTA runs, whose merges would all fall at the
+// end of the kernel on a few SMs) and groups without tokens are finished by a
+// short kernel over the whole GPU, from a list the plan writes.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -77,6 +80,8 @@ struct ItemRec {     // 16 bytes
   int out_row;       // >= 0: workspace partial row; -1: write the lane's output directly
 };
 
+constexpr int kMlaMergeInKernel = 4;  // pieces a group may have for the attention kernel to merge it
+
 struct GroupRec {    // 32 bytes: one query row group of the one-call MLA path
   int pieces;        // CTA runs its tiles span (0: no tokens in any shard)
   int tmp_begin;     // first workspace partial row if pieces > 1
@@ -91,11 +96,12 @@ struct WsHeader {
   int n_lanes;
   int n_ctas;
   int total_tiles;
-  int pad[60];       // 256 bytes
+  int n_finish;      // group order: row groups in the finish list
+  int pad[59];       // 256 bytes
 };
 
 struct WsLayout {
-  size_t lanes_off, items_off, cta_off, grp_off, tmp_o_off, tmp_lse_off, total;
+  size_t lanes_off, items_off, cta_off, grp_off, fin_off, tmp_o_off, tmp_lse_off, total;
   int max_lanes, max_items, max_ctas, max_tmp, rows_per_lane, max_groups;
 };
 
@@ -121,8 +127,8 @@ struct LaneGeom {
 LaneGeom lane_geom(const dcp_attn_desc& d);
 
 // Kernel launchers (return the launch's cudaError_t).
-// group_order: lay the lanes out row group by row group and fill the group
-// records (MLA); otherwise shard by shard.
+// group_order: lay the lanes out row group by row group, fill the group
+// records and the finish list (MLA); otherwise shard by shard.
 cudaError_t launch_plan(const RangeSpec& rs, int lanes_per_unit, int tile, int n_ctas,
                         void* ws, const WsLayout& L, bool group_order, cudaStream_t st);
 cudaError_t launch_gqa(const dcp_attn_desc& d, const void* q, const ShardSet& sh, const RangeSpec& rs,

@@ -127,8 +127,8 @@ struct MlaLayout {
   static constexpr int kOffBar = kOffQ + kQSmemChunks * kQChunkBytes;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag, residual votes (per stage)
   static constexpr int kOffLx = kOffMisc + 128;            // row-sum halves exchanged at the end of an item
-  static constexpr int kOffMw = kOffLx + 2 * kHeads * 4;   // one-call path: merge weights [8 warps][16][32]
-  static constexpr int kSmemBytes = kOffMw + kSoftmaxWarps * 16 * 32 * 4 + 1024;  // slack to align the base to 1024
+  static constexpr int kOffMw = kOffLx + 2 * kHeads * 4;   // one-call path: merge weights [8 warps][16 heads][4]
+  static constexpr int kSmemBytes = kOffMw + kSoftmaxWarps * 16 * kMlaMergeInKernel * 4 + 1024;  // + base alignment
 };
 
 // barrier slots
@@ -215,161 +215,92 @@ __device__ __forceinline__ bool continues(const MlaParams& p, int k, int k_begin
   return p.o != nullptr && same_rows(p, k, k_begin);
 }
 
-// One-call path: the CTA that completed row group rg's piece count merges the
-// pieces' value dims [256 rank, 256 rank + 256) into o (the LSE reweighting:
-// M = max LSE_i, w_i = e^(LSE_i - M), O = sum w_i O_i / sum w_i, LSE = M +
-// ln sum w_i). The 256 softmax threads: warp w takes heads 16 w .. 16 w + 15,
-// lane l columns 4l .. 4l + 3 and 128 + 4l ..; loads bypass L1 (the pieces
-// were written by other SMs). The merge sits at the end of the CTAs' runs,
-// where its dependent L2 round trips are the cost: the weights of all 16 heads
-// come from one round of loads (lane k: piece k's LSEs) and wait in shared
-// memory, and each head's pieces (or four heads' few pieces) are loaded in one
-// batch.
-constexpr int kMergeFast = 32;  // pieces whose weights fit the shared-memory table
-constexpr int kMergeBatch = 12; // pieces (x heads) loaded per round trip
-
-template <int HB>  // heads per batch: pieces per head <= kMergeBatch / HB
+// One-call path: the CTA that completed the count of a row group cut into at
+// most kMlaMergeInKernel pieces merges the pieces' value dims [256 rank,
+// 256 rank + 256) into o (the LSE reweighting: M = max LSE_i, w_i =
+// e^(LSE_i - M), O = sum w_i O_i / sum w_i, LSE = M + ln sum w_i). The 256
+// softmax threads: warp w takes heads 16 w .. 16 w + 15, lane l columns
+// 4l .. 4l + 3 and 128 + 4l ..; loads bypass L1 (the pieces were written by
+// other SMs). Its cost is dependent L2 round trips: the weights of the
+// warp's 16 heads come from one round of loads (lane k: piece k's LSEs) and
+// wait in shared memory, and the pieces of two or four heads are loaded
+// together.
+template <int HB, int KB>  // heads per batch, pieces per batch (>= the group's pieces)
 __device__ __forceinline__ void merge_rows(const MlaParams& p, const float* tmp_o, int rg, int tmp_begin, int n,
                                            uint32_t rank, int h0, int lane, const float* wt) {
-  constexpr int KB = kMergeBatch / HB;
 #pragma unroll 1
   for (int i0 = 0; i0 < 16; i0 += HB) {
-    float4 a0[HB], a1[HB];
+    float4 v0[HB][KB], v1[HB][KB];
 #pragma unroll
-    for (int hb = 0; hb < HB; ++hb) a0[hb] = a1[hb] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 1
-    for (int k0 = 0; k0 < n; k0 += KB) {
-      float4 v0[HB][KB], v1[HB][KB];
+    for (int hb = 0; hb < HB; ++hb)
 #pragma unroll
-      for (int hb = 0; hb < HB; ++hb)
-#pragma unroll
-        for (int u = 0; u < KB; ++u) {
-          const int k = k0 + u;
-          v0[hb][u] = v1[hb][u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (k < n) {
-            const float4* src = reinterpret_cast<const float4*>(
-                tmp_o + ((size_t)(tmp_begin + k) * kHeads + h0 + i0 + hb) * kDv + 256 * rank);
-            v0[hb][u] = __ldcg(src + lane);
-            v1[hb][u] = __ldcg(src + 32 + lane);
-          }
+      for (int k = 0; k < KB; ++k) {
+        v0[hb][k] = v1[hb][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (k < n) {
+          const float4* src = reinterpret_cast<const float4*>(
+              tmp_o + ((size_t)(tmp_begin + k) * kHeads + h0 + i0 + hb) * kDv + 256 * rank);
+          v0[hb][k] = __ldcg(src + lane);
+          v1[hb][k] = __ldcg(src + 32 + lane);
         }
-#pragma unroll
-      for (int hb = 0; hb < HB; ++hb)
-#pragma unroll
-        for (int u = 0; u < KB; ++u) {
-          const int k = k0 + u;
-          const float w = k < n ? wt[(i0 + hb) * kMergeFast + k] : 0.f;
-          a0[hb].x = fmaf(w, v0[hb][u].x, a0[hb].x);
-          a0[hb].y = fmaf(w, v0[hb][u].y, a0[hb].y);
-          a0[hb].z = fmaf(w, v0[hb][u].z, a0[hb].z);
-          a0[hb].w = fmaf(w, v0[hb][u].w, a0[hb].w);
-          a1[hb].x = fmaf(w, v1[hb][u].x, a1[hb].x);
-          a1[hb].y = fmaf(w, v1[hb][u].y, a1[hb].y);
-          a1[hb].z = fmaf(w, v1[hb][u].z, a1[hb].z);
-          a1[hb].w = fmaf(w, v1[hb][u].w, a1[hb].w);
-        }
-    }
+      }
 #pragma unroll
     for (int hb = 0; hb < HB; ++hb) {
+      float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+#pragma unroll
+      for (int k = 0; k < KB; ++k) {
+        const float w = k < n ? wt[(i0 + hb) * kMlaMergeInKernel + k] : 0.f;
+        a0 = make_float4(fmaf(w, v0[hb][k].x, a0.x), fmaf(w, v0[hb][k].y, a0.y), fmaf(w, v0[hb][k].z, a0.z),
+                         fmaf(w, v0[hb][k].w, a0.w));
+        a1 = make_float4(fmaf(w, v1[hb][k].x, a1.x), fmaf(w, v1[hb][k].y, a1.y), fmaf(w, v1[hb][k].z, a1.z),
+                         fmaf(w, v1[hb][k].w, a1.w));
+      }
       float4* dst = reinterpret_cast<float4*>(p.o + ((size_t)rg * kHeads + h0 + i0 + hb) * kDv + 256 * rank);
-      dst[lane] = a0[hb];
-      dst[32 + lane] = a1[hb];
+      dst[lane] = a0;
+      dst[32 + lane] = a1;
     }
   }
 }
 
-__device__ __noinline__ void merge_pieces(const MlaParams& p, int rg, int tmp_begin, int n, uint32_t rank, int warp,
+__device__ __forceinline__ void merge_pieces(const MlaParams& p, int rg, int tmp_begin, int n, uint32_t rank, int warp,
                                           int lane, float* mw) {
   const float* tmp_o = reinterpret_cast<const float*>(p.ws + p.L.tmp_o_off);
   const float* tmp_lse = reinterpret_cast<const float*>(p.ws + p.L.tmp_lse_off);
   const int h0 = 16 * warp;
-  if (n <= kMergeFast) {
-    // lane k: piece k's LSEs of the warp's 16 heads (one round of loads)
-    float lv[16];
-    if (lane < n) {
-      const float4* src = reinterpret_cast<const float4*>(tmp_lse + (size_t)(tmp_begin + lane) * kHeads + h0);
+  float lv[16];
+  if (lane < n) {
+    const float4* src = reinterpret_cast<const float4*>(tmp_lse + (size_t)(tmp_begin + lane) * kHeads + h0);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float4 v = __ldcg(src + c);
-        lv[4 * c] = v.x;
-        lv[4 * c + 1] = v.y;
-        lv[4 * c + 2] = v.z;
-        lv[4 * c + 3] = v.w;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) lv[i] = -INFINITY;
+    for (int c = 0; c < 4; ++c) {
+      const float4 v = __ldcg(src + c);
+      lv[4 * c] = v.x;
+      lv[4 * c + 1] = v.y;
+      lv[4 * c + 2] = v.z;
+      lv[4 * c + 3] = v.w;
     }
-    float* wt = mw + warp * 16 * kMergeFast;  // [head][piece]: normalised weights
+  } else {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float M = lv[i];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      const float w = (M == -INFINITY || lv[i] == -INFINITY) ? 0.f : expf(lv[i] - M);
-      float ws = w;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
-      wt[i * kMergeFast + lane] = ws > 0.f ? w / ws : 0.f;
-      if (rank == 0 && lane == 0 && p.lse_out)
-        p.lse_out[(size_t)rg * kHeads + h0 + i] = ws > 0.f ? M + logf(ws) : -INFINITY;
-    }
-    __syncwarp();
-    if (n * 4 <= kMergeBatch)
-      merge_rows<4>(p, tmp_o, rg, tmp_begin, n, rank, h0, lane, wt);
-    else
-      merge_rows<1>(p, tmp_o, rg, tmp_begin, n, rank, h0, lane, wt);
-    __syncwarp();
-    return;
+    for (int i = 0; i < 16; ++i) lv[i] = -INFINITY;
   }
-  // many pieces (a few very long row groups over few CTA runs): head by head
-#pragma unroll 1
-  for (int h = h0; h < h0 + 16; ++h) {
-    float M = -INFINITY;
-    for (int k = lane; k < n; k += 32) M = fmaxf(M, __ldcg(tmp_lse + (size_t)(tmp_begin + k) * kHeads + h));
+  float* wt = mw + warp * 16 * kMlaMergeInKernel;  // [head][piece]: normalised weights
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float M = lv[i];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float wsum = 0.f;
-    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-    if (M != -INFINITY) {
-#pragma unroll 1
-      for (int k0 = 0; k0 < n; k0 += 8) {
-        float4 v0[8], v1[8];
-        float w[8];
+    const float w = (M == -INFINITY || lv[i] == -INFINITY) ? 0.f : expf(lv[i] - M);
+    float ws = w;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int k = k0 + u;
-          w[u] = 0.f;
-          v0[u] = v1[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (k < n) {
-            const size_t row = (size_t)(tmp_begin + k) * kHeads + h;
-            const float li = __ldcg(tmp_lse + row);
-            w[u] = li == -INFINITY ? 0.f : expf(li - M);
-            const float4* src = reinterpret_cast<const float4*>(tmp_o + row * kDv + 256 * rank);
-            v0[u] = __ldcg(src + lane);
-            v1[u] = __ldcg(src + 32 + lane);
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          wsum += w[u];
-          a0.x = fmaf(w[u], v0[u].x, a0.x);
-          a0.y = fmaf(w[u], v0[u].y, a0.y);
-          a0.z = fmaf(w[u], v0[u].z, a0.z);
-          a0.w = fmaf(w[u], v0[u].w, a0.w);
-          a1.x = fmaf(w[u], v1[u].x, a1.x);
-          a1.y = fmaf(w[u], v1[u].y, a1.y);
-          a1.z = fmaf(w[u], v1[u].z, a1.z);
-          a1.w = fmaf(w[u], v1[u].w, a1.w);
-        }
-      }
-    }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    float4* dst = reinterpret_cast<float4*>(p.o + ((size_t)rg * kHeads + h) * kDv + 256 * rank);
-    dst[lane] = make_float4(a0.x * inv, a0.y * inv, a0.z * inv, a0.w * inv);
-    dst[32 + lane] = make_float4(a1.x * inv, a1.y * inv, a1.z * inv, a1.w * inv);
-    if (rank == 0 && lane == 0 && p.lse_out) p.lse_out[(size_t)rg * kHeads + h] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+    for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+    if (lane < kMlaMergeInKernel) wt[i * kMlaMergeInKernel + lane] = ws > 0.f ? w / ws : 0.f;
+    if (rank == 0 && lane == 0 && p.lse_out)
+      p.lse_out[(size_t)rg * kHeads + h0 + i] = ws > 0.f ? M + logf(ws) : -INFINITY;
   }
+  __syncwarp();
+  if (n <= 2)
+    merge_rows<4, 2>(p, tmp_o, rg, tmp_begin, n, rank, h0, lane, wt);
+  else
+    merge_rows<2, kMlaMergeInKernel>(p, tmp_o, rg, tmp_begin, n, rank, h0, lane, wt);
+  __syncwarp();
 }
 
 // Physical block of tile t of the item, or -1 if the table entry is unusable.
@@ -988,7 +919,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       gt += nt;
       ++n_epi;
-      if (piece) {
+      if (piece && gr.pieces <= kMlaMergeInKernel) {
         // count this CTA's piece once all its rows are out (every thread's
         // stores, then a fence, then its arrival); the count that completes
         // the group merges it. Bounded waits on mbarriers, not bar.sync, so
@@ -1015,19 +946,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (p.o) {
-      // row groups without a token in any shard (no CTA visits them): o = 0, LSE = -inf
-      const GroupRec* grp = reinterpret_cast<const GroupRec*>(p.ws + p.L.grp_off);
-      for (int rg = cluster; rg < p.B; rg += (int)(gridDim.x >> 1)) {
-        if (grp[rg].pieces != 0) continue;
-        for (int hh = warp; hh < kHeads; hh += kSoftmaxWarps) {
-          float4* dst = reinterpret_cast<float4*>(p.o + ((size_t)rg * kHeads + hh) * kDv + 256 * rank);
-          dst[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
-          dst[32 + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (rank == 0 && lane == 0 && p.lse_out) p.lse_out[(size_t)rg * kHeads + hh] = -INFINITY;
-        }
-      }
-    }
   }
 
   tc_fence_before();
@@ -1037,6 +955,88 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols));
   }
   cluster_sync();  // neither CTA exits while the other's copies or arrivals may still reach it
+}
+
+// One-call path, after the attention kernel: the row groups of the plan's
+// finish list -- no token in any shard (o = 0, LSE = -inf), or cut into more
+// than kMlaMergeInKernel pieces -- one warp per output row over the whole GPU:
+// lane k holds the LSEs of pieces k, k + 32, ... (a group has at most one
+// piece per CTA pair, at most 128: the launch checks), the weights follow by
+// warp reductions, and each lane accumulates 16 of the row's 512 columns,
+// four pieces per round of loads.
+constexpr int kFinishThreads = 256;
+constexpr int kFinishMax = 128;
+
+__global__ void __launch_bounds__(kFinishThreads) mla_finish_kernel(const char* __restrict__ ws, WsLayout L,
+                                                                     float* __restrict__ o,
+                                                                     float* __restrict__ lse_out) {
+  const int n_fin = reinterpret_cast<const WsHeader*>(ws)->n_finish;
+  const int* fin = reinterpret_cast<const int*>(ws + L.fin_off);
+  const GroupRec* grp = reinterpret_cast<const GroupRec*>(ws + L.grp_off);
+  const float* tmp_o = reinterpret_cast<const float*>(ws + L.tmp_o_off);
+  const float* tmp_lse = reinterpret_cast<const float*>(ws + L.tmp_lse_off);
+  const int lane = threadIdx.x & 31;
+  const long long rows = (long long)n_fin * kHeads;
+  const long long warps = (long long)gridDim.x * (kFinishThreads / 32);
+  for (long long x = (long long)blockIdx.x * (kFinishThreads / 32) + (threadIdx.x >> 5); x < rows; x += warps) {
+    const int rg = fin[x / kHeads], h = (int)(x % kHeads);
+    const GroupRec gr = grp[rg];
+    const int n = gr.pieces;
+    float l[kFinishMax / 32], w[kFinishMax / 32];
+    float M = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kFinishMax / 32; ++c) {
+      const int k = lane + 32 * c;
+      l[c] = k < n ? __ldcg(tmp_lse + (size_t)(gr.tmp_begin + k) * kHeads + h) : -INFINITY;
+      M = fmaxf(M, l[c]);
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, s));
+    float wsum = 0.f;
+#pragma unroll
+    for (int c = 0; c < kFinishMax / 32; ++c) {
+      w[c] = (M == -INFINITY || l[c] == -INFINITY) ? 0.f : expf(l[c] - M);
+      wsum += w[c];
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, s);
+    float4 acc[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+    for (int k0 = 0; k0 < n; k0 += 4) {  // (k0 .. k0 + 3 lie in one group of 32)
+      const int c = k0 >> 5;
+      const float wc = c == 0 ? w[0] : c == 1 ? w[1] : c == 2 ? w[2] : w[3];
+      float4 v[4][4];
+      float wk[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int k = k0 + u;
+        wk[u] = __shfl_sync(0xffffffffu, wc, k & 31);
+        if (k < n) {
+          const float4* src = reinterpret_cast<const float4*>(tmp_o + ((size_t)(gr.tmp_begin + k) * kHeads + h) * kDv);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) v[u][j] = __ldcg(src + lane + 32 * j);
+        } else {
+          wk[u] = 0.f;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) v[u][j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          acc[j] = make_float4(fmaf(wk[u], v[u][j].x, acc[j].x), fmaf(wk[u], v[u][j].y, acc[j].y),
+                               fmaf(wk[u], v[u][j].z, acc[j].z), fmaf(wk[u], v[u][j].w, acc[j].w));
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    float4* dst = reinterpret_cast<float4*>(o + ((size_t)rg * kHeads + h) * kDv);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      dst[lane + 32 * j] = make_float4(acc[j].x * inv, acc[j].y * inv, acc[j].z * inv, acc[j].w * inv);
+    if (lane == 0 && lse_out) lse_out[(size_t)rg * kHeads + h] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1103,6 +1103,7 @@ cudaError_t launch_mla(const dcp_attn_desc& d, const void* q, const ShardSet& sh
                        cudaStream_t st, float* o, float* lse_out) {
   const bool f8 = d.kv_dtype == DCP_KV_FP8_E4M3;
   if (n_ctas <= 0 || (f8 ? mla_clusters<true>() : mla_clusters<false>()) <= 0) return cudaErrorNotSupported;
+  if (o && n_ctas > kFinishMax) return cudaErrorNotSupported;  // a row group's pieces must fit the finish kernel
   MlaParams p;
   memset(&p, 0, sizeof(p));
   if (!f8) {  // the 8-bit kernel copies its pages with plain bulk copies and loads its query itself
@@ -1127,6 +1128,17 @@ cudaError_t launch_mla(const dcp_attn_desc& d, const void* q, const ShardSet& sh
     mla_partial_kernel<true><<<2 * n_ctas, kThreads, MlaLayout<true>::kSmemBytes, st>>>(p);
   else
     mla_partial_kernel<false><<<2 * n_ctas, kThreads, MlaLayout<false>::kSmemBytes, st>>>(p);
+  if (o) {
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess)
+      return cudaErrorUnknown;
+    // the list's length is on the device: a grid for up to ~4 rows per warp
+    // at the 8-sequence size, and an immediate exit when the list is empty
+    mla_finish_kernel<<<4 * sms, kFinishThreads, 0, st>>>(static_cast<const char*>(ws), L, o, lse_out);
+  }
   return cudaGetLastError();
 }
 

@@ -8,6 +8,9 @@
 //   cta_begin  CTA c processes items [cta_begin[c], cta_begin[c+1])
 //   groups[r]  (group order only) the CTA runs row group r spans, its
 //              workspace rows, and zeroed piece counters
+//   finish     (group order only) the row groups the MLA one-call path
+//              finishes in a kernel of its own: no tokens, or more than
+//              kMlaMergeInKernel pieces
 // CTA c's tiles are [c*T/S, (c+1)*T/S) of the T tiles laid end to end, so the
 // CTAs' loads differ by at most one tile.
 #include <climits>
@@ -101,6 +104,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(RangeSpec rs, int la
   ItemRec* items = reinterpret_cast<ItemRec*>(ws + L.items_off);
   int* cta_begin = reinterpret_cast<int*>(ws + L.cta_off);
   GroupRec* groups = reinterpret_cast<GroupRec*>(ws + L.grp_off);
+  int* finish = reinterpret_cast<int*>(ws + L.fin_off);
+  long long n_finish = 0;
 
   const int n_lanes = rs.B * rs.N * lanes_per_unit;
   const int group_lanes = rs.N * lanes_per_unit;  // lanes of one row group
@@ -170,15 +175,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(RangeSpec rs, int la
       *first = e > a ? cta_of(a, T, S) : 0;
       return e > a ? cta_of(e - 1, T, S) - *first + 1 : 0;
     };
-    long long my_rows = 0;
+    auto finished_apart = [](int n) { return n == 0 || n > kMlaMergeInKernel; };
+    long long my_rows = 0, my_fin = 0;
     for (int r = g0; r < g1; ++r) {
       int first;
       const int n = span(r, &first);
       if (n > 1) my_rows += n;
+      if (finished_apart(n)) ++my_fin;
     }
     Scan2 tot3;
-    Scan2 pre3 = block_exclusive_scan2(Scan2{my_rows, 0}, &tot3);
-    long long row = pre3.a;
+    Scan2 pre3 = block_exclusive_scan2(Scan2{my_rows, my_fin}, &tot3);
+    long long row = pre3.a, fin = pre3.b;
     for (int r = g0; r < g1; ++r) {
       GroupRec gr;
       gr.pieces = span(r, &gr.first_cta);
@@ -188,7 +195,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(RangeSpec rs, int la
       gr.pad2[0] = gr.pad2[1] = 0;
       groups[r] = gr;
       if (gr.pieces > 1) row += gr.pieces;
+      if (finished_apart(gr.pieces)) finish[fin++] = r;
     }
+    n_finish = tot3.b;
     __syncthreads();
   }
 
@@ -230,6 +239,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(RangeSpec rs, int la
     hdr->n_lanes = n_lanes;
     hdr->n_ctas = n_ctas;
     hdr->total_tiles = (int)T;
+    hdr->n_finish = (int)n_finish;
   }
 }
 

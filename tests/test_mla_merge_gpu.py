@@ -1,10 +1,12 @@
 """The one-call MLA path (dcp_attention_all): the attention kernel merges the
 shards itself. A CTA pair carries one online softmax through the consecutive
 shards of a query row group; row groups cut by a CTA-run boundary leave
-pieces in the workspace that the CTA completing the group merges. Checked
-against the float64 oracle on shapes that produce every kind of row group:
-one piece (many short sequences), many pieces (long sequences over few CTA
-runs), empty shards, empty row groups, multi-token steps, the 8-bit cache."""
+pieces in the workspace, which the CTA completing the group merges (up to
+four pieces) or a short finishing kernel merges (more pieces; it also writes
+the groups without tokens). Checked against the float64 oracle on shapes
+that produce every kind of row group: one piece (many short sequences), two
+to four pieces, many pieces (long sequences over few CTA runs), empty shards,
+empty row groups, multi-token steps, the 8-bit cache."""
 import numpy as np
 import pytest
 import torch
@@ -26,6 +28,8 @@ CASES = [
     ("mla_decode", 1, dict(batch=300, shards=2, ctx_kind="lognormal", median=90, sigma=0.8,
                            ctx_lo=1, ctx_hi=400)),                                    # most groups in one run
     ("mla_decode", 1, dict(batch=2, ctx_kind="fixed", ctx_fixed=40000, shards=8)),    # ~40 pieces a group
+    ("mla_decode", 1, dict(batch=25, ctx_kind="fixed", ctx_fixed=2000, shards=4)),    # 3-4 pieces: in the kernel
+    ("mla_decode", 1, dict(batch=40, ctx_kind="fixed", ctx_fixed=2000, shards=4)),    # 2-3 pieces
     ("mla_decode", 1, dict(batch=2, ctx_kind="fixed", ctx_fixed=5000, shards=3, scale=1.0)),  # peaky
     ("mla_decode", 1, dict(batch=3, ctx_kind="fixed", ctx_fixed=3000, shards=4, needles=3)),  # planted keys
     ("mla_decode", 1, dict(batch=2, ctx_kind="fixed", ctx_fixed=900, shards=2, scale=-0.0417)),  # negative scale

@@ -275,17 +275,26 @@ DCP_API int dcp_decode_partial_all_mtp(const dcp_attn_desc* desc, const void* q,
                                        size_t ws_bytes, int32_t* dev_err_flag, void* stream);
 
 /* Steps 2 and 3 in one call: the partial attention of every shard (as
- * dcp_decode_partial_all_mtp; q_len = 1 for a decode step) followed by one
- * pass that merges, for every output row, the pieces of all N shards -- the
- * shard's partial row, or the pieces of a shard range the balanced split cut
- * across several CTAs -- by the LSE reweighting of dcp_merge. Same result as
- * dcp_decode_partial_all_mtp + dcp_merge, one kernel launch fewer, and the
- * split pieces are read once instead of being combined into o_parts first.
- * (The pages merge the shards' partials after the per-shard attention --
- * Qiita write-up, section "トークンの区間でGPUに割り振る", third step; this
- * joins the two on one GPU.)
+ * dcp_decode_partial_all_mtp; q_len = 1 for a decode step) and the merge of
+ * the shards by the LSE reweighting of dcp_merge. (The pages merge the
+ * shards' partials after the per-shard attention -- Qiita write-up, section
+ * "トークンの区間でGPUに割り振る", third step; this joins the two on one GPU,
+ * keeping the intermediate results in reused buffers or on chip as
+ * "Inference Systems Infrastructure Notes (7): DCP", section 3, does with its
+ * scratch buffer.) Same result as dcp_decode_partial_all_mtp + dcp_merge
+ * within the parity bar:
+ *   GQA: after the attention kernel, one pass merges every output row's
+ *        pieces -- the shard's partial row, or the pieces of a shard range the
+ *        balanced split cut across several CTAs.
+ *   MLA: the attention kernel merges the shards itself. A CTA pair carries one
+ *        online softmax through consecutive shards of a query row (the shards
+ *        meet inside the softmax's rescaling), rows cut by a CTA-run boundary
+ *        leave pieces in the workspace, merged by the CTA completing their
+ *        count (up to 4 pieces) or by a short finishing kernel; o_parts and
+ *        lses are not touched. Results are deterministic for a given device,
+ *        problem and workspace.
  *   o_parts, lses  device fp32 scratch [N, B, q_len, Hq, Dv] / [N, B, q_len, Hq]
- *                  (partial rows of shards whose range one CTA covered)
+ *                  (GQA: partial rows of shards whose range one CTA covered)
  *   o        device fp32 [B, q_len, num_q_heads, head_dim_v] (out)
  *   lse_out  device fp32 [B, q_len, num_q_heads] (out) or NULL
  *   workspace >= dcp_workspace_size_mtp(desc, B, q_len, N) bytes

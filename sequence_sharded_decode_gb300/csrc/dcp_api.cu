@@ -198,12 +198,15 @@ static int run_partial(const dcp_attn_desc* desc, const Path& path, const void* 
   const LaneGeom& g = path.lg;
   // MLA with o: the attention kernel merges the shards itself
   const bool mla_merge = d.kind == DCP_KIND_MLA && o != nullptr;
-  if (launch_plan(rs, g.lanes_per_unit, g.tile, n_ctas, ws, L, d.kind == DCP_KIND_MLA, st) != cudaSuccess)
+  // many-row GQA: gangs of CTAs over the token groups of one KV range
+  const int gang = path.tc ? gqa_tc_gang((rs.qlen + rs.tpr - 1) / rs.tpr, n_ctas) : 1;
+  if (launch_plan(rs, g.lanes_per_unit, g.tile, n_ctas / gang, ws, L, d.kind == DCP_KIND_MLA, gang, st) !=
+      cudaSuccess)
     return DCP_ERR_CUDA;
   cudaError_t e;
   if (d.kind == DCP_KIND_MLA)
     e = launch_mla(d, q, sh, rs, o_parts, lses, ws, L, n_ctas, err, st, mla_merge ? o : nullptr, lse_out);
-  else if (path.tc) e = launch_gqa_tc(d, q, sh, rs, o_parts, lses, ws, L, n_ctas, err, st);
+  else if (path.tc) e = launch_gqa_tc(d, q, sh, rs, o_parts, lses, ws, L, n_ctas, gang, err, st);
   else e = launch_gqa(d, q, sh, rs, o_parts, lses, ws, L, n_ctas, err, st);
   if (e == cudaErrorNotSupported) return DCP_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return DCP_ERR_CUDA;

@@ -16,8 +16,12 @@
 // heads of the KV head (row r = token slot r / g, head r % g), taken as NB
 // blocks of 128 rows that share every K/V tile (NB = 2 once a step has 256
 // rows per KV head: two groups of four softmax warps then work on the two
-// blocks in turn while the tensor cores serve the other). Per 64-token tile
-// of the lane's range, for each block:
+// blocks in turn while the tensor cores serve the other). The token groups of
+// one (shard, sequence, KV head) read the same K/V; gangs of up to eight CTAs
+// take consecutive groups over the same items (the union of their ranges;
+// each row is masked at its own token), so the gang reads each tile at about
+// the same time and L2 serves all but the first read. Per 64-token tile of
+// the lane's range, for each block:
 //   1. S = Q . K^T (M=128 rows, N=64 tokens, K=128) into TMEM, the queries
 //      being the MMA's A operand in TMEM
 //   2. online softmax per row (thread r owns TMEM lane r), causal at the
@@ -107,27 +111,32 @@ struct TcParams {
   int g;      // query heads per KV head
   int Hq, Hkv, Bs;
   int box;    // rows of a copy box: min(block_size, 64)
+  int gang;   // CTAs that run the same items, one token group each
+  int n_gangs;
   float sl2;  // scale * log2(e)
 };
 
-// Geometry of one work item, derived identically by every role.
+// Geometry of one work item for member m of the gang (token group m of the
+// item's gang of lanes), derived identically by every role.
 struct ItemGeom {
   int lane, shard, b, tg, kvh, t0, t1, out_row, lo, hi, start;
 };
-__device__ __forceinline__ ItemGeom item_geom(const TcParams& p, int k) {
+__device__ __forceinline__ ItemGeom item_geom(const TcParams& p, int k, int m) {
   const ItemRec it = reinterpret_cast<const ItemRec*>(p.ws + p.L.items_off)[k];
-  const LaneRec ln = reinterpret_cast<const LaneRec*>(p.ws + p.L.lanes_off)[it.lane];
+  const int lane = it.lane + m * p.Hkv;
+  const LaneRec ln = reinterpret_cast<const LaneRec*>(p.ws + p.L.lanes_off)[lane];
   ItemGeom g;
-  g.lane = it.lane;
-  const int u = it.lane / p.Hkv;
-  g.kvh = it.lane - u * p.Hkv;
+  g.lane = lane;
+  const int u = lane / p.Hkv;
+  g.kvh = lane - u * p.Hkv;
   g.shard = u / p.B;
   const int rg = u - g.shard * p.B;
   g.b = rg / p.G;
   g.tg = rg - g.b * p.G;
   g.t0 = it.t0;
   g.t1 = it.t1;
-  g.out_row = it.out_row;
+  // a split range's pieces: this lane's rows, one per item of the gang
+  g.out_row = it.out_row >= 0 ? ln.tmp_begin + (k - ln.item_begin) : -1;
   g.lo = ln.lo;
   g.hi = ln.hi;
   g.start = ln.start;
@@ -178,8 +187,12 @@ __global__ void __launch_bounds__(TcCfg<NB>::kThreads, 1) gqa_tc_kernel(const __
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // the plan's work runs belong to gangs of p.gang CTAs; member m of a gang
+  // takes token group m of every item (CTAs past the last gang idle)
   const int* cta_begin = reinterpret_cast<const int*>(p.ws + p.L.cta_off);
-  const int k_begin = cta_begin[blockIdx.x], k_end = cta_begin[blockIdx.x + 1];
+  const int gang_id = blockIdx.x / p.gang, member = blockIdx.x - gang_id * p.gang;
+  const int k_begin = gang_id < p.n_gangs ? cta_begin[gang_id] : 0;
+  const int k_end = gang_id < p.n_gangs ? cta_begin[gang_id + 1] : 0;
   const int pieces = kTile / p.box;  // copy boxes per tile (1, 2 or 4)
 
   if (warp == C::kCopyWarp) {
@@ -189,7 +202,7 @@ __global__ void __launch_bounds__(TcCfg<NB>::kThreads, 1) gqa_tc_kernel(const __
     uint32_t fills = 0;
     bool stop = false;
     for (int k = k_begin; k < k_end && !stop; ++k) {
-      const ItemGeom g = item_geom(p, k);
+      const ItemGeom g = item_geom(p, k, member);
       const int32_t* table = p.sh.table[g.shard] + (size_t)g.b * p.sh.max_blocks[g.shard];
       const int local_hi = g.hi - g.start;
       for (int j = 0; j < g.t1 - g.t0; ++j) {
@@ -382,7 +395,7 @@ __global__ void __launch_bounds__(TcCfg<NB>::kThreads, 1) gqa_tc_kernel(const __
     int n_items = 0;
     bool ok = true;
     for (int k = k_begin; k < k_end && ok; ++k) {
-      const ItemGeom g = item_geom(p, k);
+      const ItemGeom g = item_geom(p, k, member);
       const int nt = g.t1 - g.t0;
       const int jt = g.tg * p.tpr + js_row;  // this row's query token
       const bool active = jt < p.qlen;
@@ -679,11 +692,23 @@ int gqa_tc_ctas(const dcp_attn_desc& d, const DeviceInfo&, int qlen) {
   return blocks_for(d, qlen) == 2 ? tc_ctas_cached<2>() : tc_ctas_cached<1>();
 }
 
+// Gang size for a step with `token_groups` lanes per (shard, sequence, KV
+// head): the largest divisor up to 8. A prefill chunk's token groups all
+// stream the same context; a CTA running them one after the other re-read it
+// from HBM once per group (256-token chunks: 12.6x the unique KV bytes), a
+// gang of CTAs runs them side by side and L2 serves the repeats.
+int gqa_tc_gang(int token_groups, int n_ctas) {
+  for (int c = token_groups < 8 ? token_groups : 8; c > 1; --c)
+    if (token_groups % c == 0 && c <= n_ctas) return c;
+  return 1;
+}
+
 cudaError_t launch_gqa_tc(const dcp_attn_desc& d, const void* q, const ShardSet& sh, const RangeSpec& rs,
-                          float* o_parts, float* lses, void* ws, const WsLayout& L, int n_ctas, int32_t* err,
-                          cudaStream_t st) {
+                          float* o_parts, float* lses, void* ws, const WsLayout& L, int n_ctas, int gang,
+                          int32_t* err, cudaStream_t st) {
   const int nb = blocks_for(d, rs.qlen);
-  if (n_ctas <= 0 || (nb == 2 ? tc_ctas_cached<2>() : tc_ctas_cached<1>()) <= 0) return cudaErrorNotSupported;
+  if (n_ctas <= 0 || gang < 1 || n_ctas < gang || (nb == 2 ? tc_ctas_cached<2>() : tc_ctas_cached<1>()) <= 0)
+    return cudaErrorNotSupported;
   static_assert(sizeof(TcParams) <= 32000, "kernel parameters");
   TcParams p;
   memset(&p, 0, sizeof(p));
@@ -710,6 +735,8 @@ cudaError_t launch_gqa_tc(const dcp_attn_desc& d, const void* q, const ShardSet&
   p.Hkv = d.num_kv_heads;
   p.Bs = d.block_size;
   p.box = box;
+  p.gang = gang;
+  p.n_gangs = n_ctas / gang;
   p.sl2 = d.scale * kLog2e;
   if (nb == 2)
     gqa_tc_kernel<2><<<n_ctas, TcCfg<2>::kThreads, TcCfg<2>::kSmemBytes, st>>>(p);

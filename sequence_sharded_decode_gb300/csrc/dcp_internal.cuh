@@ -128,9 +128,13 @@ LaneGeom lane_geom(const dcp_attn_desc& d);
 
 // Kernel launchers (return the launch's cudaError_t).
 // group_order: lay the lanes out row group by row group, fill the group
-// records and the finish list (MLA); otherwise shard by shard.
+// records and the finish list (MLA); otherwise shard by shard. gang > 1 (the
+// many-row GQA kernel; gang divides the token groups per sequence): n_ctas
+// counts gangs of `gang` CTAs, and a work unit is `gang` lanes of
+// consecutive token groups of one (shard, sequence, KV head) over the union
+// of their ranges, each CTA of the gang taking one lane.
 cudaError_t launch_plan(const RangeSpec& rs, int lanes_per_unit, int tile, int n_ctas,
-                        void* ws, const WsLayout& L, bool group_order, cudaStream_t st);
+                        void* ws, const WsLayout& L, bool group_order, int gang, cudaStream_t st);
 cudaError_t launch_gqa(const dcp_attn_desc& d, const void* q, const ShardSet& sh, const RangeSpec& rs,
                        float* o_parts, float* lses, void* ws, const WsLayout& L, int n_ctas,
                        int32_t* err, cudaStream_t st);
@@ -148,9 +152,11 @@ int mla_ctas(const dcp_attn_desc& d, const DeviceInfo& di);
 bool gqa_tc_eligible(const dcp_attn_desc& d, int qlen);
 int gqa_tc_rows_tokens(const dcp_attn_desc& d, int qlen);  // query tokens per lane: 128 or 256 rows / g
 int gqa_tc_ctas(const dcp_attn_desc& d, const DeviceInfo& di, int qlen);
+// gang: CTAs per gang of the plan (n_ctas CTAs, n_ctas / gang gangs).
+int gqa_tc_gang(int token_groups, int n_ctas);
 cudaError_t launch_gqa_tc(const dcp_attn_desc& d, const void* q, const ShardSet& sh, const RangeSpec& rs,
-                          float* o_parts, float* lses, void* ws, const WsLayout& L, int n_ctas, int32_t* err,
-                          cudaStream_t st);
+                          float* o_parts, float* lses, void* ws, const WsLayout& L, int n_ctas, int gang,
+                          int32_t* err, cudaStream_t st);
 cudaError_t launch_combine(const dcp_attn_desc& d, const LaneGeom& lg, const RangeSpec& rs, int n_lanes,
                            const void* ws, const WsLayout& L, float* o_parts, float* lses, cudaStream_t st);
 // Steps 2 and 3 joined: merges every output row's pieces across the shards

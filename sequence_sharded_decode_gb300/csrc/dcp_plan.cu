@@ -12,7 +12,10 @@
 //              finishes in a kernel of its own: no tokens, or more than
 //              kMlaMergeInKernel pieces
 // CTA c's tiles are [c*T/S, (c+1)*T/S) of the T tiles laid end to end, so the
-// CTAs' loads differ by at most one tile.
+// CTAs' loads differ by at most one tile. With gangs (the many-row GQA kernel:
+// `gang` token groups of one KV range), a "CTA" of the plan is a gang of CTAs
+// that run the same items, each on its own token group's lane, so the gang
+// reads every K/V tile at about the same time and it leaves HBM about once.
 #include <climits>
 
 #include "dcp_internal.cuh"
@@ -98,7 +101,8 @@ __device__ __forceinline__ long long cta_start(long long c, long long T, long lo
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(RangeSpec rs, int lanes_per_unit, int tile,
-                                                            int n_ctas, char* ws, WsLayout L, int group_order) {
+                                                            int n_ctas, char* ws, WsLayout L, int group_order,
+                                                            int gang) {
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   LaneRec* lanes = reinterpret_cast<LaneRec*>(ws + L.lanes_off);
   ItemRec* items = reinterpret_cast<ItemRec*>(ws + L.items_off);
@@ -109,34 +113,59 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(RangeSpec rs, int la
 
   const int n_lanes = rs.B * rs.N * lanes_per_unit;
   const int group_lanes = rs.N * lanes_per_unit;  // lanes of one row group
-  // the lane at layout position x: shard by shard (x itself), or row group by
-  // row group (x = (r * N + shard) * lanes_per_unit + j)
+  const int G = (rs.qlen + rs.tpr - 1) / rs.tpr;  // token groups per sequence
+  const int n_work = n_lanes / gang;              // laid-out work units: lanes, or gangs of lanes
+  // the (first) lane of the work unit at layout position x: shard by shard (x
+  // itself), row group by row group (x = (r * N + shard) * lanes_per_unit + j),
+  // or (gang > 1) gang by gang: the lanes of token groups kb * gang .. kb *
+  // gang + gang - 1 of one (shard, sequence, KV head), lanes_per_unit apart
   auto lane_at = [&](int x) {
-    if (!group_order) return x;
-    const int r = x / group_lanes, rem = x - r * group_lanes;
-    const int i = rem / lanes_per_unit, j = rem - i * lanes_per_unit;
-    return (i * rs.B + r) * lanes_per_unit + j;
+    if (group_order) {
+      const int r = x / group_lanes, rem = x - r * group_lanes;
+      const int i = rem / lanes_per_unit, j = rem - i * lanes_per_unit;
+      return (i * rs.B + r) * lanes_per_unit + j;
+    }
+    if (gang == 1) return x;
+    const int kvh = x % lanes_per_unit, rest = x / lanes_per_unit;
+    const int per_seq = G / gang, sb = rest / per_seq, kb = rest - sb * per_seq;  // sb = shard * seqs + b
+    return (sb * G + kb * gang) * lanes_per_unit + kvh;
   };
-  const int per = (n_lanes + kPlanThreads - 1) / kPlanThreads;
+  const int per = (n_work + kPlanThreads - 1) / kPlanThreads;
   const int x0 = threadIdx.x * per;
-  const int x1 = min(n_lanes, x0 + per);
+  const int x1 = min(n_work, x0 + per);
 
-  // pass 1: ranges and tile counts
+  // pass 1: ranges and tile counts. A gang's lanes (one KV range, causal
+  // limits a token group apart) all take the union of their non-empty ranges:
+  // their rows are masked at their own tokens' limits anyway.
   long long my_tiles = 0;
   for (int x = x0; x < x1; ++x) {
-    const int l = lane_at(x);
-    int lo, hi, start;
-    unit_range(rs, l / lanes_per_unit, &lo, &hi, &start);
+    const int l0 = lane_at(x);
+    int lo_u = 0, hi_u = 0, start_u = 0;
+    bool any = false;
+    for (int m = 0; m < gang; ++m) {
+      int lo, hi, start;
+      unit_range(rs, (l0 + m * lanes_per_unit) / lanes_per_unit, &lo, &hi, &start);
+      if (hi > lo) {
+        lo_u = any ? min(lo_u, lo) : lo;
+        hi_u = any ? max(hi_u, hi) : hi;
+        start_u = start;
+        any = true;
+      } else if (m == 0) {
+        lo_u = lo;
+        hi_u = hi;
+        start_u = start;
+      }
+    }
     LaneRec r;
-    r.lo = lo;
-    r.hi = hi;
-    r.start = start;
-    r.tiles = (hi - lo + tile - 1) / tile;
+    r.lo = lo_u;
+    r.hi = hi_u;
+    r.start = start_u;
+    r.tiles = (hi_u - lo_u + tile - 1) / tile;
     r.item_begin = 0;
     r.n_items = 0;
     r.tmp_begin = 0;
     r.pad = 0;
-    lanes[l] = r;
+    for (int m = 0; m < gang; ++m) lanes[l0 + m * lanes_per_unit] = r;
     my_tiles += r.tiles;
   }
   Scan2 tot;
@@ -146,17 +175,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(RangeSpec rs, int la
   // CTA's run is empty and every item covers at least one tile.
   const long long S = T < n_ctas ? (T > 0 ? T : 1) : n_ctas;
 
-  // pass 2: items per lane (number of CTA runs the lane overlaps)
+  // pass 2: items per work unit (number of CTA runs it overlaps)
   long long p = pre.a, my_items = 0, my_split = 0;
   for (int x = x0; x < x1; ++x) {
     const int l = lane_at(x);
     const int t = lanes[l].tiles;
     int n = 0;
     if (t > 0) n = cta_of(p + t - 1, T, S) - cta_of(p, T, S) + 1;
-    lanes[l].n_items = n;
+    for (int m = 0; m < gang; ++m) lanes[l + m * lanes_per_unit].n_items = n;
     lanes[l].pad = (int)p;  // tile prefix, used below and in pass 3
     my_items += n;
-    if (n > 1) my_split += n;
+    if (n > 1) my_split += (long long)n * gang;
     p += t;
   }
   Scan2 tot2;
@@ -201,16 +230,19 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(RangeSpec rs, int la
     __syncthreads();
   }
 
-  // pass 3: items
+  // pass 3: items (a gang's items name its first lane; lane m of the gang
+  // keeps its split pieces in workspace rows tmp_begin + m * n_items ..)
   long long ib = pre2.a, tb = pre2.b;
   for (int x = x0; x < x1; ++x) {
     const int l = lane_at(x);
     LaneRec r = lanes[l];
     const long long P = r.pad;
     r.item_begin = (int)ib;
-    r.tmp_begin = (int)tb;
     r.pad = 0;
-    lanes[l] = r;
+    for (int m = 0; m < gang; ++m) {
+      r.tmp_begin = (int)(tb + (long long)m * r.n_items);
+      lanes[l + m * lanes_per_unit] = r;
+    }
     if (r.n_items > 0) {
       const int c0 = cta_of(P, T, S);
       for (int j = 0; j < r.n_items; ++j) {
@@ -228,7 +260,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(RangeSpec rs, int la
       }
     }
     ib += r.n_items;
-    if (r.n_items > 1) tb += r.n_items;
+    if (r.n_items > 1) tb += (long long)r.n_items * gang;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -246,9 +278,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(RangeSpec rs, int la
 }  // namespace
 
 cudaError_t launch_plan(const RangeSpec& rs, int lanes_per_unit, int tile, int n_ctas, void* ws,
-                        const WsLayout& L, bool group_order, cudaStream_t st) {
+                        const WsLayout& L, bool group_order, int gang, cudaStream_t st) {
   plan_kernel<<<1, kPlanThreads, 0, st>>>(rs, lanes_per_unit, tile, n_ctas, static_cast<char*>(ws), L,
-                                          group_order ? 1 : 0);
+                                          group_order ? 1 : 0, gang);
   return cudaGetLastError();
 }
 

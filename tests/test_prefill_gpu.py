@@ -29,7 +29,9 @@ def test_prefill_chunk_matches_oracle(name, chunk, over):
 
 
 # Steps with q_len * g >= 128 query rows per KV head (GQA, head dim 128)
-# take the tcgen05 kernel: lanes of 128 rows = 128/g tokens x g heads.
+# take the tcgen05 kernel: lanes of 128 rows = 128/g tokens x g heads; the
+# token groups of one KV range run on gangs of up to 8 CTAs (2, 3, 4, 6 and 8
+# below).
 TC_CASES = [
     ("gqa_mid", 8, dict(batch=2, ctx_fixed=700, shards=2)),                             # g=16: 8 tokens per lane
     ("gqa_mid", 20, dict(batch=2, ctx_fixed=1000, shards=3)),                           # a partial last token group
@@ -49,6 +51,9 @@ TC_CASES = [
     ("gqa_mid", 3, dict(batch=2, q_heads=128, kv_heads=1, ctx_fixed=500, shards=3)),    # g=128: one token per block
     ("gqa_mid", 32, dict(batch=2, ctx_kind="lognormal", median=400, sigma=1.0, ctx_lo=0, ctx_hi=2000,
                          shards=32)),                                                   # the most shards, many empty
+    ("gqa_mid", 128, dict(batch=2, ctx_fixed=6000, shards=2)),     # gangs of 8 CTAs; their ranges cut across runs
+    ("gqa_mid", 96, dict(batch=3, ctx_kind="lognormal", median=900, sigma=1.0, ctx_lo=0, ctx_hi=4000,
+                         shards=3)),                                                    # gangs of 6, ragged
 ]
 
 

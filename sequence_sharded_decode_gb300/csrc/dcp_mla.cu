@@ -114,21 +114,31 @@ constexpr int kCodesPage = kTile * kDk;          // 8-bit cache: one page of E4M
 // of the other CTA's value dims (dims 256 (1-r) .. 256 (1-r) + 255), which this
 // CTA reads only in the score MMA: one P buffer per stage, so writing P never
 // waits for the previous tile's P.V.
-// The 8-bit cache (F8) rings pages of E4M3 codes instead (36 KB per stage,
-// one bulk copy each, no multicast), and the softmax warps widen each page,
-// exactly, into one fp16 page laid out like the bf16 boxes (kOffF16), which
-// the fp16 MMAs read; its P then lives in that page's dead boxes.
+// The 8-bit cache (F8) copies pages of E4M3 codes instead (36 KB, one bulk
+// copy each, no multicast) into a one-page codes stage, and the softmax warps
+// widen each page, exactly, into fp16 boxes laid out like the bf16 ones: the
+// five boxes only the score reads (the other CTA's value dims and dims
+// 512-575) into one shared region, this CTA's four value boxes into one of
+// two value slots by page parity. P has a buffer of its own. So page g + 1
+// can be widened as soon as page g's scores are read -- its score then runs
+// while page g's softmax does -- the value slot it needs having been freed by
+// the P.V of page g - 1.
 constexpr int kNumBars = 23;
 template <bool F8>
 struct MlaLayout {
-  static constexpr int kStage = F8 ? kCodesPage : kStageBytes;  // one ring stage
-  static constexpr int kOffF16 = kOffKv + kStages * kStage;      // F8: the widened page
-  static constexpr int kOffQ = F8 ? kOffF16 + kStageBytes : kOffF16;
+  static constexpr int kRing = F8 ? 1 : kStages;                 // copy stages
+  static constexpr int kStage = F8 ? kCodesPage : kStageBytes;  // one copy stage
+  static constexpr int kOffSh = kOffKv + kRing * kStage;          // F8: the score-only boxes (5)
+  static constexpr int kOffV = kOffSh + (F8 ? 5 * kKvChunkBytes : 0);  // F8: own value boxes, 2 x 4
+  static constexpr int kOffP = kOffV + (F8 ? 8 * kKvChunkBytes : 0);   // F8: P (hi, lo)
+  static constexpr int kOffQ = kOffP + (F8 ? 2 * kPBytes : 0);
   static constexpr int kOffBar = kOffQ + kQSmemChunks * kQChunkBytes;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // TMEM slot, abort flag, residual votes (per stage)
   static constexpr int kOffLx = kOffMisc + 128;            // row-sum halves exchanged at the end of an item
   static constexpr int kOffMw = kOffLx + 2 * kHeads * 4;   // one-call path: merge weights [8 warps][16 heads][4]
   static constexpr int kSmemBytes = kOffMw + kSoftmaxWarps * 16 * kMlaMergeInKernel * 4 + 1024;  // + base alignment
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(kOffSh % 1024 == 0 && kOffV % 1024 == 0 && kOffP % 1024 == 0 && kOffQ % 1024 == 0, "swizzle atoms");
 };
 
 // barrier slots
@@ -140,8 +150,8 @@ constexpr int BQ_FULL = 0, BQ_EMPTY = 1, BS_FULL = 2, BS_EMPTY = 3, BP_EMPTY = 4
               BKV_FULL = 7, BKV_EMPTY = 7 + kStages, BXCH = 7 + 2 * kStages,  // BXCH: one per lane quadrant
               BDRAIN2 = BXCH + 4, BP_FULL = 16,  // BP_FULL + stage: the tile's P is in its stage
               BQT = BP_FULL + kStages,           // the copy of the query tail landed
-              BF_FULL = BQT + 1,                 // F8: the widened page is in place
-              BF_EMPTY = BQT + 2,                // F8: the widened page's P.V finished
+              BF_FULL = BQT + 1,                 // F8: the page's widened boxes are in place
+              BF_EMPTY = BQT + 2,                // (unused)
               BPC = BQT + 3,                     // one-call path: every softmax thread's piece rows are out
               BGO = BQT + 4;                     // one-call path: the piece is counted (merge or not)
 static_assert(BDRAIN2 + 1 <= BP_FULL && BGO + 1 <= kNumBars, "barrier slots");
@@ -345,7 +355,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_partial_kernel(const __grid_constant__ MlaParams p) {
   using Lay = MlaLayout<F8>;
   constexpr int kOffQ = Lay::kOffQ, kOffBar = Lay::kOffBar, kOffMisc = Lay::kOffMisc, kOffLx = Lay::kOffLx;
-  constexpr int kStage = Lay::kStage, kOffF16 = Lay::kOffF16;
+  constexpr int kStage = Lay::kStage, kRing = Lay::kRing;
+  constexpr int kOffSh = Lay::kOffSh, kOffV = Lay::kOffV, kOffP = Lay::kOffP;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = saddr(smem_raw);
   unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -368,7 +379,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) bar_init(bar(BP_EMPTY + s), 1);
     bar_init(bar(BDRAIN), 1);
     bar_init(bar(BDRAIN2), 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kRing; ++s) {
       bar_init(bar(BKV_FULL + s), 1);
       // bf16: the P.V of both CTAs (the page lands in both); F8: the widening of the codes
       bar_init(bar(BKV_EMPTY + s), F8 ? kSoftmaxThreads : 2);
@@ -441,7 +452,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           phys_pf = jp < nt ? ((jp >> 5) == (j >> 5) ? a : b2) : -1;
         }
         if (lane == 0) {
-          const uint32_t s = fills % kStages, use = fills / kStages;
+          const uint32_t s = fills % kRing, use = fills / kRing;
           if (use > 0 && !wait_bar(bar(BKV_EMPTY + s), (use - 1) & 1u, abort_flag, p.err, false)) {
             ok = false;
           } else {
@@ -480,8 +491,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // (the other CTA's copies into this one land on the same barriers; it
       // can be at most one page ahead, which may never complete here: the
       // poll bound ends that wait)
-      const uint32_t f0 = fills > (uint32_t)kStages ? fills - kStages : 0;
-      for (uint32_t f = f0; f < fills + 1; ++f) drain_bar(bar(BKV_FULL + f % kStages), (f / kStages) & 1u);
+      const uint32_t f0 = fills > (uint32_t)kRing ? fills - kRing : 0;
+      for (uint32_t f = f0; f < fills + 1; ++f) drain_bar(bar(BKV_FULL + f % kRing), (f / kRing) & 1u);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ score MMA issuer
@@ -491,8 +502,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // of waiting for all its 36 MMAs.
     {
       const uint32_t id_s = idesc(128, 64, 0, F8);
-      const uint64_t kdesc0 = sdesc(sbase + (F8 ? kOffF16 : kOffKv), 0);
+      const uint64_t kdesc0 = sdesc(sbase + (F8 ? kOffSh : kOffKv), 0);
       const uint64_t qdesc0 = sdesc(sbase + kOffQ, 0);
+      // F8: this CTA's value boxes of even / odd pages
+      const uint64_t vdesc_e = sdesc(sbase + kOffV, 0), vdesc_o = sdesc(sbase + kOffV + 4 * kKvChunkBytes, 0);
       auto n_tiles = [&](int k) {
         const ItemRec it = reinterpret_cast<const ItemRec*>(p.ws + p.L.items_off)[k];
         return it.t1 - it.t0;
@@ -514,9 +527,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tc_fence_after();
           // descriptors advance by (byte offset >> 4) in their address field
           const uint64_t kd = kdesc0 + (F8 ? 0ull : (uint64_t)((s * kStageBytes) >> 4));
+          const uint64_t kv = (g_s & 1u) ? vdesc_o : vdesc_e;
 #pragma unroll
           for (int kk = 0; kk < kKSteps; ++kk) {
-            const uint64_t bdesc = kd + (uint64_t)((((kk >> 2) * kKvChunkBytes) + 32 * (kk & 3)) >> 4);
+            const int box = kk >> 2;
+            uint64_t bdesc;
+            if constexpr (F8) {
+              // this CTA's value boxes in the page's value slot; the other
+              // CTA's value boxes and box 8 (slot 4) in the shared region
+              const bool own = (box >> 2) == (int)rank;
+              const int slot = box == 8 ? 4 : (box & 3);
+              bdesc = (own ? kv : kd) + (uint64_t)((slot * kKvChunkBytes + 32 * (kk & 3)) >> 4);
+            } else {
+              bdesc = kd + (uint64_t)(((box * kKvChunkBytes) + 32 * (kk & 3)) >> 4);
+            }
             if (kk < kKStepsTmem) {
               mma_ts(tmem + kColS, tmem + kColQ + 8 * kk, bdesc, id_s, kk > 0);
             } else {
@@ -560,9 +584,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // behind on either barrier and its parity waits are unambiguous.
     {
       const uint32_t id_pv = idesc(128, 256, 1, F8);
-      const uint32_t pbase = sbase + (F8 ? kOffF16 : kOffKv);  // the page the MMAs read
-      const uint64_t pdesc0 = sdesc(pbase + 4 * (1 - rank) * kKvChunkBytes, 0);
-      const uint64_t vdesc0 = sdesc(pbase + 4 * rank * kKvChunkBytes, kKvChunkBytes);
+      // bf16: P in the stage's dead boxes, V in the stage; F8: P in its own
+      // buffer, V in the page parity's value slot
+      const uint64_t pdesc0 = sdesc(F8 ? sbase + kOffP : sbase + kOffKv + 4 * (1 - rank) * kKvChunkBytes, 0);
+      const uint64_t vdesc0 = sdesc(F8 ? sbase + kOffV : sbase + kOffKv + 4 * rank * kKvChunkBytes, kKvChunkBytes);
       auto n_tiles = [&](int k) {
         const ItemRec it = reinterpret_cast<const ItemRec*>(p.ws + p.L.items_off)[k];
         return it.t1 - it.t0;
@@ -575,9 +600,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t s = g_p % kStages;
         if (bar_test_warp(bar(BP_FULL + s), (g_p / kStages) & 1u)) {
           tc_fence_after();
-          const uint64_t soff = F8 ? 0ull : (uint64_t)((s * kStageBytes) >> 4);
-          const uint64_t vd = vdesc0 + soff;  // V dims of this CTA
-          const uint64_t pd = pdesc0 + soff;  // P of this tile
+          const uint64_t soff = (uint64_t)((s * kStageBytes) >> 4);
+          const uint64_t vd = vdesc0 + (F8 ? (uint64_t)(((g_p & 1u) * 4 * kKvChunkBytes) >> 4) : soff);  // V dims of this CTA
+          const uint64_t pd = pdesc0 + (F8 ? 0ull : soff);  // P of this tile
           int any_lo = 0;
 #pragma unroll
           for (int w = 0; w < kSoftmaxWarps; ++w) any_lo |= lo_flags[kSoftmaxWarps * s + w];
@@ -590,10 +615,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               mma_ss(tmem + kColO, pd + (uint64_t)((term * kPBytes + 32 * kt) >> 4),
                   vd + (uint64_t)((2048 * kt) >> 4), id_pv, (jp == 0 && !acc_in && term == 0 && kt == 0) ? 0 : 1);
           }
-          if (F8)
-            mma_commit(bar(BF_EMPTY));  // the widened page may be overwritten
-          else
-            mma_commit_mc(bar(BKV_EMPTY + s), 0x3);  // the stage is free in both CTAs once both P.V finished
+          if (!F8) mma_commit_mc(bar(BKV_EMPTY + s), 0x3);  // the stage is free in both CTAs once both P.V finished
+          // (F8: the value slot and P may be overwritten)
           mma_commit(bar(BP_EMPTY + s));  // also tells softmax that this P.V finished
           if (++jp == ntp) {
             ++kp;
@@ -634,6 +657,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t n_pc = 0;       // pieces counted (one-call path)
     float m_run = -INFINITY, l_half = 0.f;
     volatile int* merge_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 96);
+    // F8: widen page G's codes (in the codes stage) to fp16, exactly (E4M3 is
+    // a subset of fp16): part 0 the score-only boxes into the shared region,
+    // part 1 this CTA's value boxes into the value slot of G's parity. Rows
+    // past the range (or of an unusable table entry) become zeros, so that no
+    // value can carry NaN bits. Four threads per row (thread = row 4r + q),
+    // 16 codes per load: codes 16 (q + 4i) .. + 15 -> box i, 16-byte chunks
+    // 2q, 2q + 1.
+    auto widen = [&](uint32_t G, int n_rows, int part) {
+      const int r = threadIdx.x >> 2, q4 = threadIdx.x & 3;
+      const uint32_t src = sbase + kOffKv + r * kDk + 16 * q4;
+      const uint32_t sw = (uint32_t)(r & 7), ch = 2u * (uint32_t)q4;
+      const uint32_t c0 = (ch ^ sw) << 4, c1 = ((ch + 1) ^ sw) << 4;
+      const bool live = r < n_rows;
+      // part 0: the other CTA's value boxes 4 (1 - rank) + i (i < 4), then
+      // box 8 (i = 4), into slots i of the shared region; part 1: this CTA's
+      // value boxes 4 rank + i into the value slot of G's parity
+      const int n = part == 0 ? 5 : 4;
+      const uint32_t dst0 = (part == 0 ? sbase + kOffSh : sbase + kOffV + (G & 1u) * 4 * kKvChunkBytes) + r * 128;
+      const int box0 = part == 0 ? 4 * (1 - (int)rank) : 4 * (int)rank;
+#pragma unroll
+      for (int i = 0; i < 5; ++i) {
+        if (i >= n) break;
+        const int box = (part == 0 && i == 4) ? 8 : box0 + i;
+        const uint32_t dst = dst0 + i * kKvChunkBytes;
+        uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        if (live) {
+          const uint4 c = lds128_u32(src + 64 * box);
+          e4m3x4_to_f16x4(c.x, w[0], w[1]);
+          e4m3x4_to_f16x4(c.y, w[2], w[3]);
+          e4m3x4_to_f16x4(c.z, w[4], w[5]);
+          e4m3x4_to_f16x4(c.w, w[6], w[7]);
+        }
+        st_shared_v4(dst + c0, w[0], w[1], w[2], w[3]);
+        st_shared_v4(dst + c1, w[4], w[5], w[6], w[7]);
+      }
+    };
     bool ok = true;
     for (int k = k_begin; k < k_end && ok; ++k) {
       const ItemGeom g = item_geom(p, k);
@@ -687,41 +746,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int t = g.t0 + j;
         const int phys = tile_block(p, g, t);  // its latency hides behind the score wait
         if constexpr (F8) {
-          // 0. widen the page's codes to fp16, exactly (E4M3 is a subset of
-          // fp16), into the page the MMAs read, once the previous page's P.V
-          // has finished with it; rows past the range (or of an unusable
-          // table entry) become zeros, so that no value can carry NaN bits
-          const int n_rows = phys < 0 ? 0 : min(kTile, g.hi - (g.lo + kTile * t));
-          if (gi >= 1 && !wait_warp(bar(BF_EMPTY), (gi - 1) & 1u, abort_flag, p.err, false)) { ok = false; break; }
-          if (!wait_warp(bar(BKV_FULL + s), (gi / kStages) & 1u, abort_flag, p.err, false)) { ok = false; break; }
-          // four threads per row (thread = row 4r + q), 16 codes per load:
-          // codes 16 g .. 16 g + 15 -> box g / 4, 16-byte chunks 2 (g % 4), +1
-          {
-            const int r = threadIdx.x >> 2, q4 = threadIdx.x & 3;
-            const uint32_t src = sbase + kOffKv + s * kStage + r * kDk;
-            const uint32_t dst = sbase + kOffF16 + r * 128;
-            const uint32_t sw = (uint32_t)(r & 7);
-            const bool live = r < n_rows;
-#pragma unroll 3
-            for (int i = 0; i < kDk / 64; ++i) {
-              const int g16 = q4 + 4 * i;  // 0 .. 35
-              uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-              if (live) {
-                const uint4 c = lds128_u32(src + 16 * g16);
-                e4m3x4_to_f16x4(c.x, w[0], w[1]);
-                e4m3x4_to_f16x4(c.y, w[2], w[3]);
-                e4m3x4_to_f16x4(c.z, w[4], w[5]);
-                e4m3x4_to_f16x4(c.w, w[6], w[7]);
-              }
-              const uint32_t box = dst + (g16 >> 2) * kKvChunkBytes;
-              const uint32_t ch = 2u * (uint32_t)(g16 & 3);
-              st_shared_v4(box + ((ch ^ sw) << 4), w[0], w[1], w[2], w[3]);
-              st_shared_v4(box + (((ch + 1) ^ sw) << 4), w[4], w[5], w[6], w[7]);
-            }
+          if (gi == 0) {  // 0. the run's first page is widened before its score
+            const int n_rows = phys < 0 ? 0 : min(kTile, g.hi - (g.lo + kTile * t));
+            if (!wait_warp(bar(BKV_FULL), 0u, abort_flag, p.err, false)) { ok = false; break; }
+            widen(0u, n_rows, 0);
+            widen(0u, n_rows, 1);
+            asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+            bar_arrive(bar(BF_FULL));
+            bar_arrive(bar(BKV_EMPTY));  // the codes' stage may be refilled
           }
-          asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-          bar_arrive(bar(BF_FULL));
-          bar_arrive(bar(BKV_EMPTY + s));  // the codes' stage may be refilled
         }
         // 1. scores of the tile: all 64 for the maximum, this warp's 32 for P
         if (!wait_warp(bar(BS_FULL), gi & 1u, abort_flag, p.err, false)) { ok = false; break; }
@@ -734,6 +767,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         tc_fence_before();
         bar_arrive(bar(BS_EMPTY));
+        if constexpr (F8) {
+          // 1b. widen the next page (this item's next tile, or the next
+          // item's first) now, so that its score runs during this page's
+          // softmax: the score-only boxes at once (this page's score has
+          // finished with them), this CTA's value boxes once the P.V of the
+          // page before this one has finished with their slot
+          int tn = -1;
+          ItemGeom gn = g;
+          if (j + 1 < nt) {
+            tn = t + 1;
+          } else if (k + 1 < k_end) {
+            gn = item_geom(p, k + 1);
+            tn = gn.t0;
+          }
+          if (tn >= 0) {
+            const uint32_t G = gi + 1;
+            const int physn = tile_block(p, gn, tn);
+            const int n_rows = physn < 0 ? 0 : min(kTile, gn.hi - (gn.lo + kTile * tn));
+            if (!wait_warp(bar(BKV_FULL), G & 1u, abort_flag, p.err, false)) { ok = false; break; }
+            widen(G, n_rows, 0);
+            if (G >= 2 && !wait_warp(bar(BP_EMPTY + (G & 1u)), ((G - 2) >> 1) & 1u, abort_flag, p.err, false)) {
+              ok = false;
+              break;
+            }
+            widen(G, n_rows, 1);
+            asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+            bar_arrive(bar(BF_FULL));
+            bar_arrive(bar(BKV_EMPTY));  // the codes' stage may be refilled
+          }
+        }
         // 2. online softmax (log2 units). The maximum of scale * s is taken as
         // scale * max(s) (or * min(s) for a negative scale): one multiply.
         const int n_valid = phys < 0 ? 0 : min(kTile, g.hi - (g.lo + kTile * t));
@@ -800,10 +863,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // 128 rows, so when any warp asks for it, every row must be current.
         const bool any_lo = __any_sync(0xffffffffu, lsum > kLoFraction * l_half);
         // 3. P into its stage (the score MMA that read those boxes has finished;
-        // F8: into the widened page, as fp16 terms)
+        // F8: into the P buffer, as fp16 terms, once the previous page's P.V
+        // has finished with it -- mostly already waited for by the widening)
+        if (F8 && gi >= 1 &&
+            !wait_warp(bar(BP_EMPTY + (gi - 1) % kStages), ((gi - 1) / kStages) & 1u, abort_flag, p.err, false)) {
+          ok = false;
+          break;
+        }
         {
-          const uint32_t hrow = (F8 ? sbase + kOffF16 : sbase + kOffKv + s * kStageBytes) +
-                                4 * (1 - rank) * kKvChunkBytes + h * 128;
+          const uint32_t hrow =
+              (F8 ? sbase + kOffP : sbase + kOffKv + s * kStageBytes + 4 * (1 - rank) * kKvChunkBytes) + h * 128;
           const uint32_t lrow = hrow + kPBytes;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {

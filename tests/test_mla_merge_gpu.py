@@ -23,6 +23,8 @@ RAGGED = dict(ctx_kind="lognormal", median=900, sigma=1.0, ctx_lo=1, ctx_hi=6000
 CASES = [
     ("mla_decode", 1, dict(batch=2, ctx_kind="fixed", ctx_fixed=300, shards=4)),
     ("mla_decode", 1, dict(batch=1, ctx_kind="fixed", ctx_fixed=0, shards=2)),        # one token
+    ("mla_decode", 1, dict(batch=2, ctx_kind="fixed", ctx_fixed=63, shards=1)),       # one shard, one tile
+    ("mla_decode", 1, dict(batch=3, ctx_kind="fixed", ctx_fixed=9000, shards=1)),     # one shard over several runs
     ("mla_decode", 1, dict(batch=5, shards=8, **RAGGED)),                             # ragged, partial tiles
     ("mla_decode", 1, dict(batch=3, shards=32, ctx_kind="fixed", ctx_fixed=700)),     # many empty shards
     ("mla_decode", 1, dict(batch=300, shards=2, ctx_kind="lognormal", median=90, sigma=0.8,

@@ -62,18 +62,23 @@
 // waits are unambiguous; every wait is bounded: on expiry the kernel raises
 // DCP_DEVERR_TIMEOUT, stops all roles, drains what it issued and frees TMEM.
 //
+// The plan lays each query row group's N shard lanes next to each other, so
+// consecutive items of a CTA pair mostly share their query: it stays in place
+// (and the next row group's query is pulled into L2 one item ahead).
+//
 // One-call path (o non-NULL; step 3 joined to step 2, "Inference Systems
 // Infrastructure Notes (7): DCP", section 3: intermediate results stay in
-// reused buffers -- here, on chip): the plan lays each query row group's N
-// shard lanes next to each other, and a CTA pair whose run holds several
-// shards of a row group carries one online softmax through them -- the
-// running maximum, row sums and O simply continue from one shard's tiles to
-// the next, which is the LSE reweighting of the merge done as it goes, and the
-// query stays in place. A row group whose tiles lie in one CTA run is written
-// to o directly; one cut by a run boundary leaves one normalised piece (and
-// its LSE) per run in the workspace, each CTA then counts its piece with an
-// atomic, and the CTA whose count completes the group merges the pieces of
-// its value dims (the same reweighting) into o. No CTA ever waits for another.
+// reused buffers -- here, on chip): a CTA pair whose run holds several shards
+// of a row group carries one online softmax through them -- the running
+// maximum, row sums and O simply continue from one shard's tiles to the next,
+// which is the LSE reweighting of the merge done as it goes. A row group whose
+// tiles lie in one CTA run is written to o directly; one cut by run
+// boundaries leaves one normalised piece (and its LSE) per run in the
+// workspace. Up to kMlaMergeInKernel pieces, each CTA counts its piece with an
+// atomic and the CTA whose count completes the group merges the pieces of its
+// value dims (the same reweighting) into o; groups cut into more pieces, and
+// groups without tokens, are finished by mla_finish_kernel over the whole GPU.
+// No CTA ever waits for another.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -123,7 +128,7 @@ constexpr int kCodesPage = kTile * kDk;          // 8-bit cache: one page of E4M
 // can be widened as soon as page g's scores are read -- its score then runs
 // while page g's softmax does -- the value slot it needs having been freed by
 // the P.V of page g - 1.
-constexpr int kNumBars = 23;
+constexpr int kNumBars = 22;
 template <bool F8>
 struct MlaLayout {
   static constexpr int kRing = F8 ? 1 : kStages;                 // copy stages
@@ -151,9 +156,8 @@ constexpr int BQ_FULL = 0, BQ_EMPTY = 1, BS_FULL = 2, BS_EMPTY = 3, BP_EMPTY = 4
               BDRAIN2 = BXCH + 4, BP_FULL = 16,  // BP_FULL + stage: the tile's P is in its stage
               BQT = BP_FULL + kStages,           // the copy of the query tail landed
               BF_FULL = BQT + 1,                 // F8: the page's widened boxes are in place
-              BF_EMPTY = BQT + 2,                // (unused)
-              BPC = BQT + 3,                     // one-call path: every softmax thread's piece rows are out
-              BGO = BQT + 4;                     // one-call path: the piece is counted (merge or not)
+              BPC = BQT + 2,                     // one-call path: every softmax thread's piece rows are out
+              BGO = BQT + 3;                     // one-call path: the piece is counted (merge or not)
 static_assert(BDRAIN2 + 1 <= BP_FULL && BGO + 1 <= kNumBars, "barrier slots");
 
 constexpr uint32_t kTmemCols = 512;
@@ -386,7 +390,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int q4 = 0; q4 < 4; ++q4) bar_init(bar(BXCH + q4), 64);  // the two warps of a lane quadrant
     bar_init(bar(BF_FULL), kSoftmaxThreads);
-    bar_init(bar(BF_EMPTY), 1);
     bar_init(bar(BPC), kSoftmaxThreads);
     bar_init(bar(BGO), 1);
     *abort_flag = 0;

@@ -28,6 +28,7 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLoFraction = 1.0f / 32.0f;  // F8: tile share of a row's weight above which P_lo . V is issued
 
 // F8: the cache holds FP8 E4M3 codes (1 byte per element) instead of bf16;
 // a stage is then half as large. kMinCtas: with head dim 128 the 8-bit
@@ -42,6 +43,11 @@ __device__ __forceinline__ void mma16816_f16(float* d, const uint32_t* a, uint32
       "{%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t f16x2_rn(float x0, float x1) {
+  const __half2 h = __floats2half2_rn(x0, x1);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // hi = fp16(x), lo = fp16(x - hi), packed in pairs for an A fragment
@@ -422,8 +428,10 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads, (GqaCfg<D, F8, T>::kMinCt
         p_[h][2] = exp2f(s[h][2] - r1);
         p_[h][3] = exp2f(s[h][3] - r1);
       }
-      l0 = l0 * a0 + (p_[0][0] + p_[0][1] + p_[1][0] + p_[1][1]);
-      l1 = l1 * a1 + (p_[0][2] + p_[0][3] + p_[1][2] + p_[1][3]);
+      const float t0 = p_[0][0] + p_[0][1] + p_[1][0] + p_[1][1];
+      const float t1 = p_[0][2] + p_[0][3] + p_[1][2] + p_[1][3];
+      l0 = l0 * a0 + t0;
+      l1 = l1 * a1 + t1;
       // once the running maxima settle, a0 = a1 = 1 exactly: skip the rescale
       if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
@@ -438,11 +446,26 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads, (GqaCfg<D, F8, T>::kMinCt
       // carries ~16 mantissa bits of P instead of bf16's 8, so the partial
       // of a short shard (few tokens, |O| ~ |v|) keeps fp32-level accuracy.
       uint32_t pa[4], pl[4];
+      // F8 (P in fp16: the hi term alone keeps 11 bits): the residual P.V is
+      // issued only for tiles that carry more than 1/32 of some row's running
+      // weight (the first tiles of a lane, or a dominant token); elsewhere
+      // dropping it changes O by at most 2^-11 x that share x max|v|. Each
+      // lane's partial tile sums bound its rows' (the quad adds them up), so
+      // judging per lane is conservative; the vote keeps the warp uniform.
+      bool any_lo = true;
       if constexpr (F8) {
-        split_f16(p_[0][0], p_[0][1], pa[0], pl[0]);
-        split_f16(p_[0][2], p_[0][3], pa[1], pl[1]);
-        split_f16(p_[1][0], p_[1][1], pa[2], pl[2]);
-        split_f16(p_[1][2], p_[1][3], pa[3], pl[3]);
+        any_lo = __any_sync(0xffffffffu, t0 > kLoFraction * l0 || t1 > kLoFraction * l1);
+        if (any_lo) {
+          split_f16(p_[0][0], p_[0][1], pa[0], pl[0]);
+          split_f16(p_[0][2], p_[0][3], pa[1], pl[1]);
+          split_f16(p_[1][0], p_[1][1], pa[2], pl[2]);
+          split_f16(p_[1][2], p_[1][3], pa[3], pl[3]);
+        } else {
+          pa[0] = f16x2_rn(p_[0][0], p_[0][1]);
+          pa[1] = f16x2_rn(p_[0][2], p_[0][3]);
+          pa[2] = f16x2_rn(p_[1][0], p_[1][1]);
+          pa[3] = f16x2_rn(p_[1][2], p_[1][3]);
+        }
       } else {
         split_bf16(p_[0][0], p_[0][1], pa[0], pl[0]);
         split_bf16(p_[0][2], p_[0][3], pa[1], pl[1]);
@@ -458,7 +481,7 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads, (GqaCfg<D, F8, T>::kMinCt
           uint32_t b0, b1;
           e4m3x4_to_f16x4(w, b0, b1);
           mma16816_f16(o[nd], pa, b0, b1);
-          mma16816_f16(o[nd], pl, b0, b1);
+          if (any_lo) mma16816_f16(o[nd], pl, b0, b1);
         }
       } else {
         const int mi = lane >> 3;

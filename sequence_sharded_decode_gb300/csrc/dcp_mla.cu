@@ -181,6 +181,7 @@ constexpr float kLoFraction = 1.0f / 32.0f;      // tile share of the row sum ab
 struct MlaParams {
   CUtensorMap tm_q;
   CUtensorMap tm_kv[kMaxShards];
+  CUtensorMap tm_kv4[kMaxShards];  // token-split kernel: four 64-column boxes of a half page in one copy
   ShardSet sh;
   const __nv_bfloat16* q;
   const char* ws;
@@ -1112,6 +1113,695 @@ __global__ void __launch_bounds__(kFinishThreads) mla_finish_kernel(const char* 
 }
 
 // ---------------------------------------------------------------------------
+// Token-split pair kernel (bf16 cache)
+// ---------------------------------------------------------------------------
+// The same results as mla_partial_kernel<false>, with a page's work divided
+// differently between the two CTAs of the pair. CTA r still accumulates value
+// dims [256 r, 256 r + 256) of O, but scores only its own 32 tokens of each
+// 64-token page (tokens 32 r .. 32 r + 31): S_r = Q . K_r^T (M = 128, N = 32,
+// K = 576). The row maxima of the two halves and the two halves of P are
+// exchanged through distributed shared memory, and each CTA's P.V runs over
+// all 64 tokens. The score is no longer computed twice, and a CTA holds only
+// what it reads: its own 32 tokens in full (for its score) plus the other 32
+// tokens' rows of its own value dims (for P.V) -- 52 KB per page instead of
+// 72 KB -- so three stages fit where two did. Per page and CTA:
+//   1. the copies: its own tokens' value dims and dims 512-575 (private),
+//      its own tokens' other value dims, which the other CTA needs for P.V
+//      (one multicast copy into both CTAs, at the same slots), and the other
+//      CTA's multicast of its tokens' rows of this CTA's value dims
+//   2. S_r into TMEM (query dims 0-447 as the A operand in TMEM, 448-575 in
+//      shared memory)
+//   3. the row maximum of the own 32 tokens, sent to the other CTA; both then
+//      take the maximum of the two halves and run the same lazy rescale, so
+//      their running maxima stay equal without further talk
+//   4. P of the own tokens as two bf16 terms (hi, lo) into the slots that
+//      only the score read; hi is sent to the other CTA with one bulk copy,
+//      lo only when a tile carries a noticeable share of some row's weight
+//      (the other CTA is told by a flag, and its lo buffer is a single slot
+//      it releases after use)
+//   5. O_r += P . V_r over both token halves
+// At the end of an output row group the two CTAs' row sums are exchanged the
+// same way. Every wait is bounded, as in mla_partial_kernel.
+namespace ts {
+constexpr int kStages = 3;
+constexpr int kHalf = 32;                          // tokens of a page per CTA
+constexpr int kBox = kHalf * 128;                  // 64 columns x 32 rows of bf16: 4 KB
+constexpr int kSlots = 14;                         // boxes per stage
+constexpr int kStage = kSlots * kBox;              // 56 KB
+// slots of a stage: 0-3 tokens 0-31 x dims 256-511 (copied by CTA 0 into
+// both), 4-7 tokens 32-63 x dims 0-255 (copied by CTA 1 into both), 8-11 the
+// own tokens x the own value dims, 12 the own tokens x dims 512-575, 13 spare.
+// After the score, CTA r's slots 4r .. 4r + 3 hold P_hi (two token halves of
+// 8 KB: its own and the other CTA's) and slots 12-13 its own P_lo.
+constexpr int kSlotOwnV = 8, kSlotRope = 12, kSlotLo = 12;
+constexpr int kPHalf = kHeads * kHalf * 2;         // 8 KB: 128 heads x 32 tokens of bf16
+constexpr int kKStepsTmem = 28;                    // query dims 0-447 in TMEM
+constexpr int kQChunks = 2;                        // query dims 448-575 in shared memory
+constexpr uint32_t kColO = 0, kColS = 256, kColQ = 288;  // 256 + 32 + 224 columns
+constexpr int kOffKv = 0;
+constexpr int kOffQ = kOffKv + kStages * kStage;
+constexpr int kOffLoPeer = kOffQ + kQChunks * kQChunkBytes;  // the other CTA's P_lo half
+constexpr int kOffBar = kOffLoPeer + kPHalf;
+constexpr int kNumBars = 40;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;   // TMEM slot, abort, merge flag, P flags, lo votes
+constexpr int kOffMx = kOffMisc + 256;             // [stage][head]: the other CTA's row maxima
+constexpr int kOffLx = kOffMx + kStages * kHeads * 4;  // [2][head]: row-sum halves of this CTA
+constexpr int kOffLp = kOffLx + 2 * kHeads * 4;        // [2][head]: the other CTA's row sums
+constexpr int kOffMw = kOffLp + 2 * kHeads * 4;        // merge weights
+constexpr int kSmemBytes = kOffMw + kSoftmaxWarps * 16 * kMlaMergeInKernel * 4 + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+static_assert(kStage % 1024 == 0 && kOffQ % 1024 == 0 && kOffLoPeer % 1024 == 0, "swizzle atoms");
+constexpr int B_QFULL = 0, B_QEMPTY = 1, B_QT = 2, B_SFULL = 3, B_SEMPTY = 4, B_LOFREE = 5, B_DRAIN = 6,
+              B_DRAIN2 = 7, B_PC = 8, B_GO = 9, B_XCH = 10 /* + quadrant */, B_LX = 14 /* + parity */,
+              B_KVFULL = 16, B_KVEMPTY = B_KVFULL + kStages, B_MX = B_KVEMPTY + kStages,
+              B_POWN = B_MX + kStages, B_PPEER = B_POWN + kStages, B_PEMPTY = B_PPEER + kStages,
+              B_PLO = B_PEMPTY + kStages;  // the other CTA's P_lo half landed
+static_assert(B_PLO + 1 <= kNumBars, "barrier slots");
+
+// slot of 64-column box c (0-8) of CTA r's own tokens
+__device__ __forceinline__ int score_slot(int c, int r) {
+  return c == 8 ? kSlotRope : (c >> 2) == r ? kSlotOwnV + (c & 3) : 4 * r + (c & 3);
+}
+// first slot of the value rows of token half h for CTA r
+__device__ __forceinline__ int value_slot(int h, int r) { return h == r ? kSlotOwnV : 4 * h; }
+// byte offset of 8-token chunk `chunk` of row `row` in a 128-row x 32-token
+// K-major tile with the 64-byte swizzle: 64-byte rows, the 16-byte chunk
+// index XORed with address bits 7-8 (= (row / 2) % 4)
+__device__ __forceinline__ uint32_t ptile_off(int row, int chunk) {
+  return (uint32_t)(row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
+}
+}  // namespace ts
+
+// Four consecutive 64-column boxes (column blocks z .. z + 3) of 32 rows from
+// y, landing as four consecutive 4 KB boxes (the 3-D map's innermost dims are
+// the 64 columns and the rows, its outer dim the column block)
+__device__ __forceinline__ void tma_load4(uint32_t dst, const CUtensorMap* map, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(y), "r"(z), "r"(bar) : "memory");
+}
+__device__ __forceinline__ void tma_load4_mc(uint32_t dst, const CUtensorMap* map, int y, int z, uint32_t bar,
+                                             uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;\n"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(y), "r"(z), "r"(bar), "h"(cta_mask) : "memory");
+}
+// the same shared-memory offset in CTA `peer` of the cluster
+__device__ __forceinline__ uint32_t peer_addr(uint32_t a, uint32_t peer) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(a), "r"(peer));
+  return r;
+}
+// 4-byte store into another CTA's shared memory that completes as tx bytes
+// on that CTA's mbarrier (no fence or arrival needed by the sender)
+__device__ __forceinline__ void st_async_u32(uint32_t a, uint32_t v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];\n" ::"r"(a), "r"(v), "r"(bar)
+               : "memory");
+}
+// bulk copy from this CTA's shared memory into another CTA's (dst and bar are
+// cluster addresses), completing on that CTA's mbarrier
+__device__ __forceinline__ void bulk_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+               ::"r"(dst), "r"(src), "r"(bytes), "r"(bar) : "memory");
+}
+__device__ __forceinline__ bool bar_test_cluster(uint32_t b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok) : "r"(b), "r"(parity) : "memory");
+  return ok != 0;
+}
+// bounded, polled, warp-uniform wait with cluster-scope acquire (the phase
+// may have been completed by the other CTA)
+__device__ __forceinline__ bool poll_warp_cluster(uint32_t b, uint32_t parity, volatile int* abort_flag,
+                                                  int32_t* err) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (__all_sync(0xffffffffu, bar_test_cluster(b, parity))) return true;
+    if ((i & 63u) == 63u && __any_sync(0xffffffffu, *abort_flag != 0)) return false;
+  }
+  *abort_flag = 1;
+  raise_flag(err, DCP_DEVERR_TIMEOUT);
+  return false;
+}
+// K-major shared-memory descriptor, 64-byte swizzle: 64-byte rows, 8-row
+// groups 512 B apart (a 128-row x 32-token bf16 tile)
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t addr) {
+  uint64_t d = (uint64_t)((addr >> 4) & 0x3FFF);
+  d |= (uint64_t)(512 >> 4) << 32;
+  d |= 1ull << 46;  // descriptor version for tcgen05
+  d |= 4ull << 61;  // 64-byte swizzle
+  return d;
+}
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    mla_split_kernel(const __grid_constant__ MlaParams p) {
+  using namespace ts;
+  // (the names this kernel shares with mla_partial_kernel's constants)
+  constexpr int kStages = ts::kStages, kOffKv = ts::kOffKv, kKStepsTmem = ts::kKStepsTmem;
+  constexpr uint32_t kColO = ts::kColO, kColS = ts::kColS, kColQ = ts::kColQ;
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = saddr(smem_raw);
+  unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  const uint32_t sbase = saddr(smem);
+  const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
+  const int cluster = blockIdx.x >> 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto bar = [&](int i) { return sbase + kOffBar + 8u * i; };
+  auto stage_base = [&](uint32_t s) { return sbase + kOffKv + s * kStage; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 8);
+  volatile int* merge_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 12);
+  volatile int* pflag = reinterpret_cast<volatile int*>(smem + kOffMisc + 16);     // [stage]: the other CTA's lo
+  volatile int* lo_votes = reinterpret_cast<volatile int*>(smem + kOffMisc + 32);  // [stage][softmax warp]
+
+  if (threadIdx.x == 0) {
+    bar_init(bar(B_QFULL), kSoftmaxThreads);
+    bar_init(bar(B_QEMPTY), 1);
+    bar_init(bar(B_QT), 1);
+    bar_init(bar(B_SFULL), 1);
+    bar_init(bar(B_SEMPTY), kSoftmaxThreads);
+    bar_init(bar(B_LOFREE), 1);  // the other CTA's P.V finished with this CTA's lo in its buffer
+    bar_init(bar(B_DRAIN), 1);
+    bar_init(bar(B_DRAIN2), 1);
+    bar_init(bar(B_PC), kSoftmaxThreads);
+    bar_init(bar(B_GO), 1);
+    for (int q4 = 0; q4 < 4; ++q4) bar_init(bar(B_XCH + q4), 64);
+    for (int x = 0; x < 2; ++x) bar_init(bar(B_LX + x), 1);  // the other CTA's row sums (512 bytes)
+    bar_init(bar(B_PLO), 1);
+    for (int s = 0; s < kStages; ++s) {
+      bar_init(bar(B_KVFULL + s), 1);
+      bar_init(bar(B_KVEMPTY + s), 2);           // both CTAs' P.V of the page
+      bar_init(bar(B_MX + s), 1);                // the other CTA's row maxima (512 bytes)
+      bar_init(bar(B_POWN + s), kSoftmaxThreads);
+      bar_init(bar(B_PPEER + s), 1);             // the other CTA's P_hi half and lo flag landed
+      bar_init(bar(B_PEMPTY + s), 1);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(saddr(tmem_slot)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before either writes into the other
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int* cta_begin = reinterpret_cast<const int*>(p.ws + p.L.cta_off);
+  const int k_begin = cta_begin[cluster], k_end = cta_begin[cluster + 1];
+  auto n_tiles = [&](int k) {
+    const ItemRec it = reinterpret_cast<const ItemRec*>(p.ws + p.L.items_off)[k];
+    return it.t1 - it.t0;
+  };
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    uint32_t fills = 0;
+    int q_done = 0;
+    bool stop = false;
+    for (int k = k_begin; k < k_end && !stop; ++k) {
+      const ItemGeom g = item_geom(p, k);
+      const int nt = g.t1 - g.t0;
+      const bool same_q = same_rows(p, k, k_begin);
+      if (lane == 0 && rank == 0 && k + 1 < k_end && !same_rows(p, k + 1, k_begin)) {
+        const int nb = reinterpret_cast<const ItemRec*>(p.ws + p.L.items_off)[k + 1].lane % p.B;
+        l2_prefetch(p.q + (size_t)nb * kHeads * kDk, kHeads * kDk * 2);
+      }
+      int cur = lane < nt ? tile_block(p, g, g.t0 + lane) : -1;
+      int nxt = 32 + lane < nt ? tile_block(p, g, g.t0 + 32 + lane) : -1;
+      bool ok = true;
+      if (lane == 0 && !same_q) {
+        if (q_done > 0 && !wait_bar(bar(B_QEMPTY), (q_done - 1) & 1, abort_flag, p.err, false)) {
+          ok = false;
+        } else {
+          bar_arrive_tx(bar(B_QT), kQChunks * kQChunkBytes);
+          for (int c = 0; c < kQChunks; ++c)
+            tma_load(sbase + kOffQ + c * kQChunkBytes, &p.tm_q, 448 + 64 * c, g.b * kHeads, bar(B_QT));
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) { stop = true; break; }
+      if (!same_q) ++q_done;
+      for (int j = 0; j < nt; ++j) {
+        if ((j & 31) == 0 && j > 0) {
+          cur = nxt;
+          nxt = j + 32 + lane < nt ? tile_block(p, g, g.t0 + j + 32 + lane) : -1;
+        }
+        const int phys = __shfl_sync(0xffffffffu, cur, j & 31);
+        int phys_pf = -1;
+        if (kPrefetch > 0) {
+          const int jp = j + kPrefetch;
+          const int a = __shfl_sync(0xffffffffu, cur, jp & 31), b2 = __shfl_sync(0xffffffffu, nxt, jp & 31);
+          phys_pf = jp < nt ? ((jp >> 5) == (j >> 5) ? a : b2) : -1;
+        }
+        if (lane == 0) {
+          const uint32_t s = fills % kStages, use = fills / kStages;
+          if (use > 0 && !wait_bar(bar(B_KVEMPTY + s), (use - 1) & 1u, abort_flag, p.err, false)) {
+            ok = false;
+          } else {
+            if (phys < 0 && rank == 0) raise_flag(p.err, DCP_DEVERR_BLOCK_RANGE);
+            // rows of this CTA's tokens (an unusable entry reads zeros above row 0)
+            const int row = (phys < 0 ? -kTile : phys * kTile) + kHalf * (int)rank;
+            const uint32_t st = stage_base(s);
+            // 13 boxes land here: 5 private, 4 of this CTA's multicast, 4 of the other's
+            bar_arrive_tx(bar(B_KVFULL + s), 13 * kBox);
+            // the other CTA's value dims of the own tokens (into both CTAs), the
+            // own value dims, dims 512-575
+            tma_load4_mc(st + 4 * rank * kBox, &p.tm_kv4[g.shard], row, 4 * (int)peer, bar(B_KVFULL + s), 0x3);
+            tma_load4(st + kSlotOwnV * kBox, &p.tm_kv4[g.shard], row, 4 * (int)rank, bar(B_KVFULL + s));
+            tma_load(st + kSlotRope * kBox, &p.tm_kv[g.shard], 512, row, bar(B_KVFULL + s));
+            if (kPrefetch > 0 && rank == 0 && phys_pf >= 0)
+              l2_prefetch(static_cast<const char*>(p.sh.k[g.shard]) + (size_t)phys_pf * kStageBytes, kStageBytes);
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) { stop = true; break; }
+        ++fills;
+      }
+    }
+    if (lane == 0 && *abort_flag) {  // copies in flight must land before the CTA may exit
+      if (q_done > 0) drain_bar(bar(B_QT), (q_done - 1) & 1u);
+      const uint32_t f0 = fills > (uint32_t)kStages ? fills - kStages : 0;
+      for (uint32_t f = f0; f < fills + 1; ++f) drain_bar(bar(B_KVFULL + f % kStages), (f / kStages) & 1u);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ score MMA issuer
+    const uint32_t id_s = idesc(128, kHalf, 0);
+    const uint64_t qdesc0 = sdesc(sbase + kOffQ, 0);
+    int ks = k_begin, js = 0, nts = ks < k_end ? n_tiles(ks) : 0;
+    uint32_t g_s = 0, q_loads = 0;
+    bool q_ready = false;
+    uint32_t idle = 0;
+    while (ks < k_end) {
+      bool progressed = false;
+      if (!q_ready && bar_test_warp(bar(B_QFULL), q_loads & 1u) && bar_test_warp(bar(B_QT), q_loads & 1u)) {
+        q_ready = true;
+        tc_fence_after();
+      }
+      const uint32_t s = g_s % kStages;
+      if (q_ready && bar_test_warp(bar(B_KVFULL + s), (g_s / kStages) & 1u) &&
+          (g_s == 0 || bar_test_warp(bar(B_SEMPTY), (g_s - 1) & 1u))) {
+        tc_fence_after();
+        const uint64_t kd = sdesc(stage_base(s), 0);
+#pragma unroll
+        for (int kk = 0; kk < kKSteps; ++kk) {
+          const int box = kk >> 2;
+          const uint64_t bdesc = kd + (uint64_t)((score_slot(box, (int)rank) * kBox + 32 * (kk & 3)) >> 4);
+          if (kk < kKStepsTmem) {
+            mma_ts(tmem + kColS, tmem + kColQ + 8 * kk, bdesc, id_s, kk > 0);
+          } else {
+            const int qk = kk - kKStepsTmem;
+            mma_ss(tmem + kColS, qdesc0 + (uint64_t)((((qk >> 2) * kQChunkBytes) + 32 * (qk & 3)) >> 4), bdesc, id_s,
+                   1);
+          }
+        }
+        mma_commit(bar(B_SFULL));
+        if (++js == nts) {
+          if (!(ks + 1 < k_end && same_rows(p, ks + 1, k_begin))) {
+            mma_commit(bar(B_QEMPTY));
+            ++q_loads;
+            q_ready = false;
+          }
+          ++ks;
+          js = 0;
+          nts = ks < k_end ? n_tiles(ks) : 0;
+        }
+        ++g_s;
+        progressed = true;
+      }
+      if (progressed) {
+        idle = 0;
+      } else if (++idle >= kSpinLimit) {
+        *abort_flag = 1;
+        raise_flag(p.err, DCP_DEVERR_TIMEOUT);
+        break;
+      } else if ((idle & 63u) == 0 && __any_sync(0xffffffffu, *abort_flag != 0)) {
+        break;
+      }
+    }
+    mma_commit(bar(B_DRAIN));
+    drain_bar(bar(B_DRAIN), 0);
+  } else if (warp == kPvWarp) {
+    // ------------------------------------------------------------ P exchange and P.V MMA issuer
+    const uint32_t id_pv = idesc(128, 256, 1);
+    int kp = k_begin, jp = 0, ntp = kp < k_end ? n_tiles(kp) : 0;
+    bool acc_in = false;
+    uint32_t g_p = 0, lo_sent = 0, lo_recv = 0;
+    bool ok = true;
+    while (kp < k_end && ok) {
+      const uint32_t s = g_p % kStages, ph = (g_p / kStages) & 1u;
+      const uint32_t st = stage_base(s);
+      const uint32_t pbase = st + 4 * rank * kBox;  // P_hi: token half h at pbase + h * kPHalf
+      // 0. expect the other CTA's P_hi half and flag for this tile
+      if (lane == 0) bar_arrive_tx(bar(B_PPEER + s), kPHalf + 4);
+      // 1. this CTA's P is in place
+      if (!poll_warp_cluster(bar(B_POWN + s), ph, abort_flag, p.err)) { ok = false; break; }
+      int f_own = 0;
+#pragma unroll
+      for (int w = 0; w < kSoftmaxWarps; ++w) f_own |= lo_votes[kSoftmaxWarps * s + w];
+      // 2. send it: hi always, lo when asked for (into the other CTA's single
+      // lo buffer, once its P.V has finished with the previous one)
+      if (f_own && lo_sent > 0 && !poll_warp_cluster(bar(B_LOFREE), (lo_sent - 1) & 1u, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
+        const uint32_t pb = peer_addr(bar(B_PPEER + s), peer);
+        // the other CTA keeps its P_hi in its slots 4 peer ..; this half goes to token half `rank`
+        bulk_to_peer(peer_addr(st + 4 * peer * kBox + rank * kPHalf, peer), pbase + rank * kPHalf, kPHalf, pb);
+        st_async_u32(peer_addr(sbase + kOffMisc + 16 + 4 * s, peer), (uint32_t)f_own, pb);
+        if (f_own)
+          bulk_to_peer(peer_addr(sbase + kOffLoPeer, peer), st + kSlotLo * kBox, kPHalf, peer_addr(bar(B_PLO), peer));
+      }
+      __syncwarp();
+      if (f_own) ++lo_sent;
+      // 3. the other CTA's half (and its lo, when its flag asks for it)
+      if (!poll_warp_cluster(bar(B_PPEER + s), ph, abort_flag, p.err)) { ok = false; break; }
+      const int f_peer = pflag[s];
+      if (f_peer) {
+        if (lane == 0) bar_arrive_tx(bar(B_PLO), kPHalf);
+        __syncwarp();
+        if (!poll_warp_cluster(bar(B_PLO), lo_recv & 1u, abort_flag, p.err)) { ok = false; break; }
+        ++lo_recv;
+      }
+      tc_fence_after();
+      // 4. O_r += P . V_r over the two token halves
+      bool first = jp == 0 && !acc_in;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint64_t vd = sdesc(st + value_slot(h, (int)rank) * kBox, kBox);
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          mma_ss(tmem + kColO, sdesc_sw64(pbase + h * kPHalf + 32 * kk),
+                 vd + (uint64_t)((2048 * kk) >> 4), id_pv, first ? 0 : 1);
+          first = false;
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const bool own = h == (int)rank;
+        if (!(own ? f_own : f_peer)) continue;
+        const uint32_t lo_tile = own ? st + kSlotLo * kBox : sbase + kOffLoPeer;
+        const uint64_t vd = sdesc(st + value_slot(h, (int)rank) * kBox, kBox);
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+          mma_ss(tmem + kColO, sdesc_sw64(lo_tile + 32 * kk), vd + (uint64_t)((2048 * kk) >> 4),
+                 id_pv, 1);
+      }
+      mma_commit_mc(bar(B_KVEMPTY + s), 0x3);  // the stage is free in both CTAs once both P.V finished
+      mma_commit(bar(B_PEMPTY + s));
+      if (f_peer) {
+        mma_commit_mc(bar(B_LOFREE), (uint16_t)(1u << peer));  // the other CTA may send its next lo
+      }
+      if (++jp == ntp) {
+        ++kp;
+        jp = 0;
+        ntp = kp < k_end ? n_tiles(kp) : 0;
+        acc_in = kp < k_end && continues(p, kp, k_begin);
+      }
+      ++g_p;
+    }
+    if (!ok && lane == 0) {
+      // the other CTA's copies into this one may still be in flight: let the
+      // ones it can have issued land (bounded polls)
+      for (uint32_t f = g_p; f < g_p + kStages; ++f) drain_bar(bar(B_PPEER + f % kStages), (f / kStages) & 1u);
+      drain_bar(bar(B_PLO), lo_recv & 1u);
+    }
+    __syncwarp();
+    mma_commit(bar(B_DRAIN2));
+    drain_bar(bar(B_DRAIN2), 0);
+  } else {
+    // ------------------------------------------------------------ softmax / epilogue
+    // Warp w: TMEM lane quadrant qd = w % 4 (heads 32 qd ..), half e = w / 4:
+    // the own tokens 16 e .. 16 e + 15 for the exponentials and P, and this
+    // CTA's value dims 128 e .. 128 e + 127 of O. Both warps of a quadrant read
+    // all 32 own scores of their rows, so they take the same maximum.
+    const int qd = warp & 3, e = warp >> 2;
+    const int h = 32 * qd + lane;
+    const uint32_t lane_off = (uint32_t)(32 * qd) << 16;
+    const bool pos_scale = p.sl2 >= 0.f;
+    float* lx = reinterpret_cast<float*>(smem + kOffLx);
+    const float* mxp = reinterpret_cast<const float*>(smem + kOffMx);
+    const float* lp = reinterpret_cast<const float*>(smem + kOffLp);
+    uint32_t gt = 0;
+    int n_q = 0, n_epi = 0;
+    uint32_t n_pc = 0;
+    float m_run = -INFINITY, l_half = 0.f;
+    bool ok = true;
+    for (int k = k_begin; k < k_end && ok; ++k) {
+      const ItemGeom g = item_geom(p, k);
+      const int nt = g.t1 - g.t0;
+      if (!same_rows(p, k, k_begin)) {
+        // query dims 224 e .. 224 e + 223 into TMEM, after the previous row group's score MMAs
+        if (n_q > 0 && !wait_warp(bar(B_QEMPTY), (n_q - 1) & 1, abort_flag, p.err, false)) break;
+        tc_fence_after();
+        const uint4* qr = reinterpret_cast<const uint4*>(p.q + ((size_t)g.b * kHeads + h) * kDk + 224 * e);
+        uint32_t qv[16];
+        __syncwarp();
+#pragma unroll 1
+        for (int c = 0; c < 7; ++c) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint4 v = qr[4 * c + i];
+            qv[4 * i] = v.x;
+            qv[4 * i + 1] = v.y;
+            qv[4 * i + 2] = v.z;
+            qv[4 * i + 3] = v.w;
+          }
+          tmem_st16(tmem + lane_off + kColQ + 112 * e + 16 * c, qv);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        bar_arrive(bar(B_QFULL));
+        ++n_q;
+      }
+      if (!continues(p, k, k_begin)) {
+        m_run = -INFINITY;
+        l_half = 0.f;
+      }
+      for (int j = 0; j < nt; ++j) {
+        const uint32_t gi = gt + j, s = gi % kStages, ph = (gi / kStages) & 1u;
+        const uint32_t st = stage_base(s);
+        const int t = g.t0 + j;
+        const int phys = tile_block(p, g, t);
+        const int n_valid = phys < 0 ? 0 : min(kTile, g.hi - (g.lo + kTile * t));
+        const int own0 = kHalf * (int)rank;  // first own token of the tile
+        // 1. the own 32 scores (polled: a suspended wait wakes late)
+        if (!poll_warp_cluster(bar(B_SFULL), gi & 1u, abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t sv[32];
+        __syncwarp();
+        tmem_ld32(tmem + lane_off + kColS, sv);
+        tmem_wait_ld();
+        tc_fence_before();
+        bar_arrive(bar(B_SEMPTY));
+        // 2. the own maximum (of scale * s, as scale * max or min of s), sent
+        float raw_ext = pos_scale ? -INFINITY : INFINITY;
+        if (n_valid - own0 >= kHalf) {  // common case: no masking; a tree for ILP
+          float m4[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float* x = reinterpret_cast<const float*>(sv + 8 * q);
+            m4[q] = pos_scale ? fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])), fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])))
+                              : fminf(fminf(fminf(x[0], x[1]), fminf(x[2], x[3])), fminf(fminf(x[4], x[5]), fminf(x[6], x[7])));
+          }
+          raw_ext = pos_scale ? fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) : fminf(fminf(m4[0], m4[1]), fminf(m4[2], m4[3]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < kHalf; ++i) {
+            const float x = __uint_as_float(sv[i]);
+            if (own0 + i < n_valid) raw_ext = pos_scale ? fmaxf(raw_ext, x) : fminf(raw_ext, x);
+          }
+        }
+        const float mx_own = n_valid > own0 ? raw_ext * p.sl2 : -INFINITY;
+        if (threadIdx.x == 0) bar_arrive_tx(bar(B_MX + s), kHeads * 4);  // expect the other CTA's maxima
+        if (e == 0)
+          st_async_u32(peer_addr(sbase + kOffMx + (s * kHeads + h) * 4, peer), __float_as_uint(mx_own),
+                       peer_addr(bar(B_MX + s), peer));
+        if (!poll_warp_cluster(bar(B_MX + s), ph, abort_flag, p.err)) { ok = false; break; }
+        const float mx = fmaxf(mx_own, mxp[s * kHeads + h]);
+        float m_new = m_run, alpha = 1.f;
+        bool rescale = false;
+        if (m_run == -INFINITY) {
+          m_new = mx;
+        } else if (mx > m_run + kRescaleThreshold) {
+          m_new = mx;
+          alpha = exp2f(m_run - m_new);
+          rescale = true;
+        }
+        const float ref = m_new == -INFINITY ? 0.f : m_new;
+        // 3. P of this warp's 16 own tokens
+        float sc[16];
+        float lsum;
+        {
+          uint32_t mine[16];  // this warp's 16 scores (static register indices)
+          if (e == 0) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) mine[i] = sv[i];
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) mine[i] = sv[16 + i];
+          }
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int tok = own0 + 16 * e + i;
+            const float x = fmaf(__uint_as_float(mine[i]), p.sl2, -ref);
+            sc[i] = tok < n_valid ? ex2_ftz(x) : 0.f;
+            ls[i & 3] += sc[i];
+          }
+          lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        }
+        l_half = l_half * alpha + lsum;
+        m_run = m_new;
+        const bool any_lo = __any_sync(0xffffffffu, lsum > kLoFraction * l_half);
+        {
+          const uint32_t hi_tile = st + 4 * rank * kBox + rank * kPHalf, lo_tile = st + kSlotLo * kBox;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int k2 = 0; k2 < 4; ++k2) split_p_bf16(sc[8 * c + 2 * k2], sc[8 * c + 2 * k2 + 1], hi[k2], lo[k2]);
+            const uint32_t off = ptile_off(h, 2 * e + c);
+            st_shared_v4(hi_tile + off, hi[0], hi[1], hi[2], hi[3]);
+            st_shared_v4(lo_tile + off, lo[0], lo[1], lo[2], lo[3]);
+          }
+          if (lane == 0) lo_votes[kSoftmaxWarps * s + warp] = any_lo ? 1 : 0;
+        }
+        // 4. value rows past the end of a partial tile may hold anything: zero
+        // this CTA's value dims of those rows, in both token halves
+        if (n_valid < kTile) {
+          const int tid = threadIdx.x;
+          for (int x = tid; x < (kTile - n_valid) * 4 * 8; x += kSoftmaxThreads) {
+            const int tok = n_valid + x / 32, c = (x >> 3) & 3, piece = x & 7;
+            const int hh = tok / kHalf, r = tok % kHalf;
+            st_shared_v4(st + (value_slot(hh, (int)rank) + c) * kBox + r * 128 + piece * 16, 0u, 0u, 0u, 0u);
+          }
+        }
+        // 5. lazy rescale of this warp's half of O, after the previous P.V
+        if (__any_sync(0xffffffffu, rescale)) {
+          if (gi >= 1 && !wait_warp(bar(B_PEMPTY + (gi - 1) % kStages), ((gi - 1) / kStages) & 1u, abort_flag, p.err,
+                                    false)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint32_t ov[32];
+          __syncwarp();
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t col = kColO + 128 * e + 32 * c;
+            tmem_ld32(tmem + lane_off + col, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st32(tmem + lane_off + col, ov);
+          }
+          tmem_wait_st();
+        }
+        // 6. publish P (for this CTA's P.V and for the copy to the other CTA)
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        tc_fence_before();
+        bar_arrive(bar(B_POWN + s));
+      }
+      if (!ok) break;
+      if (k + 1 < k_end && continues(p, k + 1, k_begin)) {
+        gt += nt;
+        continue;
+      }
+      // epilogue: this CTA's row sum (two halves), then the other CTA's
+      lx[e * kHeads + h] = l_half;
+      bar_arrive(bar(B_XCH + qd));
+      if (!wait_warp(bar(B_XCH + qd), (uint32_t)n_epi & 1u, abort_flag, p.err, false)) break;
+      const float l_cta = l_half + lx[(1 - e) * kHeads + h];
+      const int px = n_epi & 1;
+      if (threadIdx.x == 0) bar_arrive_tx(bar(B_LX + px), kHeads * 4);
+      if (e == 0)
+        st_async_u32(peer_addr(sbase + kOffLp + (px * kHeads + h) * 4, peer), __float_as_uint(l_cta),
+                     peer_addr(bar(B_LX + px), peer));
+      if (!poll_warp_cluster(bar(B_LX + px), ((uint32_t)n_epi >> 1) & 1u, abort_flag, p.err)) break;
+      const float l_run = l_cta + lp[px * kHeads + h];
+      const uint32_t glast = gt + nt - 1;
+      if (!wait_warp(bar(B_PEMPTY + glast % kStages), (glast / kStages) & 1u, abort_flag, p.err, false)) break;
+      tc_fence_after();
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      float* out;
+      float* out_lse;
+      GroupRec gr;
+      bool piece = false;
+      if (p.o) {
+        gr = reinterpret_cast<const GroupRec*>(p.ws + p.L.grp_off)[g.b];
+        piece = gr.pieces > 1;
+        if (piece) {
+          const size_t row = (size_t)(gr.tmp_begin + cluster - gr.first_cta);
+          out = reinterpret_cast<float*>(const_cast<char*>(p.ws) + p.L.tmp_o_off) + (row * kHeads + h) * kDv;
+          out_lse = reinterpret_cast<float*>(const_cast<char*>(p.ws) + p.L.tmp_lse_off) + row * kHeads + h;
+        } else {
+          out = p.o + ((size_t)g.b * kHeads + h) * kDv;
+          out_lse = p.lse_out ? p.lse_out + (size_t)g.b * kHeads + h : nullptr;
+        }
+      } else if (g.out_row >= 0) {
+        out = reinterpret_cast<float*>(const_cast<char*>(p.ws) + p.L.tmp_o_off) +
+              ((size_t)g.out_row * kHeads + h) * kDv;
+        out_lse = reinterpret_cast<float*>(const_cast<char*>(p.ws) + p.L.tmp_lse_off) + (size_t)g.out_row * kHeads + h;
+      } else {
+        out = p.o_parts + ((size_t)g.u * kHeads + h) * kDv;
+        out_lse = p.lses + (size_t)g.u * kHeads + h;
+      }
+      out += 256 * rank + 128 * e;
+      uint32_t ov[32];
+      __syncwarp();
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(tmem + lane_off + kColO + 128 * e + 32 * c, ov);
+        tmem_wait_ld();
+        float4* o4 = reinterpret_cast<float4*>(out + 32 * c);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          o4[i] = make_float4(__uint_as_float(ov[4 * i]) * inv, __uint_as_float(ov[4 * i + 1]) * inv,
+                              __uint_as_float(ov[4 * i + 2]) * inv, __uint_as_float(ov[4 * i + 3]) * inv);
+      }
+      if (e == 0 && out_lse && (rank == 0 || piece))
+        *out_lse = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+      tc_fence_before();
+      gt += nt;
+      ++n_epi;
+      if (piece && gr.pieces <= kMlaMergeInKernel) {
+        __threadfence();
+        bar_arrive(bar(B_PC));
+        if (threadIdx.x == 0) {
+          int last = 0;
+          if (wait_bar(bar(B_PC), n_pc & 1u, abort_flag, p.err, false)) {
+            __threadfence();
+            GroupRec* grw = reinterpret_cast<GroupRec*>(const_cast<char*>(p.ws) + p.L.grp_off);
+            last = atomicAdd(&grw[g.b].cnt[rank], 1) == gr.pieces - 1 ? 1 : 0;
+            __threadfence();
+          }
+          *merge_flag = last;
+          bar_arrive(bar(B_GO));
+        }
+        if (!wait_warp(bar(B_GO), n_pc & 1u, abort_flag, p.err, false)) break;
+        ++n_pc;
+        if (*merge_flag) {
+          __threadfence();
+          merge_pieces(p, g.b, gr.tmp_begin, gr.pieces, rank, warp, lane, reinterpret_cast<float*>(smem + kOffMw));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols));
+  }
+  cluster_sync();  // neither CTA exits while the other's copies or arrivals may still reach it
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 // 2-D bf16 map over rows of 576 latent/query columns; boxes of 64 columns
@@ -1124,6 +1814,21 @@ bool latent_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_ro
   cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D view of the same rows for the token-split kernel: dims (64 columns,
+// rows, 9 column blocks of 128 bytes), boxes of 64 columns x 32 rows x 4
+// blocks, which land as four consecutive 4 KB boxes.
+bool latent_map4(CUtensorMap* m, const void* base, uint64_t rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {64, rows, 9};
+  cuuint64_t strides[2] = {576 * 2, 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)ts::kHalf, 4};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1164,24 +1869,70 @@ int mla_clusters() {
   return n;
 }
 
+// Co-resident clusters of the token-split kernel (0 on failure), cached.
+int mla_split_clusters() {
+  static std::mutex mu;
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] > 0) return cache[dev];
+  if (cudaFuncSetAttribute(mla_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ts::kSmemBytes) !=
+      cudaSuccess)
+    return 0;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = ts::kSmemBytes;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, mla_split_kernel, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = sms / 2;
+  }
+  cache[dev] = n;
+  return n;
+}
+
+// The bf16 cache runs the token-split kernel (1) or the kernel that repeats
+// the score in both CTAs (0).
+#ifndef DCP_MLA_TOKEN_SPLIT
+#define DCP_MLA_TOKEN_SPLIT 1
+#endif
+constexpr bool kTokenSplit = DCP_MLA_TOKEN_SPLIT != 0;
+
 }  // namespace
 
 int mla_ctas(const dcp_attn_desc& d, const DeviceInfo&) {
-  return d.kv_dtype == DCP_KV_FP8_E4M3 ? mla_clusters<true>() : mla_clusters<false>();
+  if (d.kv_dtype == DCP_KV_FP8_E4M3) return mla_clusters<true>();
+  return kTokenSplit ? mla_split_clusters() : mla_clusters<false>();
 }
 
 cudaError_t launch_mla(const dcp_attn_desc& d, const void* q, const ShardSet& sh, const RangeSpec& rs,
                        float* o_parts, float* lses, void* ws, const WsLayout& L, int n_ctas, int32_t* err,
                        cudaStream_t st, float* o, float* lse_out) {
   const bool f8 = d.kv_dtype == DCP_KV_FP8_E4M3;
-  if (n_ctas <= 0 || (f8 ? mla_clusters<true>() : mla_clusters<false>()) <= 0) return cudaErrorNotSupported;
+  const bool split = !f8 && kTokenSplit;
+  if (n_ctas <= 0 || (f8 ? mla_clusters<true>() : split ? mla_split_clusters() : mla_clusters<false>()) <= 0)
+    return cudaErrorNotSupported;
   if (o && n_ctas > kFinishMax) return cudaErrorNotSupported;  // a row group's pieces must fit the finish kernel
   MlaParams p;
   memset(&p, 0, sizeof(p));
   if (!f8) {  // the 8-bit kernel copies its pages with plain bulk copies and loads its query itself
     if (!latent_map(&p.tm_q, q, (uint64_t)rs.B * kHeads, kHeads)) return cudaErrorNotSupported;
-    for (int i = 0; i < rs.N; ++i)
-      if (!latent_map(&p.tm_kv[i], sh.k[i], (uint64_t)sh.nblk[i] * kTile, kTile)) return cudaErrorNotSupported;
+    for (int i = 0; i < rs.N; ++i) {  // boxes of a page (64 rows), or of a CTA's half page (32)
+      if (!latent_map(&p.tm_kv[i], sh.k[i], (uint64_t)sh.nblk[i] * kTile, split ? ts::kHalf : kTile))
+        return cudaErrorNotSupported;
+      if (split && !latent_map4(&p.tm_kv4[i], sh.k[i], (uint64_t)sh.nblk[i] * kTile)) return cudaErrorNotSupported;
+    }
   }
   p.sh = sh;
   p.q = static_cast<const __nv_bfloat16*>(q);
@@ -1198,6 +1949,8 @@ cudaError_t launch_mla(const dcp_attn_desc& d, const void* q, const ShardSet& sh
   p.v_scale = f8 ? d.v_scale : 1.f;
   if (f8)
     mla_partial_kernel<true><<<2 * n_ctas, kThreads, MlaLayout<true>::kSmemBytes, st>>>(p);
+  else if (split)
+    mla_split_kernel<<<2 * n_ctas, kThreads, ts::kSmemBytes, st>>>(p);
   else
     mla_partial_kernel<false><<<2 * n_ctas, kThreads, MlaLayout<false>::kSmemBytes, st>>>(p);
   if (o) {

@@ -1240,6 +1240,16 @@ __device__ __forceinline__ bool wait_warp_cluster(uint32_t b, uint32_t parity, v
   raise_flag(err, DCP_DEVERR_TIMEOUT);
   return false;
 }
+// bounded wait of one thread that polls (test_wait) instead of suspending
+__device__ __forceinline__ bool poll_bar(uint32_t b, uint32_t parity, volatile int* abort_flag, int32_t* err) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (bar_test(b, parity)) return true;
+    if ((i & 63u) == 63u && *abort_flag) return false;
+  }
+  *abort_flag = 1;
+  raise_flag(err, DCP_DEVERR_TIMEOUT);
+  return false;
+}
 // K-major shared-memory descriptor, 64-byte swizzle: 64-byte rows, 8-row
 // groups 512 B apart (a 128-row x 32-token bf16 tile)
 __device__ __forceinline__ uint64_t sdesc_sw64(uint32_t addr) {
@@ -1269,6 +1279,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   volatile int* merge_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 12);
   volatile int* pflag = reinterpret_cast<volatile int*>(smem + kOffMisc + 16);     // [stage]: the other CTA's lo
   volatile int* lo_votes = reinterpret_cast<volatile int*>(smem + kOffMisc + 32);  // [stage][softmax warp]
+  volatile int* pv_issued = reinterpret_cast<volatile int*>(smem + kOffMisc + 128);  // P.V tiles issued
 
   if (threadIdx.x == 0) {
     bar_init(bar(B_QFULL), kSoftmaxThreads);
@@ -1293,6 +1304,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bar_init(bar(B_PEMPTY + s), 1);
     }
     *abort_flag = 0;
+    *pv_issued = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == kMmaWarp) {
@@ -1354,7 +1366,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) {
           const uint32_t s = fills % kStages, use = fills / kStages;
-          if (use > 0 && !wait_bar(bar(B_KVEMPTY + s), (use - 1) & 1u, abort_flag, p.err, false)) {
+          // (polled: the copy should leave as soon as both P.V have freed the stage)
+          if (use > 0 && !poll_bar(bar(B_KVEMPTY + s), (use - 1) & 1u, abort_flag, p.err)) {
             ok = false;
           } else {
             if (phys < 0 && rank == 0) raise_flag(p.err, DCP_DEVERR_BLOCK_RANGE);
@@ -1396,7 +1409,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_after();
       }
       const uint32_t s = g_s % kStages;
-      if (q_ready && bar_test_warp(bar(B_KVFULL + s), (g_s / kStages) & 1u) &&
+      // The score of tile g waits until the P.V of tile g - 2 is in the tensor
+      // pipe (which runs MMAs in issue order): that P.V frees the stage the
+      // copy of tile g + 1 needs, while the score has a tile of slack.
+      if (q_ready && (g_s < 2 || *pv_issued >= (int)g_s - 1) && bar_test_warp(bar(B_KVFULL + s), (g_s / kStages) & 1u) &&
           (g_s == 0 || bar_test_warp(bar(B_SEMPTY), (g_s - 1) & 1u))) {
         tc_fence_after();
         const uint64_t kd = sdesc(stage_base(s), 0);
@@ -1507,6 +1523,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       mma_commit_mc(bar(B_KVEMPTY + s), 0x3);  // the stage is free in both CTAs once both P.V finished
       mma_commit(bar(B_PEMPTY + s));
+      if (lane == 0) *pv_issued = (int)g_p + 1;
       if (f_peer) {
         mma_commit_mc(bar(B_LOFREE), (uint16_t)(1u << peer));  // the other CTA may send its next lo
       }

@@ -9,13 +9,17 @@
 // latent row and the value its first 512 entries (MLA keeps effectively one KV
 // head -- same write-up, section "なぜテンソル並列だとKVキャッシュが二重に載るのか").
 //
+// Two kernels. The bf16 cache runs mla_split_kernel (further below: each CTA of
+// the pair scores its own half of each page's tokens and the pair exchanges row
+// maxima and P through distributed shared memory, which frees enough shared
+// memory for three pipeline stages). The 8-bit cache runs mla_partial_kernel,
+// described here, in which the two CTAs repeat the score.
+//
 // Layout of the work: the fp32 output accumulator of 128 heads x 512 dims is
 // 256 KB, all of one SM's tensor memory, so each work item runs on a 2-CTA
-// cluster and CTA r accumulates output dims [256 r, 256 r + 256). The two
-// CTAs share no data: each computes the full scores S = Q K^T of the tile
-// itself (the score MMA is repeated) because moving the 32 KB of fp32 scores
-// per tile between two SMs costs more: the SM-to-SM network measured ~9 B/clk
-// per direction on this part, against ~23 B/clk of HBM bandwidth per SM.
+// cluster and CTA r accumulates output dims [256 r, 256 r + 256). In
+// mla_partial_kernel the two CTAs share no data: each computes the full
+// scores S = Q K^T of the tile itself (the score MMA is repeated).
 // (A tcgen05 pair MMA does not avoid the repeat: the pair's two halves of an
 // operand sit at the same shared-memory offsets in both CTAs, so a token half
 // of the page for the score and a value-dim half for P.V cannot share bytes,
@@ -1121,27 +1125,38 @@ __global__ void __launch_bounds__(kFinishThreads) mla_finish_kernel(const char* 
 // 64-token page (tokens 32 r .. 32 r + 31): S_r = Q . K_r^T (M = 128, N = 32,
 // K = 576). The row maxima of the two halves and the two halves of P are
 // exchanged through distributed shared memory, and each CTA's P.V runs over
-// all 64 tokens. The score is no longer computed twice, and a CTA holds only
-// what it reads: its own 32 tokens in full (for its score) plus the other 32
-// tokens' rows of its own value dims (for P.V) -- 52 KB per page instead of
-// 72 KB -- so three stages fit where two did. Per page and CTA:
-//   1. the copies: its own tokens' value dims and dims 512-575 (private),
-//      its own tokens' other value dims, which the other CTA needs for P.V
-//      (one multicast copy into both CTAs, at the same slots), and the other
-//      CTA's multicast of its tokens' rows of this CTA's value dims
+// all 64 tokens. A CTA then holds only what it reads: its own 32 tokens in
+// full (for its score) plus the other 32 tokens' rows of its own value dims
+// (for P.V) -- 52 KB per page, 56 KB with its P_lo, instead of 72 KB -- so
+// three stages fit where two did, and each SM takes in 52 KB per page
+// instead of 72. (The score itself is barely cheaper: on this part a
+// tcgen05 MMA of M = 128, K = 16 takes ~37 cycles for any N up to 64, so 36
+// MMAs of N = 32 cost about what 36 of N = 64 do; the gain is the deeper
+// pipeline.) Per page and CTA:
+//   1. the copies (three TMA copies): its own tokens' other value dims, which
+//      the other CTA needs for P.V (one multicast copy into both CTAs, at
+//      the same slots), its own tokens' value dims, dims 512-575; plus the
+//      other CTA's multicast of its tokens' rows of this CTA's value dims
 //   2. S_r into TMEM (query dims 0-447 as the A operand in TMEM, 448-575 in
 //      shared memory)
-//   3. the row maximum of the own 32 tokens, sent to the other CTA; both then
-//      take the maximum of the two halves and run the same lazy rescale, so
-//      their running maxima stay equal without further talk
-//   4. P of the own tokens as two bf16 terms (hi, lo) into the slots that
-//      only the score read; hi is sent to the other CTA with one bulk copy,
-//      lo only when a tile carries a noticeable share of some row's weight
-//      (the other CTA is told by a flag, and its lo buffer is a single slot
-//      it releases after use)
+//   3. the row maximum of the own 32 tokens, sent to the other CTA (st.async
+//      stores that complete on its barrier); both then take the maximum of
+//      the two halves and run the same lazy rescale, so their running maxima
+//      stay equal without further talk
+//   4. P of the own tokens as two bf16 terms (hi, lo) into the slots only the
+//      score read; hi goes to the other CTA with one bulk copy, lo only when
+//      a tile carries a noticeable share of some row's weight (a flag tells
+//      the other CTA, whose lo buffer is a single slot it releases after use)
 //   5. O_r += P . V_r over both token halves
 // At the end of an output row group the two CTAs' row sums are exchanged the
-// same way. Every wait is bounded, as in mla_partial_kernel.
+// same way. The waits that other warps' progress ends suspend (try_wait):
+// eleven warps share four schedulers, and polling warps took issue slots
+// from the softmax warps (512-sequence step 14.4 -> 12.4 ms). Two are
+// polled: the producer's wait for a free stage and the score warp's, so that
+// the copy and the score leave at once. The score of tile g also waits until
+// the P.V of tile g - 2 is in the tensor pipe, which runs MMAs in issue
+// order: that P.V frees the stage the copy of tile g + 1 needs. Every wait is
+// bounded, as in mla_partial_kernel.
 namespace ts {
 constexpr int kStages = 3;
 constexpr int kHalf = 32;                          // tokens of a page per CTA

@@ -65,6 +65,32 @@ constexpr int kKBytes = 2 * kChunkBytes;   // K rows of a tile: dims 0-63 | 64-1
 constexpr int kStageBytes = 2 * kKBytes;   // K then V
 constexpr int kPBytes = kRows * 128;       // 128 rows x 64 tokens bf16 (one term)
 
+// Packed fp32 pairs (one instruction for two lanes of work) and a three-input
+// maximum, to thin the softmax warps' instruction stream.
+__device__ __forceinline__ unsigned long long f2pack(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(unsigned long long r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long fadd2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
@@ -462,12 +488,15 @@ __global__ void __launch_bounds__(TcCfg<NB>::kThreads, 1) gqa_tc_kernel(const __
         if (n_valid == kTile) {
 #pragma unroll
           for (int i = 0; i < 64; ++i) sc[i] = __uint_as_float(sv[i]);
-          float m8[8];
+          // a tree of three-input maxima: 64 -> 22 -> 8 -> 3 -> 1
+          float t22[22], u8[8];
 #pragma unroll
-          for (int j8 = 0; j8 < 8; ++j8)
-            m8[j8] = fmaxf(fmaxf(fmaxf(sc[8 * j8], sc[8 * j8 + 1]), fmaxf(sc[8 * j8 + 2], sc[8 * j8 + 3])),
-                           fmaxf(fmaxf(sc[8 * j8 + 4], sc[8 * j8 + 5]), fmaxf(sc[8 * j8 + 6], sc[8 * j8 + 7])));
-          mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+          for (int i = 0; i < 21; ++i) t22[i] = max3f(sc[3 * i], sc[3 * i + 1], sc[3 * i + 2]);
+          t22[21] = sc[63];
+#pragma unroll
+          for (int i = 0; i < 7; ++i) u8[i] = max3f(t22[3 * i], t22[3 * i + 1], t22[3 * i + 2]);
+          u8[7] = t22[21];
+          mx = max3f(max3f(u8[0], u8[1], u8[2]), max3f(u8[3], u8[4], u8[5]), fmaxf(u8[6], u8[7]));
           mx *= sl2;
         } else {
           // a partial tile (the last of a range, or cut by the row's token):
@@ -491,11 +520,24 @@ __global__ void __launch_bounds__(TcCfg<NB>::kThreads, 1) gqa_tc_kernel(const __
         {
           float ls[4] = {0.f, 0.f, 0.f, 0.f};
           if (n_valid == kTile) {
+            // scale and shift two scores per instruction; row sum in pairs
+            const unsigned long long s2 = f2pack(sl2, sl2), r2 = f2pack(-ref, -ref);
+            unsigned long long a0 = f2pack(0.f, 0.f), a1 = a0;
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-              sc[i] = ex2_ftz(fmaf(sc[i], sl2, -ref));
-              ls[i & 3] += sc[i];
+            for (int i = 0; i < 32; ++i) {
+              float x0, x1;
+              f2unpack(ffma2(f2pack(sc[2 * i], sc[2 * i + 1]), s2, r2), x0, x1);
+              sc[2 * i] = ex2_ftz(x0);
+              sc[2 * i + 1] = ex2_ftz(x1);
+              if (i & 1)
+                a1 = fadd2(a1, f2pack(sc[2 * i], sc[2 * i + 1]));
+              else
+                a0 = fadd2(a0, f2pack(sc[2 * i], sc[2 * i + 1]));
             }
+            float y0, y1;
+            f2unpack(fadd2(a0, a1), y0, y1);
+            ls[0] = y0;
+            ls[1] = y1;
           } else {
 #pragma unroll
             for (int i = 0; i < 64; ++i) {

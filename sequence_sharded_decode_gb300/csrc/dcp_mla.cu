@@ -809,23 +809,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // scale * max(s) (or * min(s) for a negative scale): one multiply.
         const int n_valid = phys < 0 ? 0 : min(kTile, g.hi - (g.lo + kTile * t));
         float raw_ext;
-        if (n_valid == kTile) {  // common case: no masking; a tree for ILP
-          float m8[8];
-          if (pos_scale) {
-#pragma unroll
-            for (int j8 = 0; j8 < 8; ++j8) {
-              const float* x = reinterpret_cast<const float*>(sv + 8 * j8);
-              m8[j8] = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])), fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
-            }
-            raw_ext = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-          } else {
-#pragma unroll
-            for (int j8 = 0; j8 < 8; ++j8) {
-              const float* x = reinterpret_cast<const float*>(sv + 8 * j8);
-              m8[j8] = fminf(fminf(fminf(x[0], x[1]), fminf(x[2], x[3])), fminf(fminf(x[4], x[5]), fminf(x[6], x[7])));
-            }
-            raw_ext = fminf(fminf(fminf(m8[0], m8[1]), fminf(m8[2], m8[3])), fminf(fminf(m8[4], m8[5]), fminf(m8[6], m8[7])));
-          }
+        if (n_valid == kTile) {  // common case: no masking; a tree of three-input extrema
+          raw_ext = pos_scale ? ext_tree<64, true>(sv) : ext_tree<64, false>(sv);
         } else {
           raw_ext = pos_scale ? -INFINITY : INFINITY;
 #pragma unroll
@@ -850,15 +835,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         float sc[32];
         float lsum;
         {
+          // two scores scaled and shifted per instruction; the row sum in pairs
           const int t0 = 32 * e;
-          float ls[4] = {0.f, 0.f, 0.f, 0.f};
+          const unsigned long long s2 = f2pack(p.sl2, p.sl2), r2 = f2pack(-ref, -ref);
+          unsigned long long a0 = f2pack(0.f, 0.f), a1 = a0;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float x = fmaf(__uint_as_float(sv[i]), p.sl2, -ref);
-            sc[i] = (t0 + i < n_valid) ? ex2_ftz(x) : 0.f;
-            ls[i & 3] += sc[i];
+          for (int i = 0; i < 16; ++i) {
+            float x0, x1;
+            f2unpack(ffma2(f2pack(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), s2, r2), x0, x1);
+            sc[2 * i] = (t0 + 2 * i < n_valid) ? ex2_ftz(x0) : 0.f;
+            sc[2 * i + 1] = (t0 + 2 * i + 1 < n_valid) ? ex2_ftz(x1) : 0.f;
+            if (i & 1)
+              a1 = fadd2(a1, f2pack(sc[2 * i], sc[2 * i + 1]));
+            else
+              a0 = fadd2(a0, f2pack(sc[2 * i], sc[2 * i + 1]));
           }
-          lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+          float y0, y1;
+          f2unpack(fadd2(a0, a1), y0, y1);
+          lsum = y0 + y1;
         }
         l_half = l_half * alpha + lsum;
         m_run = m_new;
@@ -1626,15 +1620,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bar_arrive(bar(B_SEMPTY));
         // 2. the own maximum (of scale * s, as scale * max or min of s), sent
         float raw_ext = pos_scale ? -INFINITY : INFINITY;
-        if (n_valid - own0 >= kHalf) {  // common case: no masking; a tree for ILP
-          float m4[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float* x = reinterpret_cast<const float*>(sv + 8 * q);
-            m4[q] = pos_scale ? fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])), fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])))
-                              : fminf(fminf(fminf(x[0], x[1]), fminf(x[2], x[3])), fminf(fminf(x[4], x[5]), fminf(x[6], x[7])));
-          }
-          raw_ext = pos_scale ? fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) : fminf(fminf(m4[0], m4[1]), fminf(m4[2], m4[3]));
+        if (n_valid - own0 >= kHalf) {  // common case: no masking; a tree of three-input extrema
+          raw_ext = pos_scale ? ext_tree<32, true>(sv) : ext_tree<32, false>(sv);
         } else {
 #pragma unroll
           for (int i = 0; i < kHalf; ++i) {
@@ -1671,15 +1658,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) mine[i] = sv[16 + i];
           }
-          float ls[4] = {0.f, 0.f, 0.f, 0.f};
+          // two scores scaled and shifted per instruction; the row sum in pairs
+          const int tok0 = own0 + 16 * e;
+          const unsigned long long s2 = f2pack(p.sl2, p.sl2), r2 = f2pack(-ref, -ref);
+          unsigned long long a0 = f2pack(0.f, 0.f), a1 = a0;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int tok = own0 + 16 * e + i;
-            const float x = fmaf(__uint_as_float(mine[i]), p.sl2, -ref);
-            sc[i] = tok < n_valid ? ex2_ftz(x) : 0.f;
-            ls[i & 3] += sc[i];
+          for (int i = 0; i < 8; ++i) {
+            float x0, x1;
+            f2unpack(ffma2(f2pack(__uint_as_float(mine[2 * i]), __uint_as_float(mine[2 * i + 1])), s2, r2), x0, x1);
+            sc[2 * i] = tok0 + 2 * i < n_valid ? ex2_ftz(x0) : 0.f;
+            sc[2 * i + 1] = tok0 + 2 * i + 1 < n_valid ? ex2_ftz(x1) : 0.f;
+            if (i & 1)
+              a1 = fadd2(a1, f2pack(sc[2 * i], sc[2 * i + 1]));
+            else
+              a0 = fadd2(a0, f2pack(sc[2 * i], sc[2 * i + 1]));
           }
-          lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+          float y0, y1;
+          f2unpack(fadd2(a0, a1), y0, y1);
+          lsum = y0 + y1;
         }
         l_half = l_half * alpha + lsum;
         m_run = m_new;

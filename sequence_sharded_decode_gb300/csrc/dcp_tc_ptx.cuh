@@ -200,6 +200,62 @@ __device__ __forceinline__ float ex2_ftz(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
 }
+// Packed fp32 pairs (one instruction for two lanes of work) and three-input
+// extrema, to thin the softmax warps' instruction streams.
+__device__ __forceinline__ unsigned long long f2pack(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(unsigned long long r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long fadd2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// maximum (MAX) or minimum of 32 or 64 fp32 bit patterns, as a tree of
+// three-input extrema (17 / 32 instructions instead of 31 / 63)
+template <int N, bool MAX>
+__device__ __forceinline__ float ext_tree(const uint32_t* v) {
+  static_assert(N == 32 || N == 64, "32 or 64 values");
+  auto e3 = [](float a, float b, float c) { return MAX ? max3f(a, b, c) : min3f(a, b, c); };
+  auto e2 = [](float a, float b) { return MAX ? fmaxf(a, b) : fminf(a, b); };
+  auto f = [&](int i) { return __uint_as_float(v[i]); };
+  if constexpr (N == 64) {
+    float t[22], u[8];
+#pragma unroll
+    for (int i = 0; i < 21; ++i) t[i] = e3(f(3 * i), f(3 * i + 1), f(3 * i + 2));
+    t[21] = f(63);
+#pragma unroll
+    for (int i = 0; i < 7; ++i) u[i] = e3(t[3 * i], t[3 * i + 1], t[3 * i + 2]);
+    u[7] = t[21];
+    return e3(e3(u[0], u[1], u[2]), e3(u[3], u[4], u[5]), e2(u[6], u[7]));
+  } else {
+    float t[11];
+#pragma unroll
+    for (int i = 0; i < 10; ++i) t[i] = e3(f(3 * i), f(3 * i + 1), f(3 * i + 2));
+    t[10] = e2(f(30), f(31));
+    return e2(e3(e3(t[0], t[1], t[2]), e3(t[3], t[4], t[5]), e3(t[6], t[7], t[8])), e2(t[9], t[10]));
+  }
+}
+
 // bf16 pair (x0 in the low half), round to nearest even
 __device__ __forceinline__ uint32_t pack_bf16(float x0, float x1) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);

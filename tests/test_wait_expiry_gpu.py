@@ -1,5 +1,6 @@
-"""The bounded waits of the tcgen05 kernels (MLA pair kernel, many-row GQA
-kernel) give up after a fixed number of polls, raise DCP_DEVERR_TIMEOUT,
+"""The bounded waits of the tcgen05 kernels (the MLA token-split kernel of
+the bf16 cache, the MLA kernel of the 8-bit cache, the many-row GQA kernel)
+give up after a fixed number of polls, raise DCP_DEVERR_TIMEOUT,
 stop every role, drain the copies and MMAs they issued, free tensor memory
 and return. This builds a second copy of the library whose poll limit is 1
 (-DDCP_SPIN_LIMIT=1), so that each of those kernels aborts at its first wait
@@ -31,6 +32,7 @@ from sequence_sharded_decode_gb300.state import DecodeState
 
 variant, normal = sys.argv[2], sys.argv[3]
 cases = [(configs.get("mla_decode").with_(batch=2, ctx_kind="fixed", ctx_fixed=900, shards=3), 1),
+         (configs.get("mla_decode").with_(batch=2, ctx_kind="fixed", ctx_fixed=900, shards=3, kv_dtype="fp8"), 1),
          (configs.get("gqa_mid").with_(batch=1, ctx_fixed=700, shards=2), 16)]
 for wl, q_len in cases:
     dcp._lib, dcp._LIB_PATH = None, variant

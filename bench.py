@@ -470,7 +470,9 @@ def run_ours(args, wl):
                            else "dcp_kv_append, dcp_decode_partial_all, dcp_merge"),
             "e2e": {"value": round(whole_job_gbs(world, step_bytes, e2e_ms), 2), "unit": "GB/s",
                     "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": (3 if one_call_mla else 4 if fused else 5) * K,
+            # per step: append, plan, attention and, one call: the finishing
+            # kernel (MLA) or the one-pass merge (GQA); two calls: combine and merge
+            "gpu_launches": (4 if (one_call_mla or fused) else 5) * K,
             "clocks": clocks,
         }
         if args.q_len > 1:

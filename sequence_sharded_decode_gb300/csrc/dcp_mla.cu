@@ -1289,6 +1289,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   volatile int* pflag = reinterpret_cast<volatile int*>(smem + kOffMisc + 16);     // [stage]: the other CTA's lo
   volatile int* lo_votes = reinterpret_cast<volatile int*>(smem + kOffMisc + 32);  // [stage][softmax warp]
   volatile int* pv_issued = reinterpret_cast<volatile int*>(smem + kOffMisc + 128);  // P.V tiles issued
+  // each tile's physical block as the producer read it (ring of 16), so that
+  // the softmax warps need no block-table load of their own
+  volatile int* phys_written = reinterpret_cast<volatile int*>(smem + kOffMisc + 136);
+  volatile int* phys_ring = reinterpret_cast<volatile int*>(smem + kOffMisc + 160);
 
   if (threadIdx.x == 0) {
     bar_init(bar(B_QFULL), kSoftmaxThreads);
@@ -1314,6 +1318,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     *abort_flag = 0;
     *pv_issued = 0;
+    *phys_written = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == kMmaWarp) {
@@ -1379,6 +1384,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (use > 0 && !poll_bar(bar(B_KVEMPTY + s), (use - 1) & 1u, abort_flag, p.err)) {
             ok = false;
           } else {
+            phys_ring[fills & 15u] = phys;
+            __threadfence_block();
+            *phys_written = (int)fills + 1;
             if (phys < 0 && rank == 0) raise_flag(p.err, DCP_DEVERR_BLOCK_RANGE);
             // rows of this CTA's tokens (an unusable entry reads zeros above row 0)
             const int row = (phys < 0 ? -kTile : phys * kTile) + kHalf * (int)rank;
@@ -1606,7 +1614,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t gi = gt + j, s = gi % kStages, ph = (gi / kStages) & 1u;
         const uint32_t st = stage_base(s);
         const int t = g.t0 + j;
-        const int phys = tile_block(p, g, t);
+        int phys = -2;  // the tile's block, as the producer published it
+        for (uint32_t it = 0; it < kSpinLimit; ++it) {
+          if (*phys_written > (int)gi) { phys = phys_ring[gi & 15u]; break; }
+          if ((it & 63u) == 63u && *abort_flag) break;
+        }
+        if (phys == -2) {
+          if (!*abort_flag) { *abort_flag = 1; raise_flag(p.err, DCP_DEVERR_TIMEOUT); }
+          ok = false;
+          break;
+        }
         const int n_valid = phys < 0 ? 0 : min(kTile, g.hi - (g.lo + kTile * t));
         const int own0 = kHalf * (int)rank;  // first own token of the tile
         // 1. the own 32 scores (polled: a suspended wait wakes late)

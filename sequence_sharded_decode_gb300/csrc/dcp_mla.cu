@@ -1172,7 +1172,7 @@ constexpr int kOffQ = kOffKv + kStages * kStage;
 constexpr int kOffLoPeer = kOffQ + kQChunks * kQChunkBytes;  // the other CTA's P_lo half
 constexpr int kOffBar = kOffLoPeer + kPHalf;
 constexpr int kNumBars = 40;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;   // TMEM slot, abort, merge flag, P flags, lo votes
+constexpr int kOffMisc = kOffBar + kNumBars * 8;   // TMEM slot, abort, merge flag, P flags, lo votes, counters, block ring
 constexpr int kOffMx = kOffMisc + 256;             // [stage][head]: the other CTA's row maxima
 constexpr int kOffLx = kOffMx + kStages * kHeads * 4;  // [2][head]: row-sum halves of this CTA
 constexpr int kOffLp = kOffLx + 2 * kHeads * 4;        // [2][head]: the other CTA's row sums

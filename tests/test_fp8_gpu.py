@@ -26,6 +26,7 @@ CASES = [
     ("gqa_mid", dict(batch=2, q_heads=64, kv_heads=2, ctx_fixed=999, shards=3, **F8)),   # two head groups
     ("gqa_mid", dict(batch=2, q_heads=8, kv_heads=8, ctx_fixed=555, shards=4, **F8)),    # g=1
     ("gqa_mid", dict(batch=2, q_heads=12, kv_heads=4, ctx_fixed=700, shards=2, block_size=32, **F8)),
+    ("gqa_mid", dict(batch=2, ctx_fixed=1000, shards=3, block_size=48, **F8)),  # block size not a power of two
     ("gqa_tiny", dict(batch=2, ctx_fixed=1500, shards=4, block_size=64, scale=1.0, **F8)),  # peaky softmax
     ("gqa_mid", dict(batch=1, ctx_fixed=0, shards=4, **F8)),             # one token only
     ("gqa_mid", dict(batch=3, ctx_fixed=4000, shards=4, needles=3, **F8)),

@@ -377,6 +377,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 8);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* lo_flags = reinterpret_cast<volatile int*>(smem + kOffMisc + 16);  // [stage][softmax warp]
+  // F8: each page's physical block as the producer read it (ring of 4,
+  // written before the page's copy barrier is arrived on), so that the
+  // softmax warps make no block-table load of their own
+  volatile int* phys_ring = reinterpret_cast<volatile int*>(smem + kOffMisc + 80);
 
   if (threadIdx.x == 0) {
     bar_init(bar(BQ_FULL), kSoftmaxThreads);  // every softmax thread's share of Q[:, 0:384] in TMEM
@@ -468,6 +472,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if constexpr (F8) {
               // one bulk copy of the page's codes (an unusable table entry
               // copies nothing: the widening writes zeros for it)
+              phys_ring[fills & 3u] = phys;
               if (phys < 0) {
                 bar_arrive(bar(BKV_FULL + s));
               } else {
@@ -752,17 +757,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int j = 0; j < nt; ++j) {
         const uint32_t gi = gt + j, s = gi % kStages;
         const int t = g.t0 + j;
-        const int phys = tile_block(p, g, t);  // its latency hides behind the score wait
+        int phys;  // bf16: its latency hides behind the score wait; F8: from the ring
         if constexpr (F8) {
           if (gi == 0) {  // 0. the run's first page is widened before its score
-            const int n_rows = phys < 0 ? 0 : min(kTile, g.hi - (g.lo + kTile * t));
             if (!wait_warp(bar(BKV_FULL), 0u, abort_flag, p.err, false)) { ok = false; break; }
+            phys = phys_ring[0];
+            const int n_rows = phys < 0 ? 0 : min(kTile, g.hi - (g.lo + kTile * t));
             widen(0u, n_rows, 0);
             widen(0u, n_rows, 1);
             asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
             bar_arrive(bar(BF_FULL));
             bar_arrive(bar(BKV_EMPTY));  // the codes' stage may be refilled
+          } else {
+            phys = phys_ring[gi & 3u];  // written before the page's copy barrier, which was waited for
           }
+        } else {
+          phys = tile_block(p, g, t);
         }
         // 1. scores of the tile: all 64 for the maximum, this warp's 32 for P
         if (!wait_warp(bar(BS_FULL), gi & 1u, abort_flag, p.err, false)) { ok = false; break; }
@@ -791,9 +801,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           if (tn >= 0) {
             const uint32_t G = gi + 1;
-            const int physn = tile_block(p, gn, tn);
-            const int n_rows = physn < 0 ? 0 : min(kTile, gn.hi - (gn.lo + kTile * tn));
             if (!wait_warp(bar(BKV_FULL), G & 1u, abort_flag, p.err, false)) { ok = false; break; }
+            const int physn = phys_ring[G & 3u];
+            const int n_rows = physn < 0 ? 0 : min(kTile, gn.hi - (gn.lo + kTile * tn));
             widen(G, n_rows, 0);
             if (G >= 2 && !wait_warp(bar(BP_EMPTY + (G & 1u)), ((G - 2) >> 1) & 1u, abort_flag, p.err, false)) {
               ok = false;

@@ -84,11 +84,6 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
   return v;
 }
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(v) : "r"(addr));
-  return v;
-}
 
 // bf16 pair -> fp16 pair
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
@@ -521,14 +516,21 @@ __global__ void __launch_bounds__(GqaCfg<D>::kThreads, (GqaCfg<D, F8, T>::kMinCt
       }
       // O += P V
       if constexpr (F8) {
-        // a lane's tokens 4t4 .. 4t4+3 of value row (dim) 8nd + gr: one word
+        // a lane's tokens 4t4 .. 4t4+3 of value row (dim) 8nd + gr: one word.
+        // The tile's 16-byte value rows are ldmatrix's 8 x 8 b16 matrices
+        // (lane 4 gr + t4 receives word t4 of row gr), so one x4 load brings
+        // the words of four consecutive nd (lane L addresses row 32 q + L)
 #pragma unroll
-        for (int nd = 0; nd < D / 8; ++nd) {
-          const uint32_t w = lds32(vb + (nd * 8 + gr) * 16 + t4 * 4);
-          uint32_t b0, b1;
-          e4m3x4_to_f16x4(w, b0, b1);
-          mma16816_f16(o[nd], pa, b0, b1);
-          if (any_lo) mma16816_f16(o[nd], pl, b0, b1);
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t w[4];
+          ldsm_x4(vb + (32 * q + lane) * 16, w[0], w[1], w[2], w[3]);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            uint32_t b0, b1;
+            e4m3x4_to_f16x4(w[m], b0, b1);
+            mma16816_f16(o[4 * q + m], pa, b0, b1);
+            if (any_lo) mma16816_f16(o[4 * q + m], pl, b0, b1);
+          }
         }
       } else {
         const int mi = lane >> 3;

@@ -395,10 +395,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kRing; ++s) {
       bar_init(bar(BKV_FULL + s), 1);
       // bf16: the P.V of both CTAs (the page lands in both); F8: the widening of the codes
-      bar_init(bar(BKV_EMPTY + s), F8 ? kSoftmaxThreads : 2);
+      bar_init(bar(BKV_EMPTY + s), F8 ? kSoftmaxThreads + 1 : 2);  // F8: + the producer's rope box
     }
     for (int q4 = 0; q4 < 4; ++q4) bar_init(bar(BXCH + q4), 64);  // the two warps of a lane quadrant
-    bar_init(bar(BF_FULL), kSoftmaxThreads);
+    bar_init(bar(BF_FULL), kSoftmaxThreads + 1);  // the softmax threads and the producer (rope box)
     bar_init(bar(BPC), kSoftmaxThreads);
     bar_init(bar(BGO), 1);
     *abort_flag = 0;
@@ -496,6 +496,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) { stop = true; break; }
+        if constexpr (F8) {
+          // F8: the producer widens box 8 (dims 512-575) of this page into
+          // the score-only region itself, once the codes have landed and the
+          // previous page's score has finished with that region, so that the
+          // softmax warps widen eight boxes instead of nine (same layout and
+          // zero rows as theirs: 64 rows x four 16-code pieces, 8 per lane)
+          const uint32_t G = fills;
+          const int n_rows = phys < 0 ? 0 : min(kTile, g.hi - (g.lo + kTile * (g.t0 + j)));
+          if (!wait_warp(bar(BKV_FULL), G & 1u, abort_flag, p.err, false) ||
+              (G > 0 && !wait_warp(bar(BS_FULL), (G - 1) & 1u, abort_flag, p.err, false))) {
+            stop = true;
+            break;
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int w = lane + 32 * i, r = w >> 2, q4 = w & 3;
+            const uint32_t sw = (uint32_t)(r & 7), ch = 2u * (uint32_t)q4;
+            const uint32_t dst = sbase + kOffSh + 4 * kKvChunkBytes + r * 128;
+            uint32_t wv[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+            if (r < n_rows) {
+              const uint4 c = lds128_u32(sbase + kOffKv + r * kDk + 512 + 16 * q4);
+              e4m3x4_to_f16x4(c.x, wv[0], wv[1]);
+              e4m3x4_to_f16x4(c.y, wv[2], wv[3]);
+              e4m3x4_to_f16x4(c.z, wv[4], wv[5]);
+              e4m3x4_to_f16x4(c.w, wv[6], wv[7]);
+            }
+            st_shared_v4(dst + ((ch ^ sw) << 4), wv[0], wv[1], wv[2], wv[3]);
+            st_shared_v4(dst + (((ch + 1) ^ sw) << 4), wv[4], wv[5], wv[6], wv[7]);
+          }
+          asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            bar_arrive(bar(BF_FULL));
+            bar_arrive(bar(BKV_EMPTY));  // done with the codes
+          }
+        }
         ++fills;
       }
     }
@@ -683,16 +719,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t sw = (uint32_t)(r & 7), ch = 2u * (uint32_t)q4;
       const uint32_t c0 = (ch ^ sw) << 4, c1 = ((ch + 1) ^ sw) << 4;
       const bool live = r < n_rows;
-      // part 0: the other CTA's value boxes 4 (1 - rank) + i (i < 4), then
-      // box 8 (i = 4), into slots i of the shared region; part 1: this CTA's
-      // value boxes 4 rank + i into the value slot of G's parity
-      const int n = part == 0 ? 5 : 4;
+      // part 0: the other CTA's value boxes 4 (1 - rank) + i (i < 4) into
+      // slots i of the shared region (box 8, slot 4, is the producer's);
+      // part 1: this CTA's value boxes 4 rank + i into the value slot of
+      // G's parity
       const uint32_t dst0 = (part == 0 ? sbase + kOffSh : sbase + kOffV + (G & 1u) * 4 * kKvChunkBytes) + r * 128;
       const int box0 = part == 0 ? 4 * (1 - (int)rank) : 4 * (int)rank;
 #pragma unroll
-      for (int i = 0; i < 5; ++i) {
-        if (i >= n) break;
-        const int box = (part == 0 && i == 4) ? 8 : box0 + i;
+      for (int i = 0; i < 4; ++i) {
+        const int box = box0 + i;
         const uint32_t dst = dst0 + i * kKvChunkBytes;
         uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
         if (live) {

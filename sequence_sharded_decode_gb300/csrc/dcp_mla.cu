@@ -124,11 +124,12 @@ constexpr int kCodesPage = kTile * kDk;          // 8-bit cache: one page of E4M
 // CTA reads only in the score MMA: one P buffer per stage, so writing P never
 // waits for the previous tile's P.V.
 // The 8-bit cache (F8) copies pages of E4M3 codes instead (36 KB, one bulk
-// copy each, no multicast) into a one-page codes stage, and the softmax warps
-// widen each page, exactly, into fp16 boxes laid out like the bf16 ones: the
-// five boxes only the score reads (the other CTA's value dims and dims
-// 512-575) into one shared region, this CTA's four value boxes into one of
-// two value slots by page parity. P has a buffer of its own. So page g + 1
+// copy each, no multicast) into a one-page codes stage, and each page is
+// widened, exactly, into fp16 boxes laid out like the bf16 ones: the five
+// boxes only the score reads (the other CTA's value dims, by the softmax
+// warps, and dims 512-575, by the producer warp) into one shared region,
+// this CTA's four value boxes (softmax warps) into one of two value slots by
+// page parity. P has a buffer of its own. So page g + 1
 // can be widened as soon as page g's scores are read -- its score then runs
 // while page g's softmax does -- the value slot it needs having been freed by
 // the P.V of page g - 1.
